@@ -1,0 +1,370 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Each group targets one plausible mistake: a wrong rounding direction or tie rule,
+an off-by-one exponent, a transposed block index, a dropped fragment element, a
+write outside the fragment, a lost sign.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from mxfp8_master_weight_gb300 import workloads as wl
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden_rows(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line and not line.startswith("scale"):
+                rows.append(line.split()[:2])
+    return rows
+
+
+# ------------------------------------------------------------------ E4M3
+
+def _e4m3_table():
+    """The 127 finite non-negative E4M3 values, built from the format definition."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals.append(m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+def _e4m3_brute(v):
+    """Nearest table entry by exhaustive search; ties to the even code; saturate."""
+    table = _e4m3_table()
+    out = np.empty(v.shape, np.uint8)
+    for k, x in enumerate(v):
+        if np.isnan(x):
+            out[k] = 0x7F
+            continue
+        a = min(abs(x), 448.0)
+        d = np.abs(table - a)
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        out[k] = code | (0x80 if np.signbit(x) else 0)
+    return out
+
+
+def test_e4m3_golden(oracle_mod):
+    for val, code in _golden_rows("e4m3_points.txt"):
+        got = int(oracle_mod.e4m3_encode(np.array([float(val)]))[0])
+        assert got == int(code, 16), (val, hex(got), code)
+
+
+def test_e4m3_vs_brute_force(oracle_mod):
+    table = _e4m3_table()
+    mids = (table[1:] + table[:-1]) / 2
+    rng = np.random.default_rng(1)
+    pts = np.concatenate([
+        table, mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9),
+        2.0 ** rng.uniform(-14, 10, 4000), [0.0, 448.0, 447.99, 464.0, 465.0, 1e6, np.inf],
+    ])
+    pts = np.concatenate([pts, -pts, [np.nan]])
+    assert np.array_equal(oracle_mod.e4m3_encode(pts), _e4m3_brute(pts))
+
+
+def test_e4m3_vs_torch_float8(oracle_mod):
+    """Library cross-check: torch's CPU float8_e4m3fn conversion after clamping to +-448."""
+    rng = np.random.default_rng(2)
+    v = (rng.standard_normal(200000) * 2.0 ** rng.uniform(-12, 10, 200000)).astype(np.float32)
+    v[:5] = [0.0, -0.0, 448.0, -460.0, 1e-30]
+    ref = torch.from_numpy(v).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = oracle_mod.e4m3_encode(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_decode_roundtrip(oracle_mod):
+    codes = np.array([c for c in range(256) if c & 0x7F != 0x7F], np.uint8)
+    vals = oracle_mod.e4m3_decode(codes)
+    assert np.array_equal(oracle_mod.e4m3_encode(vals), codes)
+
+
+# ------------------------------------------------------------------ BF16
+
+def _bf16_neighbour_search(x):
+    """Nearest of the two BF16 values bracketing x (truncation and its successor), ties to even."""
+    b = x.view(np.uint32)
+    lo = b & np.uint32(0xFFFF0000)
+    hi = lo + np.uint32(0x10000)  # next magnitude up (same sign)
+    vlo = lo.view(np.float32).astype(np.float64)
+    vhi = hi.view(np.float32).astype(np.float64)
+    vx = x.astype(np.float64)
+    dlo, dhi = np.abs(vx - vlo), np.abs(vhi - vx)
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (((lo >> 16) & 1) == 1))
+    return np.where(pick_hi, hi >> 16, lo >> 16).astype(np.uint16)
+
+
+def test_bf16_vs_torch_and_neighbours(oracle_mod):
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 2 ** 32, 2_000_000, dtype=np.uint64).astype(np.uint32)
+    special = np.array([0x00000000, 0x80000000, 0x00000001, 0x007FFFFF, 0x00800000, 0x3F808000,
+                        0x3F818000, 0x7F7FFFFF, 0x7F7F8000, 0x7F7F7FFF, 0xFF7FFFFF, 0x7F800000,
+                        0xFF800000, 0x00008000, 0x00018000], np.uint32)
+    bits = np.concatenate([bits, special])
+    x = bits.view(np.float32)
+    finite = np.isfinite(x)
+    got = oracle_mod.bf16_rne_bits(x)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(x)
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all((got[nan] & 0x7F80) == 0x7F80) and np.all((got[nan] & 0x7F) != 0)
+    fin_no_overflow = finite & (np.abs(x) < np.float32(3.3e38))
+    assert np.array_equal(got[fin_no_overflow], _bf16_neighbour_search(x[fin_no_overflow]))
+
+
+# ------------------------------------------------------------------ E8M0
+
+def _e8m0_brute(a):
+    """Largest p with 2^p <= a by scanning powers of two; then clamp(p - 8) + 127."""
+    powers = 2.0 ** np.arange(-160, 130, dtype=np.float64)
+    out = np.empty(a.shape, np.uint8)
+    for k, x in enumerate(a):
+        if not np.isfinite(x):
+            out[k] = 0xFF
+        elif x == 0:
+            out[k] = 0
+        else:
+            p = int(np.arange(-160, 130)[np.flatnonzero(powers <= x)[-1]])
+            out[k] = min(max(p - 8, -127), 127) + 127
+    return out
+
+
+def test_e8m0_golden(oracle_mod):
+    for val, byte in _golden_rows("e8m0_points.txt"):
+        assert int(oracle_mod.e8m0_from_amax(np.array([float(val)]))[0]) == int(byte), val
+
+
+def test_e8m0_all_bf16_patterns(oracle_mod):
+    bits = np.arange(0, 0x8000, dtype=np.uint32) << 16
+    a = bits.view(np.float32).astype(np.float64)
+    assert np.array_equal(oracle_mod.e8m0_from_amax(a), _e8m0_brute(a))
+
+
+def test_e8m0_random_f32_and_range_invariant(oracle_mod):
+    rng = np.random.default_rng(4)
+    bits = rng.integers(0, 0x7F800000, 20000, dtype=np.uint32)
+    a = bits.view(np.float32).astype(np.float64)
+    got = oracle_mod.e8m0_from_amax(a)
+    assert np.array_equal(got, _e8m0_brute(a))
+    # unclamped range: the scaled block maximum lands in [256, 512)
+    inner = (got > 0) & (got < 254)
+    scaled = a[inner] * 2.0 ** (127 - got[inner].astype(np.float64))
+    assert np.all((scaled >= 256) & (scaled < 512))
+
+
+# ------------------------------------------------------------------ worked block
+
+def test_worked_block(oracle_mod):
+    rows = _golden_rows("worked_block.txt")
+    vals = np.zeros(32, np.float32)
+    codes = np.zeros(32, np.uint8)
+    for k, (v, c) in enumerate(rows):
+        vals[k] = np.float32(float(v))
+        codes[k] = int(c, 16)
+    amax_r, _, scale_r, _, q_r, _ = oracle_mod.full_cast(vals, 1, 32, colwise=False)
+    assert amax_r[0, 0] == np.float32(3.0)
+    assert scale_r[0, 0] == 120
+    assert np.array_equal(q_r, codes)
+
+
+# ------------------------------------------------------------------ amax geometry
+
+def _amax_brute(x, rows, cols, start, length):
+    """Block maxima by enumerating members of each block explicitly (dicts, no index algebra)."""
+    r, c = {}, {}
+    for k in range(start, start + length):
+        i, j = divmod(k, cols)
+        a = abs(float(x[k]))
+        r[(i, j // 32)] = max(r.get((i, j // 32), 0.0), a)
+        c[(i // 32, j)] = max(c.get((i // 32, j), 0.0), a)
+    return r, c
+
+
+@pytest.mark.parametrize("rows,cols", [(40, 7), (33, 65), (64, 96), (5, 100)])
+def test_partial_amax_brute_force(oracle_mod, rows, cols):
+    rng = np.random.default_rng(rows * 1000 + cols)
+    n = rows * cols
+    x = wl.normal_f32(rng, n)
+    pairs = [(0, n), (0, 0), (n, 0), (n - 1, 1), (0, 1), (17, n // 4)]
+    pairs += [(int(s), int(rng.integers(0, n - s + 1))) for s in rng.integers(0, n, 60)]
+    nbr, nbc = (cols + 31) // 32, (rows + 31) // 32
+    for start, length in pairs:
+        sentinel = np.float32(-7.0)
+        ar = np.full((rows, nbr + 2), sentinel, np.float32)  # padded leading dimension
+        ac = np.full((nbc, cols + 3), sentinel, np.float32)
+        oracle_mod.partial_amax(x[start:start + length], rows, cols, start, ar, ac)
+        er, ec = _amax_brute(x, rows, cols, start, length)
+        exp_r = np.full_like(ar, sentinel)
+        exp_c = np.full_like(ac, sentinel)
+        for (i, b), v in er.items():
+            exp_r[i, b] = v
+        for (cb, j), v in ec.items():
+            exp_c[cb, j] = v
+        assert np.array_equal(ar, exp_r), (start, length)
+        assert np.array_equal(ac, exp_c), (start, length)
+
+
+def test_amax_permutation_invariance(oracle_mod):
+    rng = np.random.default_rng(5)
+    x = wl.normal_f32(rng, 64 * 64).reshape(64, 64)
+    y = x.copy()
+    for i in range(64):  # permute inside each 1x32 row block
+        y[i, :32] = y[i, rng.permutation(32)]
+        y[i, 32:] = y[i, 32 + rng.permutation(32)]
+    a = oracle_mod.full_cast(x.reshape(-1), 64, 64)
+    b = oracle_mod.full_cast(y.reshape(-1), 64, 64)
+    assert np.array_equal(a[0], b[0])
+
+
+def test_amax_bf16_input_and_nan(oracle_mod):
+    x = np.array([1.0, -3.5, 0.25, np.nan] + [0.0] * 28, np.float32)
+    xb = wl.truncate_to_bf16_bits(x)
+    ar = np.zeros((1, 1), np.uint16)
+    oracle_mod.partial_amax(xb[:3], 1, 32, 0, ar, None)
+    assert ar[0, 0] == wl.truncate_to_bf16_bits(np.array([3.5], np.float32))[0]
+    oracle_mod.partial_amax(xb, 1, 32, 0, ar, None)
+    assert np.isnan(wl.bf16_bits_to_f32(ar)[0, 0])
+
+
+# ------------------------------------------------------------------ reduce
+
+def test_max_reduce(oracle_mod):
+    rng = np.random.default_rng(6)
+    s = np.abs(wl.normal_f32(rng, (4, 1000)))
+    s[1, 10] = 0.0
+    assert np.array_equal(oracle_mod.max_reduce(s), s.max(axis=0))
+    sb = wl.truncate_to_bf16_bits(s)
+    assert np.array_equal(oracle_mod.max_reduce(sb),
+                          wl.truncate_to_bf16_bits(s).view(np.uint16).max(axis=0))
+
+
+# ------------------------------------------------------------------ cast
+
+def _cast_brute(x_bf16_vals, scale_bytes):
+    v = x_bf16_vals.astype(np.float64) * 2.0 ** (127 - scale_bytes.astype(np.float64))
+    return _e4m3_brute(v)
+
+
+def test_cast_vs_brute_force_and_error_bound(oracle_mod):
+    rows, cols = 64, 96
+    rng = np.random.default_rng(7)
+    x = wl.normal_f32(rng, rows * cols)
+    x[::97] *= 100.0
+    amax_r, amax_c, s_r, s_c, q_r, q_c = oracle_mod.full_cast(x, rows, cols)
+    y = wl.bf16_bits_to_f32(oracle_mod.bf16_rne_bits(x)).reshape(rows, cols)
+    ii, jj = np.meshgrid(np.arange(rows), np.arange(cols), indexing="ij")
+    sr = s_r[ii, jj // 32]
+    sc = s_c[ii // 32, jj]
+    assert np.array_equal(q_r.reshape(rows, cols).ravel(), _cast_brute(y.ravel(), sr.ravel()))
+    assert np.array_equal(q_c.reshape(rows, cols).ravel(), _cast_brute(y.ravel(), sc.ravel()))
+    # error bound: |decode(q) * 2^e - y| <= half an E4M3 spacing at |v| (unsaturated)
+    e = sr.astype(np.float64) - 127
+    v = y.astype(np.float64) * 2.0 ** -e
+    dec = oracle_mod.e4m3_decode(q_r.reshape(rows, cols))
+    spacing = np.where(np.abs(v) < 2.0 ** -6, 2.0 ** -9,
+                       2.0 ** (np.floor(np.log2(np.maximum(np.abs(v), 1e-300))) - 3))
+    unsat = np.abs(v) < 448
+    assert np.all(np.abs(dec - v)[unsat] <= spacing[unsat] / 2)
+
+
+def test_row_only_equals_rowwise_half(oracle_mod):
+    rng = np.random.default_rng(8)
+    x = wl.normal_f32(rng, 96 * 64)
+    bi = oracle_mod.full_cast(x, 96, 64, colwise=True)
+    ro = oracle_mod.full_cast(x, 96, 64, colwise=False)
+    for k in (0, 2, 4):
+        assert np.array_equal(bi[k], ro[k])
+    assert ro[1] is None and ro[3] is None and ro[5] is None
+
+
+def _sharded_flow(oracle_mod, x, rows, cols, cuts, colwise=True, out_fragment=False):
+    """Per-shard amax into separate zeroed slots, one max-reduce, scales, per-shard casts."""
+    rdim, cdim = oracle_mod.block_dims(rows, cols)
+    bounds = list(zip(cuts[:-1], cuts[1:]))
+    slots_r = np.zeros((len(bounds),) + rdim, x.dtype)
+    slots_c = np.zeros((len(bounds),) + cdim, x.dtype)
+    for s, (a, b) in enumerate(bounds):
+        oracle_mod.partial_amax(x[a:b], rows, cols, a, slots_r[s], slots_c[s] if colwise else None)
+    ar = oracle_mod.max_reduce(slots_r)
+    ac = oracle_mod.max_reduce(slots_c) if colwise else None
+    sr = np.zeros(rdim, np.uint8)
+    oracle_mod.update_scales(ar, *rdim, sr)
+    sc = None
+    if colwise:
+        sc = np.zeros(cdim, np.uint8)
+        oracle_mod.update_scales(ac, *cdim, sc)
+    qr = np.full(rows * cols, 0xA5, np.uint8)
+    qc = np.full(rows * cols, 0xA5, np.uint8) if colwise else None
+    for a, b in bounds:
+        if out_fragment:
+            fr = np.full(b - a, 0xA5, np.uint8)
+            fc = np.full(b - a, 0xA5, np.uint8) if colwise else None
+            oracle_mod.partial_cast(x[a:b], rows, cols, a, sr, sc, fr, fc, 0)
+            qr[a:b] = fr
+            if colwise:
+                qc[a:b] = fc
+        else:
+            oracle_mod.partial_cast(x[a:b], rows, cols, a, sr, sc, qr, qc, a)
+    return ar, ac, sr, sc, qr, qc
+
+
+@pytest.mark.parametrize("out_fragment", [False, True])
+def test_union_of_fragments_equals_full(oracle_mod, out_fragment):
+    rows, cols = 128, 96
+    rng = np.random.default_rng(9)
+    x = wl.normal_f32(rng, rows * cols)
+    n = rows * cols
+    full = oracle_mod.full_cast(x, rows, cols)
+    for cuts in ([0, 17, 17 + n // 4, n], [0, 50 * 96 + 13, 50 * 96 + 13, n], [0, 33, 65, 99, n]):
+        got = _sharded_flow(oracle_mod, x, rows, cols, cuts, out_fragment=out_fragment)
+        for k in range(6):
+            assert np.array_equal(got[k], full[k]), (cuts, k)
+
+
+def test_boundary_inside_block_same_scale(oracle_mod):
+    rows, cols = 32, 64
+    rng = np.random.default_rng(10)
+    x = wl.normal_f32(rng, rows * cols)
+    x[5] = 0.9  # the block maximum sits on one side of the cut
+    full = oracle_mod.full_cast(x, rows, cols)
+    got = _sharded_flow(oracle_mod, x, rows, cols, [0, 13, rows * cols])
+    assert got[2][0, 0] == full[2][0, 0] == oracle_mod.e8m0_from_amax(np.array([0.9]))[0]
+
+
+def test_empty_fragment_writes_nothing(oracle_mod):
+    rows, cols = 64, 64
+    x = np.ones(rows * cols, np.float32)
+    ar = np.full((rows, 2), 5.0, np.float32)
+    ac = np.full((2, cols), 5.0, np.float32)
+    oracle_mod.partial_amax(x[:0], rows, cols, 100, ar, ac)
+    assert np.all(ar == 5.0) and np.all(ac == 5.0)
+    q = np.full(rows * cols, 0xA5, np.uint8)
+    sr = np.zeros((rows, 2), np.uint8)
+    oracle_mod.partial_cast(x[:0], rows, cols, 100, sr, sr, q, q, 100)
+    assert np.all(q == 0xA5)
+
+
+def test_cast_bf16_input_no_second_rounding(oracle_mod):
+    """BF16 input is already in the model dtype: the oracle must not alter it."""
+    rng = np.random.default_rng(11)
+    x = wl.truncate_to_bf16_bits(wl.normal_f32(rng, 32 * 64))
+    xf = wl.bf16_bits_to_f32(x)
+    a = oracle_mod.full_cast(x, 32, 64)
+    b = oracle_mod.full_cast(xf, 32, 64)  # FP32 values that are exact BF16 values
+    assert np.array_equal(a[4], b[4]) and np.array_equal(a[5], b[5])
+    assert np.array_equal(a[2], b[2])
+
+
+def test_scale_ff_and_nan_conventions(oracle_mod):
+    assert oracle_mod.quantize(1.0, 0xFF) == 0x7F
+    assert oracle_mod.quantize(float("nan"), 119) == 0x7F
+    assert oracle_mod.quantize(float("inf"), 119) == 0x7E
+    assert oracle_mod.quantize(float("-inf"), 119) == 0xFE
+    assert oracle_mod.quantize(-1e-30, 119) == 0x80
