@@ -1,0 +1,354 @@
+"""Benchmark of the partial MXFP8 cast hot path on GB300.
+
+Workload: 16384x6144 FP32 master weight (per-row scale 10^U(-4,1) times
+N(0, 0.02), seed 0), one full fragment, bidirectional MXFP8 (E4M3 data, E8M0
+32-value block scales), model dtype BF16.  One step = one pass of the whole hot
+path through the public API: partial amax into the packed amax slot -> packed
+MAX reduction over the slots (one slot: one rank) -> scale update -> partial cast.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is whole-job HBM throughput in GB/s of
+algorithmic bytes (every kernel's compulsory reads and writes) with the input
+resident in device memory; `kernels` gives each kernel's CUDA-event time per
+call, GB/s and fraction of the measured HBM peak; `e2e` repeats the step with
+the input copied from pinned host memory and the outputs copied back inside the
+timed region.  `--impl reference` times the CPU oracle on a bounded sample of
+the same workload (the reference arm of this benchmark).
+N > 1 (torchrun): every rank runs its own replica of the workload on its GPU.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+ROWS, COLS = 16384, 6144
+METRIC = "MXFP8 partial amax+cast µs/call and HBM GB/s (% of GB300 roofline), 1 GPU"
+WORKLOAD = ("16384x6144 FP32 master (per-row scale 10^U(-4,1) x N(0,0.02), seed 0), full fragment, "
+            "bidirectional MXFP8 E4M3 / E8M0 32-value blocks, model dtype BF16")
+PAGES_GB200_US = {"amax": 110.395, "cast": 210.154}  # context only: other hardware
+FALLBACK_HBM_GBS = 6800.0
+
+
+def algorithmic_bytes(n: int, s_in: int = 4, colwise: bool = True) -> dict:
+    """Compulsory HBM bytes per call of each kernel for an n-element fragment."""
+    dirs = 2 if colwise else 1
+    blocks = dirs * n // 32            # amax / scale entries
+    return {
+        "amax": n * s_in + blocks * s_in,                 # read x, write amax
+        "reduce": 2 * blocks * s_in,                      # read 1 slot, write reduced
+        "scales": blocks * s_in + blocks,                 # read amax, write E8M0 bytes
+        "cast": n * s_in + blocks + dirs * n,             # read x and scales, write E4M3
+    }
+
+
+def measured_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_traffic(kernel: str):
+    """ncu DRAM bytes per launch recorded under profiles/ for the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic_16384x6144_f32.txt")
+    if not os.path.exists(path):
+        return None
+    from mxfp8_master_weight_gb300 import build as libbuild
+    digest = libbuild.source_digest()
+    for line in open(path):
+        parts = dict(p.split("=", 1) for p in line.split() if "=" in p)
+        if parts.get("kernel") == kernel and parts.get("sources_sha256") == digest:
+            return int(parts["dram_bytes_per_launch"])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in (self.out or "").splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    if n_gpus <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl")
+    return dist.get_rank(), dist.get_world_size(), local
+
+
+def aggregate_over_ranks(elapsed_s: float, units: float, world: int, device=None):
+    """(max elapsed over ranks, sum of units over ranks) via torch.distributed."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def cpu_sample_run(rows: int):
+    """Time the CPU oracle (as it stands, one thread) on the first `rows` rows of the
+    workload: amax -> scales -> cast.  Returns (seconds, algorithmic bytes)."""
+    import oracle
+    from mxfp8_master_weight_gb300 import workloads as wl
+    w = wl.cfg4_headline(rows=ROWS, cols=COLS)
+    x = np.ascontiguousarray(w.data[: rows * COLS])
+    t0 = time.perf_counter()
+    oracle.full_cast(x, rows, COLS, True)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(rows * COLS)
+    return dt, b["amax"] + b["scales"] + b["cast"]
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", 0))
+    if rank != 0:
+        return  # the CPU reference arm runs on rank 0 only
+    rows = 512
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_sample_run(rows)
+    tot_t, tot_b = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = cpu_sample_run(rows)
+        tot_t += dt
+        tot_b += b
+    gbs = tot_b / tot_t / 1e9
+    sample = f"first {rows} rows ({rows * COLS} elements) of the workload per step: amax, scales, cast"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample_rows": rows},
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_ours(args):
+    import torch
+
+    from mxfp8_master_weight_gb300 import build as libbuild
+    libbuild.build()
+    from mxfp8_master_weight_gb300 import driver
+    from mxfp8_master_weight_gb300 import workloads as wl
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = ROWS * COLS
+    w = wl.cfg4_headline(rows=ROWS, cols=COLS)
+    host = torch.from_numpy(w.data).pin_memory()
+    x = host.to(dev)
+    sc = driver.ShardedCast([driver.WeightSpec(ROWS, COLS, True)], [0, n], dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ("amax", "reduce", "scales", "cast")
+    abytes = algorithmic_bytes(n)
+    step_bytes = sum(abytes.values())
+
+    def step(events=None):
+        sc.step([x], events=events)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-kernel events on the launching stream
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for k in range(args.steps):
+            step(events=evs[k])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    elapsed = start.elapsed_time(stop) / 1e3
+    per_kernel = {nm: [] for nm in names}
+    for e in evs:
+        for i, nm in enumerate(names):
+            per_kernel[nm].append(e[i].elapsed_time(e[i + 1]) * 1e3)  # us
+    t_max, total_bytes = aggregate_over_ranks(elapsed, step_bytes * args.steps, world, dev)
+
+    # end to end through the public API with host buffers
+    out_r, out_c = sc.outputs[0]
+    s_r, s_c = sc.scales[0]
+    host_q = [torch.empty(out_r.shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    host_s = [torch.empty(s_r.shape, dtype=torch.uint8).pin_memory(),
+              torch.empty(s_c.shape, dtype=torch.uint8).pin_memory()]
+    e2e_steps = max(1, min(args.steps, 50))
+
+    def e2e_step():
+        x.copy_(host, non_blocking=True)
+        step()
+        host_q[0].copy_(out_r, non_blocking=True)
+        host_q[1].copy_(out_c, non_blocking=True)
+        host_s[0].copy_(s_r, non_blocking=True)
+        host_s[1].copy_(s_c, non_blocking=True)
+
+    for _ in range(max(3, min(args.warmup, 5))):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_t, e2e_bytes = aggregate_over_ranks(e0.elapsed_time(e1) / 1e3, step_bytes * e2e_steps, world, dev)
+    h2d = n * 4
+    d2h = 2 * n + s_r.numel() + s_c.numel()
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    kernels = {}
+    for nm in names:
+        us = statistics.median(per_kernel[nm])
+        mean_us = statistics.fmean(per_kernel[nm])
+        gbs = abytes[nm] / (mean_us * 1e-6) / 1e9
+        kernels[nm] = {"us_per_call_median": round(us, 3), "us_per_call_mean": round(mean_us, 3),
+                       "algorithmic_bytes": abytes[nm], "gbs": round(gbs, 1),
+                       "frac_of_" + peak_kind + "_peak": round(gbs / peak, 4)}
+    dom = "cast"
+    dom_mean = statistics.fmean(per_kernel[dom])
+    achieved = abytes[dom] / (dom_mean * 1e-6) / 1e9
+
+    cpu = None
+    if world == 1 or rank == 0:
+        import oracle
+        oracle.build()
+        cpu_rows = args.cpu_rows
+        dt, b = cpu_sample_run(cpu_rows)
+        cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first {cpu_rows} rows ({cpu_rows * COLS} elements) of the workload: "
+                         f"amax, scales, cast; {dt:.1f} s single-threaded"}
+
+    value = total_bytes / t_max / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_max / args.steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "rows": ROWS, "cols": COLS, "fragment": "full (offset 0)",
+                   "directions": "rowwise+columnwise", "emulated_shards": 1,
+                   "l2": "inputs larger than L2 (402.7 MB FP32 fragment vs 126 MB L2); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_call": {nm: kernels[nm]["us_per_call_median"] for nm in names},
+        "kernels": kernels,
+        "pages_gb200_us_per_call": PAGES_GB200_US,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": read_traffic(dom)},
+        "e2e": {"value": round(e2e_bytes / e2e_t / 1e9, 1), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_t / e2e_steps * 1e3, 4), "steps": e2e_steps},
+        "gpu_launches": sc.launches_per_step() * args.steps,
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=8192,
+                    help="rows of the workload the CPU-oracle baseline runs on")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,166 @@
+/*
+ * mxfp8_partial.h -- C ABI of the GB300 partial MXFP8 cast of master weights.
+ *
+ * The operation is the distributed master-weight writeback described on the page
+ * "Support row-only MXFP8 distributed master-weight casts" (TransformerEngine
+ * pull request 3488), sections "Changes" and the flow diagram: each rank holds a
+ * contiguous fragment of a flattened rows x cols FP32 (or BF16) master weight;
+ *   1. partial amax   -- 1x32 row-block and 32x1 column-block maxima of |x| over
+ *                        the fragment, for the directions the weight has;
+ *   2. packed MAX reduce of those amaxes over all ranks (here: over shard slots
+ *                        of one device buffer);
+ *   3. scale update   -- E8M0 block scales from the reduced amaxes;
+ *   4. partial cast   -- master -> BF16 (nearest-even) -> E4M3 (nearest-even,
+ *                        saturating at 448), written in place into the rowwise and,
+ *                        when present, columnwise outputs.
+ * Scale convention (the pages print none): scale exponent
+ * e = floor(log2(amax)) - 8, clamped to [-127, 127], amax 0 -> -127; the stored
+ * E8M0 byte is e + 127 (0xFF for a NaN/infinite amax).  Data byte =
+ * E4M3(bf16(x) * 2^-e).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer inside an mxfp8_tensor is a DEVICE pointer (global memory of
+ *   the current CUDA device).  The caller owns all memory; the library never
+ *   allocates, frees or keeps a pointer after the call returns.
+ * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *   legacy default stream).  A return of 0 means "validated and launched".
+ * - Tensors are dense and row-major: a 2-D tensor's row stride is shape[1].
+ * - An EMPTY handle (data == NULL, or any shape entry == 0, or a NULL handle
+ *   pointer) means "this direction is absent" (section "Changes": omission uses
+ *   empty tensor handles, not a magic shape).
+ * - Return status: 0 ok; 1 invalid argument; 2 shape/padding mismatch;
+ *   3 dtype mismatch; 4 missing required tensor; 6 CUDA launch error.
+ *   (5, non-contiguous, is raised by language bindings that can see strides.)
+ *   mxfp8_last_error() gives a message for the calling thread's last failure.
+ * - Thread safety: entry points may be called concurrently from several host
+ *   threads; results written by two launches to the same buffer race.
+ */
+#ifndef MXFP8_PARTIAL_H_
+#define MXFP8_PARTIAL_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MXFP8_DTYPE_F32 = 0,  /* float                              */
+  MXFP8_DTYPE_BF16 = 1, /* bfloat16 (16-bit patterns)         */
+  MXFP8_DTYPE_U8 = 2    /* uint8: E8M0 scales and E4M3 data   */
+} mxfp8_dtype;
+
+typedef struct {
+  void* data;       /* device pointer, element-aligned; NULL => empty      */
+  int32_t dtype;    /* mxfp8_dtype                                         */
+  int32_t ndim;     /* 1 or 2                                              */
+  int64_t shape[2]; /* shape[1] ignored when ndim == 1                     */
+} mxfp8_tensor;
+
+enum {
+  MXFP8_OK = 0,
+  MXFP8_ERR_INVALID = 1,
+  MXFP8_ERR_SHAPE = 2,
+  MXFP8_ERR_DTYPE = 3,
+  MXFP8_ERR_MISSING = 4,
+  MXFP8_ERR_NONCONTIGUOUS = 5,
+  MXFP8_ERR_CUDA = 6
+};
+
+/*
+ * Partial amax (page "Support row-only MXFP8 distributed master-weight casts",
+ * review thread: documentation of the partial amax entry point).
+ *
+ * input         [in]     fragment: numel(input) = len contiguous F32 or BF16
+ *                        values, element k of the fragment is element
+ *                        start_offset + k of the flattened rows x cols weight.
+ * amax_rowwise  [in,out] REQUIRED, 2-D [>= rows][>= ceil(cols/32)], dtype of the
+ *                        input.  Entry (i, b) = max |x| over the fragment's
+ *                        elements of row i, columns [32b, 32b+32).
+ * amax_colwise  [in,out] OPTIONAL (empty => the columnwise direction is skipped
+ *                        entirely, at compile time in the kernel), 2-D
+ *                        [>= ceil(rows/32)][>= cols], dtype of the input.
+ *                        Entry (c, j) = max |x| over the fragment's elements of
+ *                        column j, rows [32c, 32c+32).
+ * Only entries of blocks that contain at least one fragment element are written
+ * (overwritten, not max-accumulated); every other entry keeps its value, so a
+ * caller that reduces across fragments zeroes its buffers first.  An empty
+ * fragment (len 0) writes nothing and returns 0.  NaN members make the entry NaN.
+ * Errors: 1 if start_offset < 0, rows/cols <= 0, start_offset + len > rows*cols,
+ * or a pointer is not element-aligned; 2 on a too-small amax shape;
+ * 3 if an amax dtype differs from the input dtype or the input is not F32/BF16;
+ * 4 if amax_rowwise is empty (and len > 0).
+ */
+int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+                       mxfp8_tensor* amax_colwise, int64_t rows, int64_t cols,
+                       int64_t start_offset, void* stream);
+
+/*
+ * Packed MAX reduction (page "Support row-only MXFP8 distributed master-weight
+ * casts", section "Changes": one packed-amax MAX all-reduce; here the ranks are
+ * emulated as slots of one device buffer).
+ *
+ * slots  [in]  2-D [S][E] F32 or BF16: S packed amax buffers of E entries each.
+ * out    [out] E entries (any shape with numel == E), same dtype.
+ * out[k] = max over s of |slots[s][k]|; NaN propagates.  S == 1 copies |.|.
+ * out may not overlap slots.  Errors: 2 numel mismatch, 3 dtype, 4 empty out.
+ */
+int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* stream);
+
+/*
+ * Scale update (page "Support row-only MXFP8 distributed master-weight casts",
+ * flow diagram: "update scales for present directions").
+ *
+ * amax_rowwise      [in]  REQUIRED, [>= rows][>= ceil(cols/32)], F32 or BF16.
+ * amax_colwise      [in]  OPTIONAL, [>= ceil(rows/32)][>= cols], same dtype;
+ *                         empty => no columnwise scales are computed.
+ * scale_inv_rowwise [out] REQUIRED, U8 [>= rows][>= ceil(cols/32)].
+ * scale_inv_colwise [out] U8 [>= ceil(rows/32)][>= cols]; required iff
+ *                         amax_colwise is present, ignored otherwise.
+ * Writes the E8M0 byte of every entry of the compact block grid
+ * (rows x ceil(cols/32) and ceil(rows/32) x cols); padding is left untouched.
+ */
+int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
+                        mxfp8_tensor* scale_inv_rowwise, mxfp8_tensor* scale_inv_colwise,
+                        int64_t rows, int64_t cols, void* stream);
+
+/*
+ * Partial cast (page "Support row-only MXFP8 distributed master-weight casts",
+ * sections "Changes" and the review thread's documentation of the partial cast:
+ * rowwise outputs are required; columnwise scales are required when the
+ * columnwise output is present and ignored when it is omitted).
+ *
+ * input             [in]  fragment as for mxfp8_partial_amax.
+ * scale_inv_rowwise [in]  REQUIRED U8 [>= rows][>= ceil(cols/32)] E8M0 bytes.
+ * scale_inv_colwise [in]  U8 [>= ceil(rows/32)][>= cols]; required iff
+ *                         output_colwise is present, ignored otherwise.
+ * output_rowwise    [out] REQUIRED U8, numel >= out_offset + len.
+ * output_colwise    [out] OPTIONAL U8 (empty => no columnwise reads or writes),
+ *                         numel >= out_offset + len.
+ * For fragment element k (weight element (i, j)): y = BF16 rounding of x
+ * (identity for BF16 input); output_rowwise[out_offset + k] = E4M3(y * 2^-e_r),
+ * e_r from scale_inv_rowwise[i][j/32]; output_colwise likewise with
+ * scale_inv_colwise[i/32][j].  Outputs hold E4M3 bytes in the weight's own
+ * row-major layout (the columnwise copy is not transposed).  out_offset =
+ * start_offset writes into a full-size rows*cols output in place; out_offset = 0
+ * writes a fragment-sized output.  Bytes outside the fragment are not touched.
+ * Errors: 1 bad offsets/sizes; 2 output or scale too small; 3 dtype;
+ * 4 rowwise scale/output missing, or columnwise output without columnwise scales.
+ */
+int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_rowwise,
+                       const mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
+                       mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
+                       int64_t start_offset, int64_t out_offset, void* stream);
+
+/* Message describing the calling thread's most recent non-zero status ("" if none). */
+const char* mxfp8_last_error(void);
+
+/* Library version as major*10000 + minor*100 + patch. */
+int mxfp8_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP8_PARTIAL_H_ */

@@ -1,0 +1,112 @@
+"""Python binding of the C ABI, with the same entry-point names.
+
+Argument marshalling only: torch tensors are turned into ``mxfp8_tensor``
+handles and the call goes to the CUDA library on the tensor's current stream.
+Every step of the computation runs in the library's kernels.
+
+Omission contract ("Support row-only MXFP8 distributed master-weight casts",
+section "Changes"): ``None`` and every zero-element tensor -- including a view
+that still has backing storage -- become an EMPTY handle, which the library reads
+as "this direction is absent".
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _capi
+from ._capi import DTYPE_BF16, DTYPE_F32, DTYPE_U8, MXFP8Error, Tensor
+
+_DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.uint8: DTYPE_U8,
+           torch.float8_e4m3fn: DTYPE_U8}
+if hasattr(torch, "float8_e8m0fnu"):
+    _DTYPES[torch.float8_e8m0fnu] = DTYPE_U8
+
+
+def handle(t: torch.Tensor | None, name: str) -> Tensor:
+    """mxfp8_tensor for a CUDA tensor; None / zero-element tensors give an empty handle."""
+    if t is None or t.numel() == 0:
+        return _capi.empty_tensor()
+    if not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+    if not t.is_contiguous():
+        raise MXFP8Error(5, f"{name}: tensor must be contiguous")
+    if t.dtype not in _DTYPES:
+        raise MXFP8Error(3, f"{name}: unsupported dtype {t.dtype}")
+    if t.dim() > 2:
+        raise ValueError(f"{name}: expected at most 2 dimensions, got {t.dim()}")
+    shape = tuple(t.shape) if t.dim() == 2 else (t.numel(), 0)
+    return Tensor(ctypes.c_void_p(t.data_ptr()), _DTYPES[t.dtype], 2 if t.dim() == 2 else 1,
+                  (ctypes.c_int64 * 2)(*shape))
+
+
+def _stream(stream, like: torch.Tensor | None):
+    if stream is None:
+        dev = like.device if like is not None and like.is_cuda else None
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _device_of(*ts):
+    for t in ts:
+        if t is not None and t.numel() > 0 and t.is_cuda:
+            return t.device
+    return None
+
+
+def _call(fn, dev, *args):
+    lib = _capi.load()
+    if dev is not None:
+        with torch.cuda.device(dev):
+            _capi.check(getattr(lib, fn)(*args))
+    else:
+        _capi.check(getattr(lib, fn)(*args))
+
+
+def mxfp8_partial_amax(input, amax_rowwise, amax_colwise, rows: int, cols: int,
+                       start_offset: int, stream=None) -> None:
+    """Block maxima of |x| over the fragment, written in place (see include/mxfp8_partial.h)."""
+    dev = _device_of(input, amax_rowwise, amax_colwise)
+    args = [handle(input, "input"), handle(amax_rowwise, "amax_rowwise"),
+            handle(amax_colwise, "amax_colwise")]
+    _call("mxfp8_partial_amax", dev, *[ctypes.byref(a) for a in args], int(rows), int(cols),
+          int(start_offset), _stream(stream, input))
+
+
+def mxfp8_amax_max_reduce(slots, out, stream=None) -> None:
+    """out[k] = max_s |slots[s][k]| over the leading (shard) axis of a [S][E] buffer."""
+    dev = _device_of(slots, out)
+    args = [handle(slots, "slots"), handle(out, "out")]
+    _call("mxfp8_amax_max_reduce", dev, *[ctypes.byref(a) for a in args], _stream(stream, out))
+
+
+def mxfp8_update_scales(amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
+                        rows: int, cols: int, stream=None) -> None:
+    """E8M0 scale bytes of the (reduced) block amaxes for the present directions."""
+    dev = _device_of(amax_rowwise, amax_colwise, scale_inv_rowwise)
+    args = [handle(amax_rowwise, "amax_rowwise"), handle(amax_colwise, "amax_colwise"),
+            handle(scale_inv_rowwise, "scale_inv_rowwise"),
+            handle(scale_inv_colwise, "scale_inv_colwise")]
+    _call("mxfp8_update_scales", dev, *[ctypes.byref(a) for a in args], int(rows), int(cols),
+          _stream(stream, amax_rowwise))
+
+
+def mxfp8_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
+                       output_colwise, rows: int, cols: int, start_offset: int,
+                       out_offset: int | None = None, stream=None) -> None:
+    """E4M3 bytes of the fragment into the outputs (out_offset defaults to start_offset:
+    a full-size output written in place; pass 0 for a fragment-sized output)."""
+    dev = _device_of(input, output_rowwise, output_colwise)
+    if out_offset is None:
+        out_offset = start_offset
+    args = [handle(input, "input"), handle(scale_inv_rowwise, "scale_inv_rowwise"),
+            handle(scale_inv_colwise, "scale_inv_colwise"),
+            handle(output_rowwise, "output_rowwise"), handle(output_colwise, "output_colwise")]
+    _call("mxfp8_partial_cast", dev, *[ctypes.byref(a) for a in args], int(rows), int(cols),
+          int(start_offset), int(out_offset), _stream(stream, input))
+
+
+def block_shapes(rows: int, cols: int):
+    """Compact (rowwise, columnwise) block-grid shapes: [rows, ceil(cols/32)], [ceil(rows/32), cols]."""
+    return (rows, (cols + 31) // 32), ((rows + 31) // 32, cols)

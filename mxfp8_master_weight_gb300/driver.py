@@ -1,0 +1,193 @@
+"""Multi-fragment driver: a batch of weights cast from sharded master buffers.
+
+This is the flow of "Support row-only MXFP8 distributed master-weight casts"
+(flow diagram and section "Changes"): every rank computes the partial amax of
+its fragments for the directions each weight has, the amaxes of the whole batch
+are packed into one buffer and MAX-reduced ONCE across ranks, the scales of the
+present directions are updated, and every rank casts its fragments in place.
+
+Here the ranks are emulated on one GPU: shard s is its own device buffer (as a
+rank's master shard would be) and has its own slot of the packed amax buffer;
+the cross-rank MAX all-reduce is one ``mxfp8_amax_max_reduce`` over the slots.
+All arithmetic runs in the CUDA library; this module only plans fragments and
+packed offsets (host logic) and issues the calls.
+
+Packed layout: weights in batch order; for each weight its rowwise block grid
+[rows][ceil(cols/32)], then -- only when it has a columnwise direction -- its
+columnwise grid [ceil(rows/32)][cols].  Each entry starts on a multiple of 16
+elements (64 bytes for FP32) so that every view keeps 16-byte vector access;
+the padding entries stay zero and reduce to zero.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import api
+
+_ALIGN = 16
+
+
+@dataclass(frozen=True)
+class WeightSpec:
+    rows: int
+    cols: int
+    colwise: bool
+
+    @property
+    def numel(self) -> int:
+        return self.rows * self.cols
+
+
+@dataclass(frozen=True)
+class FragmentCut:
+    """Fragment of weight `weight` = weight elements [start, start+length), found at
+    `shard_offset` inside shard `shard`."""
+    shard: int
+    weight: int
+    start: int
+    length: int
+    shard_offset: int
+
+
+def plan_fragments(specs, bounds):
+    """Cut every weight of the flat batch buffer at the shard boundaries.
+
+    ``bounds`` = [b0=0, b1, ..., bS=total] (non-decreasing; equal neighbours make an
+    empty shard).  Returns, per shard, the list of non-empty FragmentCut in weight order.
+    """
+    if bounds[0] != 0 or any(b > c for b, c in zip(bounds[:-1], bounds[1:])):
+        raise ValueError("shard bounds must start at 0 and be non-decreasing")
+    total = sum(s.numel for s in specs)
+    if bounds[-1] != total:
+        raise ValueError(f"last shard bound {bounds[-1]} != batch size {total}")
+    plan = []
+    for s in range(len(bounds) - 1):
+        lo, hi = bounds[s], bounds[s + 1]
+        cuts, off = [], 0
+        for w, spec in enumerate(specs):
+            a, b = max(lo, off), min(hi, off + spec.numel)
+            if a < b:
+                cuts.append(FragmentCut(s, w, a - off, b - a, a - lo))
+            off += spec.numel
+        plan.append(cuts)
+    return plan
+
+
+class PackedLayout:
+    """Element offsets of every present block grid inside the packed amax buffer."""
+
+    def __init__(self, specs):
+        self.specs = list(specs)
+        self.rowwise, self.colwise = [], []
+        off = 0
+        for spec in self.specs:
+            (rr, rc), (cr, cc) = api.block_shapes(spec.rows, spec.cols)
+            self.rowwise.append((off, (rr, rc)))
+            off = _round_up(off + rr * rc, _ALIGN)
+            if spec.colwise:
+                self.colwise.append((off, (cr, cc)))
+                off = _round_up(off + cr * cc, _ALIGN)
+            else:
+                self.colwise.append(None)
+        self.total = off
+
+    def views(self, buf: torch.Tensor, w: int):
+        """(rowwise view, columnwise view or None) of weight w inside a 1-D packed buffer."""
+        o, shp = self.rowwise[w]
+        vr = buf[o:o + shp[0] * shp[1]].view(shp)
+        vc = None
+        if self.colwise[w] is not None:
+            o, shp = self.colwise[w]
+            vc = buf[o:o + shp[0] * shp[1]].view(shp)
+        return vr, vc
+
+
+def _round_up(x: int, a: int) -> int:
+    return (x + a - 1) // a * a
+
+
+class ShardedCast:
+    """Device state for casting one batch of weights from S emulated master shards.
+
+    Buffers (allocated once, reused by every step, so output and scale pointers are
+    stable across consecutive updates): packed amax slots [S][P], the reduced packed
+    amax [P], per-weight E8M0 scales, and per-weight full-size E4M3 outputs (rowwise
+    always, columnwise only for bidirectional weights).
+    """
+
+    def __init__(self, specs, bounds, device, dtype=torch.float32):
+        self.specs = [s if isinstance(s, WeightSpec) else WeightSpec(*s) for s in specs]
+        self.bounds = list(bounds)
+        self.plan = plan_fragments(self.specs, self.bounds)
+        self.layout = PackedLayout(self.specs)
+        self.dtype = dtype
+        S = len(self.bounds) - 1
+        self.slots = torch.zeros((S, self.layout.total), dtype=dtype, device=device)
+        self.reduced = torch.zeros(self.layout.total, dtype=dtype, device=device)
+        # a slot needs zeroing before each step unless its shard holds every weight whole
+        # (then every block entry of the slot is overwritten by the amax kernels)
+        self._zero_slot = [not (len(cuts) == len(self.specs) and
+                                all(c.start == 0 and c.length == self.specs[c.weight].numel
+                                    for c in cuts))
+                           for cuts in self.plan]
+        self.scales, self.outputs = [], []
+        for spec in self.specs:
+            (rr, rc), (cr, cc) = api.block_shapes(spec.rows, spec.cols)
+            sr = torch.zeros((rr, rc), dtype=torch.uint8, device=device)
+            sc = torch.zeros((cr, cc), dtype=torch.uint8, device=device) if spec.colwise else None
+            self.scales.append((sr, sc))
+            qr = torch.zeros(spec.numel, dtype=torch.uint8, device=device)
+            qc = torch.zeros(spec.numel, dtype=torch.uint8, device=device) if spec.colwise else None
+            self.outputs.append((qr, qc))
+
+    @property
+    def num_shards(self) -> int:
+        return len(self.bounds) - 1
+
+    def launches_per_step(self) -> int:
+        """Library kernel launches of one step (amax + cast per fragment, reduce, scales)."""
+        frags = sum(len(c) for c in self.plan)
+        return 2 * frags + 1 + len(self.specs)
+
+    def step(self, shards, stream=None, events=None) -> None:
+        """One distributed update: partial amax -> one packed MAX reduce -> scales -> casts.
+
+        ``events``: optional five CUDA events recorded on the stream before the amax
+        phase and after the amax, reduce, scale and cast phases (for timing).
+        """
+        if len(shards) != self.num_shards:
+            raise ValueError("one master shard buffer per emulated rank is required")
+        for s, shard in enumerate(shards):
+            if shard.numel() != self.bounds[s + 1] - self.bounds[s]:
+                raise ValueError(f"shard {s} holds {shard.numel()} elements, plan expects "
+                                 f"{self.bounds[s + 1] - self.bounds[s]}")
+        mark = (lambda i: events[i].record(stream)) if events is not None else (lambda i: None)
+        # amax entries a fragment does not touch must be zero before the reduction
+        for s in range(self.num_shards):
+            if self._zero_slot[s]:
+                self.slots[s].zero_()
+        mark(0)
+        for s, cuts in enumerate(self.plan):
+            for c in cuts:
+                spec = self.specs[c.weight]
+                vr, vc = self.layout.views(self.slots[s], c.weight)
+                api.mxfp8_partial_amax(shards[s][c.shard_offset:c.shard_offset + c.length], vr, vc,
+                                       spec.rows, spec.cols, c.start, stream=stream)
+        mark(1)
+        api.mxfp8_amax_max_reduce(self.slots, self.reduced, stream=stream)
+        mark(2)
+        for w, spec in enumerate(self.specs):
+            vr, vc = self.layout.views(self.reduced, w)
+            sr, sc = self.scales[w]
+            api.mxfp8_update_scales(vr, vc, sr, sc, spec.rows, spec.cols, stream=stream)
+        mark(3)
+        for s, cuts in enumerate(self.plan):
+            for c in cuts:
+                spec = self.specs[c.weight]
+                sr, sc = self.scales[c.weight]
+                qr, qc = self.outputs[c.weight]
+                api.mxfp8_partial_cast(shards[s][c.shard_offset:c.shard_offset + c.length], sr, sc,
+                                       qr, qc, spec.rows, spec.cols, c.start, stream=stream)
+        mark(4)

@@ -1,0 +1,63 @@
+"""Host-side logic of bench.py that needs no GPU: the algorithmic byte model, the
+clock-sample parser, and the N>1 aggregation (max time, summed work over ranks)
+run as two gloo ranks on the CPU."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_algorithmic_bytes_per_element():
+    n = 16384 * 6144
+    b = bench.algorithmic_bytes(n)
+    assert b["amax"] / n == pytest.approx(4.25)        # read 4 B, write 2 x 4 B / 32
+    assert b["cast"] / n == pytest.approx(6.0625)      # read 4 B + 2 scale B / 32, write 2 B
+    assert b["amax"] == 427_819_008 and b["cast"] == 610_271_232
+    ro = bench.algorithmic_bytes(n, colwise=False)
+    assert ro["cast"] / n == pytest.approx(4 + 1 / 32 + 1)
+
+
+def test_clock_summary_parser():
+    c = bench.ClockSampler(0)
+    c.out = ("0, 1965, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Active\n"
+             "0, 1980, 2070, 910.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+             "garbage line\n")
+    s = c.summary()
+    assert s["sm_mhz"] == pytest.approx(1972.5) and s["sm_max_mhz"] == 2070
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 2
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.aggregate_over_ranks(1.0 + rank, 10.0 * (rank + 1), world)
+    q.put((rank, t, u))
+    dist.destroy_process_group()
+
+
+def test_aggregate_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
+
+
+def test_single_rank_aggregation_is_identity():
+    assert bench.aggregate_over_ranks(0.5, 7.0, 1) == (0.5, 7.0)

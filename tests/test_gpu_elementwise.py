@@ -1,0 +1,106 @@
+"""Element-wise parity through the C ABI: every BF16 bit pattern and a million random
+FP32 bit patterns through the cast, under many scale bytes; every BF16 amax pattern
+and random FP32 amaxes through the scale update; the packed MAX reduction.
+Bit-exact against the oracle (the special-value conventions are stated in the
+oracle's header)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_master_weight_gb300 import api
+
+from flows import assert_bitwise, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+ROW_SCALES = np.array([0, 1, 8, 60, 100, 119, 127, 135, 160, 200, 240, 246, 250, 253, 254, 255],
+                      np.uint8)
+
+
+def _cast_with_scales(x: np.ndarray, rows: int, cols: int, s_r: np.ndarray, s_c: np.ndarray):
+    xd = to_device(x)
+    qr = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    qc = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    api.mxfp8_partial_cast(xd, torch.from_numpy(s_r).cuda(), torch.from_numpy(s_c).cuda(), qr, qc,
+                           rows, cols, 0)
+    got_r, got_c = to_host(qr), to_host(qc)
+    want_r = np.zeros(rows * cols, np.uint8)
+    want_c = np.zeros(rows * cols, np.uint8)
+    oracle.partial_cast(x, rows, cols, 0, s_r, s_c, want_r, want_c, 0)
+    return got_r, got_c, want_r, want_c
+
+
+def _scale_grids(rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    s_r = np.repeat(ROW_SCALES[:rows, None], (cols + 31) // 32, axis=1).copy()
+    s_c = rng.integers(0, 256, size=((rows + 31) // 32, cols), dtype=np.uint8)
+    return s_r, s_c
+
+
+def test_cast_every_bf16_pattern():
+    rows, cols = 16, 65536
+    x = np.tile(np.arange(65536, dtype=np.uint16), rows)
+    s_r, s_c = _scale_grids(rows, cols, 1)
+    gr, gc, wr, wc = _cast_with_scales(x, rows, cols, s_r, s_c)
+    assert_bitwise((gr, gc), (wr, wc), "bf16 patterns")
+
+
+def test_cast_random_f32_patterns():
+    rows, cols = 16, 65536
+    rng = np.random.default_rng(2)
+    bits = rng.integers(0, 2 ** 32, rows * cols, dtype=np.uint64).astype(np.uint32)
+    # make a quarter of them moderate values so most scale bytes produce non-trivial codes
+    mod = rng.standard_normal(rows * cols // 4).astype(np.float32) * 2.0 ** rng.integers(-20, 20, rows * cols // 4)
+    bits[: mod.size] = mod.astype(np.float32).view(np.uint32)
+    # BF16 rounding ties and carries into the exponent
+    bits[mod.size:mod.size + 8] = [0x3F808000, 0x3F818000, 0x7F7F8000, 0x7F7FFFFF, 0x00008000,
+                                   0x80018000, 0x3FFF8000, 0x437F8000]
+    x = rng.permutation(bits).view(np.float32)
+    s_r, s_c = _scale_grids(rows, cols, 3)
+    gr, gc, wr, wc = _cast_with_scales(x, rows, cols, s_r, s_c)
+    assert_bitwise((gr, gc), (wr, wc), "f32 patterns")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_scale_update_patterns(dtype):
+    rng = np.random.default_rng(4)
+    if dtype == "bf16":
+        a = np.arange(65536, dtype=np.uint16).reshape(256, 256)
+        af = (a.astype(np.uint32) << 16).view(np.float32)
+    else:
+        a = rng.integers(0, 2 ** 32, 512 * 1024, dtype=np.uint64).astype(np.uint32).view(np.float32)
+        a = a.reshape(512, 1024)
+        af = a
+    rows, cols = a.shape[0], a.shape[1] * 32  # so that the rowwise grid is exactly `a`
+    ad = to_device(a).view(a.shape)
+    s = torch.zeros(a.shape, dtype=torch.uint8, device="cuda")
+    api.mxfp8_update_scales(ad, None, s, None, rows, cols)
+    want = oracle.e8m0_from_amax(np.abs(af.astype(np.float64)))
+    assert np.array_equal(to_host(s), want)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nslots,elems", [(1, 1000), (4, 8_912_896), (3, 1001), (7, 64)])
+def test_max_reduce(dtype, nslots, elems):
+    rng = np.random.default_rng(nslots * 7 + elems)
+    x = np.abs(rng.standard_normal((nslots, elems)).astype(np.float32))
+    x[rng.random(x.shape) < 0.3] = 0.0
+    if dtype == "bf16":
+        x = (x.view(np.uint32) >> 16).astype(np.uint16)
+    d = to_device(x).view(nslots, elems)
+    out = torch.empty(elems, dtype=d.dtype, device="cuda")
+    api.mxfp8_amax_max_reduce(d, out)
+    assert np.array_equal(to_host(out), oracle.max_reduce(x))
+
+
+def test_max_reduce_nan_propagates():
+    x = np.zeros((3, 64), np.float32)
+    x[1, 5] = np.nan
+    x[2, 5] = 1.0
+    x[0, 6] = np.inf
+    d = to_device(x).view(3, 64)
+    out = torch.empty(64, dtype=torch.float32, device="cuda")
+    api.mxfp8_amax_max_reduce(d, out)
+    h = to_host(out)
+    assert np.isnan(h[5]) and np.isinf(h[6]) and h[0] == 0.0

@@ -1,0 +1,92 @@
+"""Multi-fragment driver on one GPU: a mixed row-only / bidirectional batch split into
+emulated master shards (one boundary inside a 32-value block, one empty shard),
+one packed on-device MAX reduction, casts in place.  Parity: the union of the
+shards' casts is bit-identical to the oracle's whole-weight cast, and the reduced
+packed amax equals the oracle's whole-weight amax, packed."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_master_weight_gb300 import driver
+from mxfp8_master_weight_gb300 import workloads as wl
+
+from flows import assert_bitwise, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(batch, dtype=torch.float32):
+    specs = [driver.WeightSpec(w.rows, w.cols, w.colwise) for w in batch.weights]
+    sc = driver.ShardedCast(specs, batch.bounds, "cuda", dtype)
+    shards = [to_device(np.ascontiguousarray(batch.shard(s))) for s in range(sc.num_shards)]
+    return sc, shards
+
+
+def _check_against_full(batch, sc):
+    torch.cuda.synchronize()
+    red = to_host(sc.reduced)
+    for w, wt in enumerate(batch.weights):
+        want = oracle.full_cast(wt.data, wt.rows, wt.cols, wt.colwise)
+        vr, vc = sc.layout.views(torch.from_numpy(red), w)
+        sr, scl = sc.scales[w]
+        qr, qc = sc.outputs[w]
+        got = (vr.numpy(), None if vc is None else vc.numpy(), to_host(sr),
+               None if scl is None else to_host(scl), to_host(qr), None if qc is None else to_host(qc))
+        assert_bitwise(got, want, f"weight {w} ({wt.rows}x{wt.cols} colwise={wt.colwise})")
+
+
+@pytest.mark.parametrize("scale", [8, 1])
+def test_cfg5_sharded_mixed_batch(scale):
+    batch = wl.cfg5_sharded_batch(seed=0, scale=scale)
+    assert batch.bounds[1] % 32 != 0 and batch.bounds[2] == batch.bounds[3]
+    sc, shards = _run(batch)
+    sc.step(shards)
+    _check_against_full(batch, sc)
+
+
+def test_consecutive_updates_keep_pointers_and_match():
+    batch = wl.cfg5_sharded_batch(seed=1, scale=16)
+    sc, shards = _run(batch)
+    ptrs = [(q[0].data_ptr(), None if q[1] is None else q[1].data_ptr()) for q in sc.outputs]
+    sc.step(shards)
+    _check_against_full(batch, sc)
+    # second update of the same state: new master values, same shard layout and buffers
+    rng = np.random.default_rng(99)
+    flat2 = wl.normal_f32(rng, batch.total) * np.float32(3.0)
+    weights2 = [wl.Weight(w.rows, w.cols, w.dtype, flat2[o:o + w.numel], w.colwise)
+                for w, o in zip(batch.weights, batch.offsets)]
+    batch2 = wl.ShardedBatch(weights2, batch.offsets, batch.bounds, flat2)
+    for s in range(sc.num_shards):
+        shards[s].copy_(torch.from_numpy(np.ascontiguousarray(batch2.shard(s))))
+    sc.step(shards)
+    _check_against_full(batch2, sc)
+    assert ptrs == [(q[0].data_ptr(), None if q[1] is None else q[1].data_ptr()) for q in sc.outputs]
+
+
+@pytest.mark.parametrize("cuts", [[0, 17, 17 + 4096 * 4096 // 4, 4096 * 4096],
+                                  [0, 4096 * 4096]])
+def test_cfg3_union_of_fragments(cuts):
+    w = wl.cfg3_square()
+    batch = wl.ShardedBatch([wl.Weight(w.rows, w.cols, wl.F32, w.data, True)], [0], cuts, w.data)
+    sc, shards = _run(batch)
+    sc.step(shards)
+    _check_against_full(batch, sc)
+
+
+def test_bf16_batch_with_empty_and_single_element_shards():
+    rng = np.random.default_rng(5)
+    dims = [(64, 96, True), (33, 65, False), (40, 256, True)]
+    weights, offs, off = [], [], 0
+    for r, c, cw in dims:
+        weights.append(wl.Weight(r, c, wl.BF16, None, cw))
+        offs.append(off)
+        off += r * c
+    flat = wl.truncate_to_bf16_bits(wl.normal_f32(rng, off))
+    for wt, o in zip(weights, offs):
+        wt.data = flat[o:o + wt.numel]
+    bounds = [0, 1, 1, 6144 + 3, 6144 + 4, off - 100, off]
+    batch = wl.ShardedBatch(weights, offs, bounds, flat)
+    sc, shards = _run(batch, torch.bfloat16)
+    sc.step(shards)
+    _check_against_full(batch, sc)
