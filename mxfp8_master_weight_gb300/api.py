@@ -107,6 +107,63 @@ def mxfp8_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwi
           int(start_offset), int(out_offset), _stream(stream, input))
 
 
+class Prepared:
+    """One library call with its tensor handles marshalled once.
+
+    ``call(stream)`` launches it on the given stream (a torch stream or a raw
+    cudaStream_t value) with the current CUDA device, which must be the device the
+    tensors live on.  The tensors are kept alive by this object; their storage must
+    not move between calls (re-prepare after reallocating).
+    """
+
+    __slots__ = ("fn", "args", "handles", "tensors", "device")
+
+    def __init__(self, fn_name, handles, scalars, tensors):
+        self.fn = getattr(_capi.load(), fn_name)
+        self.handles = handles
+        self.args = tuple(ctypes.byref(h) for h in handles) + tuple(int(v) for v in scalars)
+        self.tensors = tensors
+        self.device = _device_of(*tensors)
+
+    def call(self, stream=None) -> None:
+        if stream is None or hasattr(stream, "cuda_stream"):
+            stream = _stream(stream, self.tensors[0] if self.tensors else None)
+        rc = self.fn(*self.args, stream)
+        if rc != 0:
+            _capi.check(rc)
+
+
+def prepare_partial_amax(input, amax_rowwise, amax_colwise, rows, cols, start_offset) -> Prepared:
+    hs = [handle(input, "input"), handle(amax_rowwise, "amax_rowwise"),
+          handle(amax_colwise, "amax_colwise")]
+    return Prepared("mxfp8_partial_amax", hs, (rows, cols, start_offset),
+                    [t for t in (input, amax_rowwise, amax_colwise) if t is not None])
+
+
+def prepare_amax_max_reduce(slots, out) -> Prepared:
+    return Prepared("mxfp8_amax_max_reduce", [handle(slots, "slots"), handle(out, "out")], (),
+                    [slots, out])
+
+
+def prepare_update_scales(amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
+                          rows, cols) -> Prepared:
+    ts = (amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise)
+    hs = [handle(t, n) for t, n in zip(ts, ("amax_rowwise", "amax_colwise", "scale_inv_rowwise",
+                                            "scale_inv_colwise"))]
+    return Prepared("mxfp8_update_scales", hs, (rows, cols), [t for t in ts if t is not None])
+
+
+def prepare_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
+                         output_colwise, rows, cols, start_offset, out_offset=None) -> Prepared:
+    if out_offset is None:
+        out_offset = start_offset
+    ts = (input, scale_inv_rowwise, scale_inv_colwise, output_rowwise, output_colwise)
+    hs = [handle(t, n) for t, n in zip(ts, ("input", "scale_inv_rowwise", "scale_inv_colwise",
+                                            "output_rowwise", "output_colwise"))]
+    return Prepared("mxfp8_partial_cast", hs, (rows, cols, start_offset, out_offset),
+                    [t for t in ts if t is not None])
+
+
 def block_shapes(rows: int, cols: int):
     """Compact (rowwise, columnwise) block-grid shapes: [rows, ceil(cols/32)], [ceil(rows/32), cols]."""
     return (rows, (cols + 31) // 32), ((rows + 31) // 32, cols)
