@@ -153,6 +153,49 @@ int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_
                        mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                        int64_t start_offset, int64_t out_offset, void* stream);
 
+/*
+ * Batched entry points: many fragments (of one or several weights) per call, e.g. all
+ * fragments a rank holds for a batch of weights (page "Support row-only MXFP8
+ * distributed master-weight casts", section "Changes": mixed row-only and
+ * bidirectional batches).  Each job means exactly what the single-fragment call with
+ * the same arguments means; the jobs are validated first (a failure launches nothing
+ * and names the job), then run as few kernels as possible: jobs that share the input
+ * dtype, the direction set and the alignment class go into one launch (at most 16 jobs
+ * each), with the tiles of all jobs scheduled together.  Jobs may run concurrently:
+ * jobs whose written entries overlap (two fragments of one weight writing the SAME
+ * amax buffer, whose boundary blocks both jobs overwrite) race -- give each fragment
+ * its own amax buffer, as a packed per-rank slot does.  Fragments of one weight write
+ * disjoint output bytes and may share the outputs.  F32 and BF16 jobs may be mixed
+ * in one call.  njobs may be 0; jobs with empty fragments are skipped.
+ */
+typedef struct {
+  mxfp8_tensor input;
+  mxfp8_tensor amax_rowwise;
+  mxfp8_tensor amax_colwise; /* empty => row-only */
+  int64_t rows, cols, start_offset;
+} mxfp8_amax_job;
+
+typedef struct {
+  mxfp8_tensor input;
+  mxfp8_tensor scale_inv_rowwise;
+  mxfp8_tensor scale_inv_colwise;
+  mxfp8_tensor output_rowwise;
+  mxfp8_tensor output_colwise; /* empty => row-only */
+  int64_t rows, cols, start_offset, out_offset;
+} mxfp8_cast_job;
+
+typedef struct {
+  mxfp8_tensor amax_rowwise;
+  mxfp8_tensor amax_colwise; /* empty => row-only */
+  mxfp8_tensor scale_inv_rowwise;
+  mxfp8_tensor scale_inv_colwise;
+  int64_t rows, cols;
+} mxfp8_scale_job;
+
+int mxfp8_partial_amax_batched(const mxfp8_amax_job* jobs, int32_t njobs, void* stream);
+int mxfp8_update_scales_batched(const mxfp8_scale_job* jobs, int32_t njobs, void* stream);
+int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 const char* mxfp8_last_error(void);
 

@@ -18,7 +18,8 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "shape mismatch", 3: "dtype m
                 4: "missing required tensor", 5: "non-contiguous", 6: "CUDA error"}
 
 EXPORTED = ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
-            "mxfp8_partial_cast", "mxfp8_last_error", "mxfp8_version")
+            "mxfp8_partial_cast", "mxfp8_partial_amax_batched", "mxfp8_update_scales_batched",
+            "mxfp8_partial_cast_batched", "mxfp8_last_error", "mxfp8_version")
 
 
 class Tensor(ctypes.Structure):
@@ -26,6 +27,23 @@ class Tensor(ctypes.Structure):
 
     _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
                 ("shape", ctypes.c_int64 * 2)]
+
+
+class AmaxJob(ctypes.Structure):
+    _fields_ = [("input", Tensor), ("amax_rowwise", Tensor), ("amax_colwise", Tensor),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64), ("start_offset", ctypes.c_int64)]
+
+
+class CastJob(ctypes.Structure):
+    _fields_ = [("input", Tensor), ("scale_inv_rowwise", Tensor), ("scale_inv_colwise", Tensor),
+                ("output_rowwise", Tensor), ("output_colwise", Tensor),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64)]
+
+
+class ScaleJob(ctypes.Structure):
+    _fields_ = [("amax_rowwise", Tensor), ("amax_colwise", Tensor), ("scale_inv_rowwise", Tensor),
+                ("scale_inv_colwise", Tensor), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
 
 
 def empty_tensor() -> Tensor:
@@ -60,8 +78,14 @@ def load(path: str | None = None):
         lib.mxfp8_amax_max_reduce.argtypes = [T, T, vp]
         lib.mxfp8_update_scales.argtypes = [T, T, T, T, i64, i64, vp]
         lib.mxfp8_partial_cast.argtypes = [T, T, T, T, T, i64, i64, i64, i64, vp]
+        i32 = ctypes.c_int32
+        lib.mxfp8_partial_amax_batched.argtypes = [ctypes.POINTER(AmaxJob), i32, vp]
+        lib.mxfp8_update_scales_batched.argtypes = [ctypes.POINTER(ScaleJob), i32, vp]
+        lib.mxfp8_partial_cast_batched.argtypes = [ctypes.POINTER(CastJob), i32, vp]
         for name in ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
-                     "mxfp8_partial_cast", "mxfp8_version"):
+                     "mxfp8_partial_cast", "mxfp8_partial_amax_batched",
+                     "mxfp8_update_scales_batched", "mxfp8_partial_cast_batched",
+                     "mxfp8_version"):
             getattr(lib, name).restype = ctypes.c_int
         lib.mxfp8_last_error.argtypes = []
         lib.mxfp8_last_error.restype = ctypes.c_char_p

@@ -16,7 +16,7 @@ import ctypes
 import torch
 
 from . import _capi
-from ._capi import DTYPE_BF16, DTYPE_F32, DTYPE_U8, MXFP8Error, Tensor
+from ._capi import DTYPE_BF16, DTYPE_F32, DTYPE_U8, AmaxJob, CastJob, MXFP8Error, ScaleJob, Tensor
 
 _DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.uint8: DTYPE_U8,
            torch.float8_e4m3fn: DTYPE_U8}
@@ -107,6 +107,65 @@ def mxfp8_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwi
           int(start_offset), int(out_offset), _stream(stream, input))
 
 
+def _amax_jobs(jobs):
+    arr = (AmaxJob * max(1, len(jobs)))()
+    keep = []
+    for k, (inp, ar, ac, rows, cols, start) in enumerate(jobs):
+        arr[k] = AmaxJob(handle(inp, "input"), handle(ar, "amax_rowwise"), handle(ac, "amax_colwise"),
+                         int(rows), int(cols), int(start))
+        keep += [t for t in (inp, ar, ac) if t is not None]
+    return arr, keep
+
+
+def _cast_jobs(jobs):
+    arr = (CastJob * max(1, len(jobs)))()
+    keep = []
+    for k, job in enumerate(jobs):
+        inp, sr, sc, qr, qc, rows, cols, start = job[:8]
+        out_offset = job[8] if len(job) > 8 and job[8] is not None else start
+        arr[k] = CastJob(handle(inp, "input"), handle(sr, "scale_inv_rowwise"),
+                         handle(sc, "scale_inv_colwise"), handle(qr, "output_rowwise"),
+                         handle(qc, "output_colwise"), int(rows), int(cols), int(start),
+                         int(out_offset))
+        keep += [t for t in (inp, sr, sc, qr, qc) if t is not None]
+    return arr, keep
+
+
+def _scale_jobs(jobs):
+    arr = (ScaleJob * max(1, len(jobs)))()
+    keep = []
+    for k, (ar, ac, sr, sc, rows, cols) in enumerate(jobs):
+        arr[k] = ScaleJob(handle(ar, "amax_rowwise"), handle(ac, "amax_colwise"),
+                          handle(sr, "scale_inv_rowwise"), handle(sc, "scale_inv_colwise"),
+                          int(rows), int(cols))
+        keep += [t for t in (ar, ac, sr, sc) if t is not None]
+    return arr, keep
+
+
+def mxfp8_partial_amax_batched(jobs, stream=None) -> None:
+    """Many fragments in as few launches as possible.  ``jobs``: sequence of
+    (input, amax_rowwise, amax_colwise, rows, cols, start_offset)."""
+    arr, keep = _amax_jobs(jobs)
+    _call("mxfp8_partial_amax_batched", _device_of(*keep), arr, len(jobs),
+          _stream(stream, keep[0] if keep else None))
+
+
+def mxfp8_update_scales_batched(jobs, stream=None) -> None:
+    """``jobs``: sequence of (amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
+    rows, cols)."""
+    arr, keep = _scale_jobs(jobs)
+    _call("mxfp8_update_scales_batched", _device_of(*keep), arr, len(jobs),
+          _stream(stream, keep[0] if keep else None))
+
+
+def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
+    """``jobs``: sequence of (input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
+    output_colwise, rows, cols, start_offset[, out_offset])."""
+    arr, keep = _cast_jobs(jobs)
+    _call("mxfp8_partial_cast_batched", _device_of(*keep), arr, len(jobs),
+          _stream(stream, keep[0] if keep else None))
+
+
 class Prepared:
     """One library call with its tensor handles marshalled once.
 
@@ -118,10 +177,13 @@ class Prepared:
 
     __slots__ = ("fn", "args", "handles", "tensors", "device")
 
-    def __init__(self, fn_name, handles, scalars, tensors):
+    def __init__(self, fn_name, handles, scalars, tensors, job_array=None):
         self.fn = getattr(_capi.load(), fn_name)
         self.handles = handles
-        self.args = tuple(ctypes.byref(h) for h in handles) + tuple(int(v) for v in scalars)
+        if job_array is not None:  # batched entry: (job array, count)
+            self.args = (job_array, int(scalars[0]))
+        else:
+            self.args = tuple(ctypes.byref(h) for h in handles) + tuple(int(v) for v in scalars)
         self.tensors = tensors
         self.device = _device_of(*tensors)
 
@@ -162,6 +224,21 @@ def prepare_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_row
                                             "output_rowwise", "output_colwise"))]
     return Prepared("mxfp8_partial_cast", hs, (rows, cols, start_offset, out_offset),
                     [t for t in ts if t is not None])
+
+
+def prepare_partial_amax_batched(jobs) -> Prepared:
+    arr, keep = _amax_jobs(jobs)
+    return Prepared("mxfp8_partial_amax_batched", [arr], (len(jobs),), keep, job_array=arr)
+
+
+def prepare_update_scales_batched(jobs) -> Prepared:
+    arr, keep = _scale_jobs(jobs)
+    return Prepared("mxfp8_update_scales_batched", [arr], (len(jobs),), keep, job_array=arr)
+
+
+def prepare_partial_cast_batched(jobs) -> Prepared:
+    arr, keep = _cast_jobs(jobs)
+    return Prepared("mxfp8_partial_cast_batched", [arr], (len(jobs),), keep, job_array=arr)
 
 
 def block_shapes(rows: int, cols: int):

@@ -23,10 +23,39 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowBatch = 8;  // 16-byte loads in flight per lane
+constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
+constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
+constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 constexpr int kMaxDevices = 64;
+#ifndef MXFP8_MIN_BLOCKS
+#define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
+#endif
+
+// Per-row work shared by both tile paths: fold |x| of one chunk into the column
+// maxima and return the maximum of the chunk's 32-element row block (all lanes of
+// the warp must call this together: the row-block maximum is a butterfly).
+template <class T, bool kCol>
+__device__ __forceinline__ uint32_t fold_row(const uint4& chunk, uint4& colmax) {
+  const uint4 a = chunk_abs<T>(chunk);
+  if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
+  return group_max<T>(chunk_reduce<T>(a));
+}
 
 template <class T, bool kCol>
+__device__ __forceinline__ void store_colmax(const AmaxParams& p, int64_t row0, int64_t j,
+                                             const uint4& colmax) {
+  const int64_t base = (row0 >> 5) * p.ld_c + j;
+  if (p.vec_c) {
+    *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = colmax;
+  } else {
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(colmax, k));
+  }
+}
+
+// Whole tile inside the fragment: 16-byte loads (realigned when the fragment's
+// virtual base is not 16-byte aligned), no per-element tests.
+template <class T, bool kCol, bool kShift>
 __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -35,31 +64,25 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const bool writer = (lane % T::G) == 0;
   const int64_t out_r = row0 * p.ld_r + (j >> 5);
+  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
+  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += kRowBatch) {
-    uint4 v[kRowBatch];
+  for (int rb = 0; rb < 32; rb += NB) {
+    uint4 v[NB];
+    load_rows<NB>(v, src + rb * row_bytes, row_bytes, lane, shift);
 #pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) v[r] = ld_stream16(src + (rb + r) * row_bytes);
-#pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) {
-      const uint4 a = chunk_abs<T>(v[r]);
-      if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
-      const uint32_t m = group_max<T>(chunk_reduce<T>(a));
+    for (int r = 0; r < NB; ++r) {
+      const uint32_t m = fold_row<T, kCol>(v[r], colmax);
       if (writer) store_bits<T>(p.amax_r, out_r + (rb + r) * p.ld_r, m);
     }
   }
-  if constexpr (kCol) {
-    const int64_t base = (row0 >> 5) * p.ld_c + j;
-    if (p.vec_c) {
-      *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = colmax;
-    } else {
-#pragma unroll
-      for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(colmax, k));
-    }
-  }
+  if constexpr (kCol) store_colmax<T, kCol>(p, row0, j, colmax);
 }
 
+// Tile cut by the fragment boundary or the matrix edge: per-element predicated
+// loads, issued a batch of rows at a time; only blocks that meet the fragment are
+// written.
 template <class T, bool kCol>
 __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0, int64_t col0,
                                               int lane) {
@@ -68,25 +91,16 @@ __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0,
   const bool writer = (lane % T::G) == 0;
   const int64_t b0 = j & ~int64_t(31);  // first column of this lane's row block
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
-  for (int r = 0; r < 32; ++r) {  // warp-uniform trip count: the butterfly stays converged
-    const int64_t i = row0 + r;
-    uint4 c = make_uint4(0u, 0u, 0u, 0u);
-    if (i < g.rows) {
+#pragma unroll 1
+  for (int rb = 0; rb < 32; rb += kMaskBatch) {  // warp-uniform: the butterfly stays converged
+    uint4 v[kMaskBatch];
+    load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
 #pragma unroll
-      for (int k = 0; k < T::V; ++k) {
-        const int64_t col = j + k;
-        const int64_t f = i * g.cols + col;
-        if (col < g.cols && f >= g.start && f < g.end)
-          chunk_set<T>(c, k, load_bits<T>(p.in, f - g.start));
-      }
-    }
-    const uint4 a = chunk_abs<T>(c);
-    if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
-    const uint32_t m = group_max<T>(chunk_reduce<T>(a));
-    if (writer && i < g.rows && b0 < g.cols) {
-      const int64_t lo = i * g.cols + b0;
-      const int64_t hi = i * g.cols + min(b0 + 32, g.cols);
-      if (meets(lo, hi, g.start, g.end)) store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), m);
+    for (int r = 0; r < kMaskBatch; ++r) {
+      const uint32_t m = fold_row<T, kCol>(v[r], colmax);
+      const int64_t i = row0 + rb + r;
+      if (writer && i < g.rows && b0 < g.cols && row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1)))
+        store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), m);
     }
   }
   if constexpr (kCol) {
@@ -100,50 +114,70 @@ __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0,
   }
 }
 
-template <class T, bool kCol>
-__global__ void __launch_bounds__(kThreads) k_partial_amax(const __grid_constant__ AmaxParams p) {
+template <class T, bool kCol, bool kShift, int N>
+__global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
+    const __grid_constant__ JobBatch<AmaxParams, N> b) {
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
+  const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
   const int64_t stride = int64_t(gridDim.x) * kWarps;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < p.g.ntiles; t += stride) {
-    const int64_t row0 = (p.g.band0 + t / p.g.coltiles) * 32;
-    const int64_t col0 = (t % p.g.coltiles) * TW;
-    const int kind = classify_tile(p.g, row0, col0, TW);
+  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
+    int64_t row0, col0;
+    const AmaxParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
+    const int kind = classify_tile<T>(p.g, row0, col0, TW);
     if (kind == kTileFast) {
-      amax_tile_fast<T, kCol>(p, row0, col0, lane);
+      amax_tile_fast<T, kCol, kShift>(p, row0, col0, lane);
     } else if (kind == kTileMasked) {
       amax_tile_masked<T, kCol>(p, row0, col0, lane);
     }
   }
 }
 
-template <class T, bool kCol>
-cudaError_t launch(const AmaxParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+template <class T, bool kCol, bool kShift, int N>
+cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_partial_amax<T, kCol>,
-                                                                  kThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, k_partial_amax<T, kCol, kShift, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
   }
-  const int64_t want = (p.g.ntiles + kWarps - 1) / kWarps;
-  const int64_t cap = int64_t(dev.sms) * occ;
-  const unsigned grid = unsigned(want < cap ? want : cap);
-  k_partial_amax<T, kCol><<<grid, kThreads, 0, stream>>>(p);
+  JobBatch<AmaxParams, N> b;
+  const int64_t total = fill_batch(b, jobs, n);
+  if (total == 0) return cudaSuccess;
+  const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
+  k_partial_amax<T, kCol, kShift, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
+}
+
+template <class T, bool kCol, bool kShift>
+cudaError_t launch(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n == 1) return launch_n<T, kCol, kShift, 1>(jobs, 1, dev, stream);
+  for (int k = 0; k < n; k += kMaxBatchJobs) {
+    const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
+    const cudaError_t e = launch_n<T, kCol, kShift, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace
 
-cudaError_t launch_partial_amax(const AmaxParams& p, int dtype, bool colwise,
-                                const DeviceInfo& dev, cudaStream_t stream) {
-  if (p.g.ntiles <= 0) return cudaSuccess;
+cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool colwise,
+                                bool shifted, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
   if (dtype == 0) {
-    return colwise ? launch<F32T, true>(p, dev, stream) : launch<F32T, false>(p, dev, stream);
+    if (colwise) return shifted ? launch<F32T, true, true>(jobs, n, dev, stream)
+                                : launch<F32T, true, false>(jobs, n, dev, stream);
+    return shifted ? launch<F32T, false, true>(jobs, n, dev, stream)
+                   : launch<F32T, false, false>(jobs, n, dev, stream);
   }
-  return colwise ? launch<BF16T, true>(p, dev, stream) : launch<BF16T, false>(p, dev, stream);
+  if (colwise) return shifted ? launch<BF16T, true, true>(jobs, n, dev, stream)
+                              : launch<BF16T, true, false>(jobs, n, dev, stream);
+  return shifted ? launch<BF16T, false, true>(jobs, n, dev, stream)
+                 : launch<BF16T, false, false>(jobs, n, dev, stream);
 }
 
 }  // namespace mxfp8

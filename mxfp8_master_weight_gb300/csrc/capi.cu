@@ -122,9 +122,12 @@ FragGeom make_geom(int64_t rows, int64_t cols, int64_t start, int64_t len, int t
   g.end = start + len;
   g.coltiles = int32_t((cols + tw - 1) / tw);
   if (len > 0) {
-    const int64_t r0 = start / cols, r1 = (start + len - 1) / cols;
-    g.band0 = r0 / 32;
-    g.ntiles = (r1 / 32 - g.band0 + 1) * g.coltiles;
+    g.rs = start / cols;
+    g.cs = start % cols;
+    g.re = (start + len - 1) / cols;
+    g.ce = (start + len - 1) % cols;
+    g.band0 = g.rs / 32;
+    g.ntiles = (g.re / 32 - g.band0 + 1) * g.coltiles;
   }
   return g;
 }
@@ -135,53 +138,303 @@ uintptr_t virtual_base(const void* frag, int64_t start, int64_t eb) {
   return reinterpret_cast<uintptr_t>(frag) - uintptr_t(start * eb);
 }
 
+// ---------------------------------------------------------------- per-job preparation
+// Each prep_* validates one job exactly as the single-fragment entry point documents
+// and fills the kernel parameters.  *skip is set for an empty fragment.
+
+int prep_amax(const mxfp8_amax_job& job, AmaxParams* p, int* dtype, bool* colwise, bool* skip) {
+  const mxfp8_tensor* input = &job.input;
+  *skip = false;
+  const bool in_empty = is_empty(input);
+  if (!in_empty) {
+    if (int rc = check_tensor(input, "input")) return rc;
+  }
+  const int64_t len = in_empty ? 0 : numel(input);
+  if (int rc = check_dims(job.rows, job.cols, job.start_offset, len)) return rc;
+  if (len == 0) {
+    *skip = true;
+    return MXFP8_OK;
+  }
+  const int32_t dt = input->dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
+  if (is_empty(&job.amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
+  const int64_t rows = job.rows, cols = job.cols;
+  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
+  if (int rc = check_grid(&job.amax_rowwise, "amax_rowwise", rows, nbr, dt)) return rc;
+  *colwise = !is_empty(&job.amax_colwise);
+  if (*colwise) {
+    if (int rc = check_grid(&job.amax_colwise, "amax_colwise", nbc, cols, dt)) return rc;
+  }
+  const int64_t eb = elem_bytes(dt);
+  const int V = int(16 / eb);
+  *p = AmaxParams{};
+  p->g = make_geom(rows, cols, job.start_offset, len, mxfp8::tile_width_for(dt));
+  p->g.fast_ok = cols % V == 0;
+  p->g.shift = int32_t(virtual_base(input->data, job.start_offset, eb) % 16);
+  p->in = input->data;
+  p->amax_r = job.amax_rowwise.data;
+  p->ld_r = job.amax_rowwise.shape[1];
+  if (*colwise) {
+    p->amax_c = job.amax_colwise.data;
+    p->ld_c = job.amax_colwise.shape[1];
+    p->vec_c = (reinterpret_cast<uintptr_t>(p->amax_c) % 16 == 0) && (p->ld_c % V == 0);
+  }
+  *dtype = dt == MXFP8_DTYPE_F32 ? 0 : 1;
+  return MXFP8_OK;
+}
+
+int prep_cast(const mxfp8_cast_job& job, CastParams* p, int* dtype, bool* colwise, bool* skip) {
+  const mxfp8_tensor* input = &job.input;
+  *skip = false;
+  const bool in_empty = is_empty(input);
+  if (!in_empty) {
+    if (int rc = check_tensor(input, "input")) return rc;
+  }
+  const int64_t len = in_empty ? 0 : numel(input);
+  if (int rc = check_dims(job.rows, job.cols, job.start_offset, len)) return rc;
+  if (job.out_offset < 0) return fail(MXFP8_ERR_INVALID, "out_offset must be non-negative");
+  if (len == 0) {
+    *skip = true;
+    return MXFP8_OK;
+  }
+  const int32_t dt = input->dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
+  if (is_empty(&job.scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
+  if (is_empty(&job.output_rowwise)) return fail(MXFP8_ERR_MISSING, "output_rowwise is required");
+  const int64_t rows = job.rows, cols = job.cols, out_offset = job.out_offset;
+  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
+  if (int rc = check_grid(&job.scale_inv_rowwise, "scale_inv_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
+  const mxfp8_tensor* out_r = &job.output_rowwise;
+  if (int rc = check_tensor(out_r, "output_rowwise")) return rc;
+  if (out_r->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "output_rowwise: dtype must be U8");
+  if (numel(out_r) - len < out_offset)
+    return fail(MXFP8_ERR_SHAPE, "output_rowwise holds %lld bytes, needs out_offset + len = %lld",
+                (long long)numel(out_r), (long long)(out_offset + len));
+  *colwise = !is_empty(&job.output_colwise);
+  const mxfp8_tensor* out_c = &job.output_colwise;
+  if (*colwise) {
+    if (int rc = check_tensor(out_c, "output_colwise")) return rc;
+    if (out_c->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "output_colwise: dtype must be U8");
+    if (numel(out_c) - len < out_offset)
+      return fail(MXFP8_ERR_SHAPE, "output_colwise holds %lld bytes, needs out_offset + len = %lld",
+                  (long long)numel(out_c), (long long)(out_offset + len));
+    if (is_empty(&job.scale_inv_colwise))
+      return fail(MXFP8_ERR_MISSING, "scale_inv_colwise is required when output_colwise is present");
+    if (int rc = check_grid(&job.scale_inv_colwise, "scale_inv_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
+  }
+  const int64_t eb = elem_bytes(dt);
+  const int V = int(16 / eb);
+  const int64_t shift = out_offset - job.start_offset;
+  *p = CastParams{};
+  p->g = make_geom(rows, cols, job.start_offset, len, mxfp8::tile_width_for(dt));
+  p->g.fast_ok = cols % V == 0;
+  p->g.shift = int32_t(virtual_base(input->data, job.start_offset, eb) % 16);
+  p->in = input->data;
+  p->s_r = static_cast<const uint8_t*>(job.scale_inv_rowwise.data);
+  p->ld_sr = job.scale_inv_rowwise.shape[1];
+  p->out_r = static_cast<uint8_t*>(out_r->data);
+  p->out_shift = shift;
+  bool vec_out = (reinterpret_cast<uintptr_t>(p->out_r) + uintptr_t(shift)) % uintptr_t(V) == 0;
+  if (*colwise) {
+    p->s_c = static_cast<const uint8_t*>(job.scale_inv_colwise.data);
+    p->ld_sc = job.scale_inv_colwise.shape[1];
+    p->out_c = static_cast<uint8_t*>(out_c->data);
+    vec_out = vec_out && ((reinterpret_cast<uintptr_t>(p->out_c) + uintptr_t(shift)) % uintptr_t(V) == 0);
+    p->vec_sc = (reinterpret_cast<uintptr_t>(p->s_c) % uintptr_t(V) == 0) && (p->ld_sc % V == 0);
+  }
+  p->vec_out = vec_out;
+  *dtype = dt == MXFP8_DTYPE_F32 ? 0 : 1;
+  return MXFP8_OK;
+}
+
+int prep_scales(const mxfp8_scale_job& job, ScaleSegment* segs, int* nseg, int* dtype) {
+  const int64_t rows = job.rows, cols = job.cols;
+  if (rows <= 0 || cols <= 0) return fail(MXFP8_ERR_INVALID, "rows and cols must be positive");
+  if (rows > INT64_MAX / cols) return fail(MXFP8_ERR_INVALID, "rows*cols overflows int64");
+  if (is_empty(&job.amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
+  if (is_empty(&job.scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
+  const int32_t dt = job.amax_rowwise.dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "amax_rowwise: dtype must be F32 or BF16");
+  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
+  if (int rc = check_grid(&job.amax_rowwise, "amax_rowwise", rows, nbr, dt)) return rc;
+  if (int rc = check_grid(&job.scale_inv_rowwise, "scale_inv_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
+  const bool colwise = !is_empty(&job.amax_colwise);
+  if (colwise) {
+    if (int rc = check_grid(&job.amax_colwise, "amax_colwise", nbc, cols, dt)) return rc;
+    if (is_empty(&job.scale_inv_colwise))
+      return fail(MXFP8_ERR_MISSING, "scale_inv_colwise is required when amax_colwise is present");
+    if (int rc = check_grid(&job.scale_inv_colwise, "scale_inv_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
+  }
+  const int64_t eb = elem_bytes(dt);
+  auto seg = [&](const mxfp8_tensor* a, const mxfp8_tensor* sc, int64_t nr, int64_t nc) {
+    ScaleSegment g{};
+    g.amax = a->data;
+    g.scale = static_cast<uint8_t*>(sc->data);
+    g.nrows = nr;
+    g.ncols = nc;
+    g.ld_a = a->shape[1];
+    g.ld_s = sc->shape[1];
+    g.vec = (g.ld_a == nc) && (g.ld_s == nc) && ((nr * nc) % 4 == 0) &&
+            (reinterpret_cast<uintptr_t>(g.amax) % uintptr_t(4 * eb) == 0) &&
+            (reinterpret_cast<uintptr_t>(g.scale) % 4 == 0);
+    return g;
+  };
+  *nseg = 0;
+  segs[(*nseg)++] = seg(&job.amax_rowwise, &job.scale_inv_rowwise, rows, nbr);
+  if (colwise) segs[(*nseg)++] = seg(&job.amax_colwise, &job.scale_inv_colwise, nbc, cols);
+  *dtype = dt == MXFP8_DTYPE_F32 ? 0 : 1;
+  return MXFP8_OK;
+}
+
+// Prefix the last error message with the failing job's index.
+int job_fail(int rc, int k) {
+  char tmp[sizeof g_err];
+  std::snprintf(tmp, sizeof tmp, "job %d: %s", k, g_err);
+  std::snprintf(g_err, sizeof g_err, "%s", tmp);
+  return rc;
+}
+
+constexpr int kGroupChunk = mxfp8::kMaxBatchJobs;
+constexpr int kWindow = 64;  // jobs prepared at a time (host stack, no heap)
+
+// ---------------------------------------------------------------- batched drivers
+// Validate every job first (a failure launches nothing), then, window by window,
+// launch one kernel per (dtype, direction set, alignment class) group, at most
+// kMaxBatchJobs jobs per launch.
+
+int run_amax(const mxfp8_amax_job* jobs, int32_t njobs, void* stream) {
+  if (njobs < 0 || (njobs > 0 && jobs == nullptr)) return fail(MXFP8_ERR_INVALID, "bad job array");
+  AmaxParams win[kWindow];
+  int key[kWindow];
+  int dt;
+  bool col, skip;
+  int live = 0;
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_amax(jobs[k], &win[0], &dt, &col, &skip)) return njobs > 1 ? job_fail(rc, k) : rc;
+    live += !skip;
+  }
+  if (live == 0) return ok();
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  AmaxParams batch[kGroupChunk];
+  for (int base = 0; base < njobs; base += kWindow) {
+    const int m = njobs - base < kWindow ? njobs - base : kWindow;
+    for (int i = 0; i < m; ++i) {
+      prep_amax(jobs[base + i], &win[i], &dt, &col, &skip);
+      key[i] = skip ? -1 : dt * 4 + col * 2 + (win[i].g.shift != 0);
+    }
+    for (int kk = 0; kk < 8; ++kk) {  // dtype x colwise x shifted
+      int n = 0;
+      for (int i = 0; i <= m; ++i) {
+        if (i < m && key[i] == kk) batch[n++] = win[i];
+        if (n > 0 && (n == kGroupChunk || i == m)) {
+          if (int rc = cuda_status(mxfp8::launch_partial_amax(batch, n, kk >> 2, (kk >> 1) & 1, kk & 1,
+                                                              dev, static_cast<cudaStream_t>(stream)),
+                                   "partial amax launch"))
+            return rc;
+          n = 0;
+        }
+      }
+    }
+  }
+  return ok();
+}
+
+int run_cast(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
+  if (njobs < 0 || (njobs > 0 && jobs == nullptr)) return fail(MXFP8_ERR_INVALID, "bad job array");
+  CastParams win[kWindow];
+  int key[kWindow];
+  int dt;
+  bool col, skip;
+  int live = 0;
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_cast(jobs[k], &win[0], &dt, &col, &skip)) return njobs > 1 ? job_fail(rc, k) : rc;
+    live += !skip;
+  }
+  if (live == 0) return ok();
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  CastParams batch[kGroupChunk];
+  for (int base = 0; base < njobs; base += kWindow) {
+    const int m = njobs - base < kWindow ? njobs - base : kWindow;
+    for (int i = 0; i < m; ++i) {
+      prep_cast(jobs[base + i], &win[i], &dt, &col, &skip);
+      key[i] = skip ? -1 : dt * 8 + col * 4 + (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+    }
+    for (int kk = 0; kk < 16; ++kk) {  // dtype x colwise x shifted x aligned output
+      int n = 0;
+      for (int i = 0; i <= m; ++i) {
+        if (i < m && key[i] == kk) batch[n++] = win[i];
+        if (n > 0 && (n == kGroupChunk || i == m)) {
+          if (int rc = cuda_status(mxfp8::launch_partial_cast(batch, n, kk >> 3, (kk >> 2) & 1,
+                                                              (kk >> 1) & 1, kk & 1, dev,
+                                                              static_cast<cudaStream_t>(stream)),
+                                   "partial cast launch"))
+            return rc;
+          n = 0;
+        }
+      }
+    }
+  }
+  return ok();
+}
+
+int run_scales(const mxfp8_scale_job* jobs, int32_t njobs, void* stream) {
+  if (njobs < 0 || (njobs > 0 && jobs == nullptr)) return fail(MXFP8_ERR_INVALID, "bad job array");
+  ScaleSegment segs[2];
+  int nseg, dt;
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_scales(jobs[k], segs, &nseg, &dt)) return njobs > 1 ? job_fail(rc, k) : rc;
+  }
+  if (njobs == 0) return ok();
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  ScaleSegment batch[2 * kGroupChunk];
+  for (int kdt = 0; kdt < 2; ++kdt) {
+    int n = 0;
+    for (int k = 0; k <= njobs; ++k) {
+      if (k < njobs) {
+        prep_scales(jobs[k], segs, &nseg, &dt);
+        if (dt == kdt)
+          for (int q = 0; q < nseg; ++q) batch[n++] = segs[q];
+      }
+      if (n > 0 && (n > 2 * kGroupChunk - 2 || k == njobs)) {
+        if (int rc = cuda_status(mxfp8::launch_update_scales(batch, n, kdt, dev,
+                                                             static_cast<cudaStream_t>(stream)),
+                                 "update scales launch"))
+          return rc;
+        n = 0;
+      }
+    }
+  }
+  return ok();
+}
+
+const mxfp8_tensor kEmpty = {nullptr, MXFP8_DTYPE_U8, 1, {0, 0}};
+
+const mxfp8_tensor& or_empty(const mxfp8_tensor* t) { return t ? *t : kEmpty; }
+
 }  // namespace
 
 extern "C" {
 
 const char* mxfp8_last_error(void) { return g_err; }
 
-int mxfp8_version(void) { return 100; }
+int mxfp8_version(void) { return 200; }
 
 int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
                        mxfp8_tensor* amax_colwise, int64_t rows, int64_t cols,
                        int64_t start_offset, void* stream) {
-  const bool in_empty = is_empty(input);
-  if (!in_empty) {
-    if (int rc = check_tensor(input, "input")) return rc;
-  }
-  const int64_t len = in_empty ? 0 : numel(input);
-  if (int rc = check_dims(rows, cols, start_offset, len)) return rc;
-  if (len == 0) return ok();
-  const int32_t dt = input->dtype;
-  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
-    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
-  if (is_empty(amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
-  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
-  if (int rc = check_grid(amax_rowwise, "amax_rowwise", rows, nbr, dt)) return rc;
-  const bool colwise = !is_empty(amax_colwise);
-  if (colwise) {
-    if (int rc = check_grid(amax_colwise, "amax_colwise", nbc, cols, dt)) return rc;
-  }
-  DeviceInfo dev;
-  if (int rc = device_info(&dev)) return rc;
+  const mxfp8_amax_job job = {or_empty(input), or_empty(amax_rowwise), or_empty(amax_colwise),
+                              rows, cols, start_offset};
+  return run_amax(&job, 1, stream);
+}
 
-  const int64_t eb = elem_bytes(dt);
-  const int V = int(16 / eb);
-  AmaxParams p{};
-  p.g = make_geom(rows, cols, start_offset, len, mxfp8::tile_width_for(dt));
-  p.g.fast_ok = (virtual_base(input->data, start_offset, eb) % 16 == 0) && (cols % V == 0);
-  p.in = input->data;
-  p.amax_r = amax_rowwise->data;
-  p.ld_r = amax_rowwise->shape[1];
-  if (colwise) {
-    p.amax_c = amax_colwise->data;
-    p.ld_c = amax_colwise->shape[1];
-    p.vec_c = (reinterpret_cast<uintptr_t>(p.amax_c) % 16 == 0) && (p.ld_c % V == 0);
-  }
-  return cuda_status(mxfp8::launch_partial_amax(p, dt == MXFP8_DTYPE_F32 ? 0 : 1, colwise, dev,
-                                                static_cast<cudaStream_t>(stream)),
-                     "partial amax launch");
+int mxfp8_partial_amax_batched(const mxfp8_amax_job* jobs, int32_t njobs, void* stream) {
+  return run_amax(jobs, njobs, stream);
 }
 
 int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* stream) {
@@ -212,109 +465,27 @@ int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* st
 int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
                         mxfp8_tensor* scale_inv_rowwise, mxfp8_tensor* scale_inv_colwise,
                         int64_t rows, int64_t cols, void* stream) {
-  if (rows <= 0 || cols <= 0) return fail(MXFP8_ERR_INVALID, "rows and cols must be positive");
-  if (rows > INT64_MAX / cols) return fail(MXFP8_ERR_INVALID, "rows*cols overflows int64");
-  if (is_empty(amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
-  if (is_empty(scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
-  const int32_t dt = amax_rowwise->dtype;
-  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
-    return fail(MXFP8_ERR_DTYPE, "amax_rowwise: dtype must be F32 or BF16");
-  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
-  if (int rc = check_grid(amax_rowwise, "amax_rowwise", rows, nbr, dt)) return rc;
-  if (int rc = check_grid(scale_inv_rowwise, "scale_inv_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
-  const bool colwise = !is_empty(amax_colwise);
-  if (colwise) {
-    if (int rc = check_grid(amax_colwise, "amax_colwise", nbc, cols, dt)) return rc;
-    if (is_empty(scale_inv_colwise))
-      return fail(MXFP8_ERR_MISSING, "scale_inv_colwise is required when amax_colwise is present");
-    if (int rc = check_grid(scale_inv_colwise, "scale_inv_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
-  }
-  DeviceInfo dev;
-  if (int rc = device_info(&dev)) return rc;
-  const int64_t eb = elem_bytes(dt);
-  auto seg = [&](const mxfp8_tensor* a, mxfp8_tensor* s, int64_t nr, int64_t nc) {
-    ScaleSegment g{};
-    g.amax = a->data;
-    g.scale = static_cast<uint8_t*>(s->data);
-    g.nrows = nr;
-    g.ncols = nc;
-    g.ld_a = a->shape[1];
-    g.ld_s = s->shape[1];
-    g.vec = (g.ld_a == nc) && (g.ld_s == nc) && ((nr * nc) % 4 == 0) &&
-            (reinterpret_cast<uintptr_t>(g.amax) % uintptr_t(4 * eb) == 0) &&
-            (reinterpret_cast<uintptr_t>(g.scale) % 4 == 0);
-    return g;
-  };
-  ScaleSegment segs[2];
-  int nseg = 0;
-  segs[nseg++] = seg(amax_rowwise, scale_inv_rowwise, rows, nbr);
-  if (colwise) segs[nseg++] = seg(amax_colwise, scale_inv_colwise, nbc, cols);
-  return cuda_status(mxfp8::launch_update_scales(segs, nseg, dt == MXFP8_DTYPE_F32 ? 0 : 1, dev,
-                                                 static_cast<cudaStream_t>(stream)),
-                     "update scales launch");
+  const mxfp8_scale_job job = {or_empty(amax_rowwise), or_empty(amax_colwise),
+                               or_empty(scale_inv_rowwise), or_empty(scale_inv_colwise), rows, cols};
+  return run_scales(&job, 1, stream);
+}
+
+int mxfp8_update_scales_batched(const mxfp8_scale_job* jobs, int32_t njobs, void* stream) {
+  return run_scales(jobs, njobs, stream);
 }
 
 int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_rowwise,
                        const mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
                        mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                        int64_t start_offset, int64_t out_offset, void* stream) {
-  const bool in_empty = is_empty(input);
-  if (!in_empty) {
-    if (int rc = check_tensor(input, "input")) return rc;
-  }
-  const int64_t len = in_empty ? 0 : numel(input);
-  if (int rc = check_dims(rows, cols, start_offset, len)) return rc;
-  if (out_offset < 0) return fail(MXFP8_ERR_INVALID, "out_offset must be non-negative");
-  if (len == 0) return ok();
-  const int32_t dt = input->dtype;
-  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
-    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
-  if (is_empty(scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
-  if (is_empty(output_rowwise)) return fail(MXFP8_ERR_MISSING, "output_rowwise is required");
-  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
-  if (int rc = check_grid(scale_inv_rowwise, "scale_inv_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
-  if (int rc = check_tensor(output_rowwise, "output_rowwise")) return rc;
-  if (output_rowwise->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "output_rowwise: dtype must be U8");
-  if (numel(output_rowwise) - len < out_offset)
-    return fail(MXFP8_ERR_SHAPE, "output_rowwise holds %lld bytes, needs out_offset + len = %lld",
-                (long long)numel(output_rowwise), (long long)(out_offset + len));
-  const bool colwise = !is_empty(output_colwise);
-  if (colwise) {
-    if (int rc = check_tensor(output_colwise, "output_colwise")) return rc;
-    if (output_colwise->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "output_colwise: dtype must be U8");
-    if (numel(output_colwise) - len < out_offset)
-      return fail(MXFP8_ERR_SHAPE, "output_colwise holds %lld bytes, needs out_offset + len = %lld",
-                  (long long)numel(output_colwise), (long long)(out_offset + len));
-    if (is_empty(scale_inv_colwise))
-      return fail(MXFP8_ERR_MISSING, "scale_inv_colwise is required when output_colwise is present");
-    if (int rc = check_grid(scale_inv_colwise, "scale_inv_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
-  }
-  DeviceInfo dev;
-  if (int rc = device_info(&dev)) return rc;
+  const mxfp8_cast_job job = {or_empty(input), or_empty(scale_inv_rowwise),
+                              or_empty(scale_inv_colwise), or_empty(output_rowwise),
+                              or_empty(output_colwise), rows, cols, start_offset, out_offset};
+  return run_cast(&job, 1, stream);
+}
 
-  const int64_t eb = elem_bytes(dt);
-  const int V = int(16 / eb);
-  const int64_t shift = out_offset - start_offset;
-  CastParams p{};
-  p.g = make_geom(rows, cols, start_offset, len, mxfp8::tile_width_for(dt));
-  p.in = input->data;
-  p.s_r = static_cast<const uint8_t*>(scale_inv_rowwise->data);
-  p.ld_sr = scale_inv_rowwise->shape[1];
-  p.out_r = static_cast<uint8_t*>(output_rowwise->data);
-  p.out_shift = shift;
-  bool fast = (virtual_base(input->data, start_offset, eb) % 16 == 0) && (cols % V == 0) &&
-              ((reinterpret_cast<uintptr_t>(p.out_r) + uintptr_t(shift)) % uintptr_t(V) == 0);
-  if (colwise) {
-    p.s_c = static_cast<const uint8_t*>(scale_inv_colwise->data);
-    p.ld_sc = scale_inv_colwise->shape[1];
-    p.out_c = static_cast<uint8_t*>(output_colwise->data);
-    fast = fast && ((reinterpret_cast<uintptr_t>(p.out_c) + uintptr_t(shift)) % uintptr_t(V) == 0);
-    p.vec_sc = (reinterpret_cast<uintptr_t>(p.s_c) % uintptr_t(V) == 0) && (p.ld_sc % V == 0);
-  }
-  p.g.fast_ok = fast;
-  return cuda_status(mxfp8::launch_partial_cast(p, dt == MXFP8_DTYPE_F32 ? 0 : 1, colwise, dev,
-                                                static_cast<cudaStream_t>(stream)),
-                     "partial cast launch");
+int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
+  return run_cast(jobs, njobs, stream);
 }
 
 }  // extern "C"

@@ -22,8 +22,13 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowBatch = 8;
+constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
+constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
+constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 constexpr int kMaxDevices = 64;
+#ifndef MXFP8_MIN_BLOCKS
+#define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
+#endif
 
 // Model-dtype values of one input chunk.
 template <class T>
@@ -39,38 +44,63 @@ __device__ __forceinline__ void model_values(const uint4& c, float (&y)[T::V]) {
   }
 }
 
-// Model-dtype value of one element given as a bit pattern.
+// V E4M3 bytes of y[k] * mult[k] (element k in byte k).
 template <class T>
-__device__ __forceinline__ float model_value(uint32_t bits) {
-  if constexpr (T::kBytes == 4) {
-    return bf16_lo(bf16x2_rn(__uint_as_float(bits), 0.0f));
-  } else {
-    return __uint_as_float(bits << 16);
-  }
-}
-
-__device__ __forceinline__ uint8_t quantize1(float y, float mult) {
-  return static_cast<uint8_t>(e4m3x2_rn_sat(y * mult, 0.0f) & 0xffu);
-}
-
-// V E4M3 bytes of y[k] * mult[k], stored as one 4- or 8-byte word.
-template <class T>
-__device__ __forceinline__ void store_q(uint8_t* dst, const float (&y)[T::V], const float (&mult)[T::V]) {
-  if constexpr (T::V == 4) {
-    const uint32_t q = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
-                       (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
-    *reinterpret_cast<uint32_t*>(dst) = q;
-  } else {
-    uint2 q;
-    q.x = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
-          (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
+__device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
+  uint2 q;
+  q.x = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
+        (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
+  if constexpr (T::V == 8) {
     q.y = e4m3x2_rn_sat(y[4] * mult[4], y[5] * mult[5]) |
           (e4m3x2_rn_sat(y[6] * mult[6], y[7] * mult[7]) << 16);
-    *reinterpret_cast<uint2*>(dst) = q;
+  } else {
+    q.y = 0;
+  }
+  return q;
+}
+
+// Store V bytes: one 4- or 8-byte word when the destination is aligned, else bytes.
+template <class T, bool kVec>
+__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint2& q) {
+  if constexpr (kVec) {
+    if constexpr (T::V == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = q.x;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = q;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) dst[k] = static_cast<uint8_t>((k < 4 ? q.x : q.y) >> (8 * (k & 3)));
   }
 }
 
-template <class T, bool kCol>
+// Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
+template <class T>
+__device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t row0, int64_t j,
+                                                    float (&mc)[T::V]) {
+  const uint8_t* sc = p.s_c + (row0 >> 5) * p.ld_sc + j;
+  if (p.vec_sc) {
+    if constexpr (T::V == 4) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(sc);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mc[k] = scale_multiplier((w >> (8 * k)) & 0xffu);
+    } else {
+      const uint2 w = *reinterpret_cast<const uint2*>(sc);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        mc[k] = scale_multiplier((w.x >> (8 * k)) & 0xffu);
+        mc[k + 4] = scale_multiplier((w.y >> (8 * k)) & 0xffu);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) mc[k] = scale_multiplier(sc[k]);
+  }
+}
+
+// Whole tile inside the fragment: 16-byte loads (realigned for a shifted virtual
+// base), one scale byte per row, word stores when the outputs are aligned.
+template <class T, bool kCol, bool kShift, bool kVec>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -79,38 +109,19 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const uint8_t* srow = p.s_r + row0 * p.ld_sr + (j >> 5);
   const int64_t o0 = row0 * cols + j + p.out_shift;
+  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
+  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
   float mc[T::V];
-  if constexpr (kCol) {
-    const uint8_t* sc = p.s_c + (row0 >> 5) * p.ld_sc + j;
-    if (p.vec_sc) {
-      if constexpr (T::V == 4) {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(sc);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) mc[k] = scale_multiplier((w >> (8 * k)) & 0xffu);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2*>(sc);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          mc[k] = scale_multiplier((w.x >> (8 * k)) & 0xffu);
-          mc[k + 4] = scale_multiplier((w.y >> (8 * k)) & 0xffu);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int k = 0; k < T::V; ++k) mc[k] = scale_multiplier(sc[k]);
-    }
-  }
+  if constexpr (kCol) colwise_multipliers<T>(p, row0, j, mc);
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += kRowBatch) {
-    uint4 v[kRowBatch];
-    uint32_t sb[kRowBatch];
+  for (int rb = 0; rb < 32; rb += NB) {
+    uint4 v[NB];
+    uint32_t sb[NB];
 #pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) {
-      v[r] = ld_stream16(src + (rb + r) * row_bytes);
-      sb[r] = srow[(rb + r) * p.ld_sr];
-    }
+    for (int r = 0; r < NB; ++r) sb[r] = srow[(rb + r) * p.ld_sr];
+    load_rows<NB>(v, src + rb * row_bytes, row_bytes, lane, shift);
 #pragma unroll
-    for (int r = 0; r < kRowBatch; ++r) {
+    for (int r = 0; r < NB; ++r) {
       float y[T::V];
       model_values<T>(v[r], y);
       float mr[T::V];
@@ -118,78 +129,145 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const int64_t o = o0 + (rb + r) * cols;
-      store_q<T>(p.out_r + o, y, mr);
-      if constexpr (kCol) store_q<T>(p.out_c + o, y, mc);
+      store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
+      if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
     }
   }
 }
 
-template <class T, bool kCol>
+// Tile cut by the fragment boundary or the matrix edge: loads a batch of rows at a
+// time (16-byte loads for chunks wholly inside the fragment, predicated per-element
+// loads otherwise), one scale byte per row and block, and stores only the
+// fragment's elements (a word per whole chunk when the output is aligned).
+template <class T, bool kCol, bool kVec>
 __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0, int64_t col0,
                                               int lane) {
+  constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
-  const int64_t r_end = min(row0 + 32, g.rows);
-  for (int64_t i = row0; i < r_end; ++i) {
+  if (j >= g.cols) return;  // no element of this lane is inside the matrix
+  const bool word_ok = kVec && g.fast_ok;  // whole chunks sit on V-aligned output addresses
+  const int64_t blk = j >> 5;              // the lane's V columns share one row block
+  float mc[T::V];
+  if constexpr (kCol) {
 #pragma unroll
-    for (int k = 0; k < T::V; ++k) {
-      const int64_t col = j + k;
-      const int64_t f = i * g.cols + col;
-      if (col < g.cols && f >= g.start && f < g.end) {
-        const float y = model_value<T>(load_bits<T>(p.in, f - g.start));
-        p.out_r[f + p.out_shift] = quantize1(y, scale_multiplier(p.s_r[i * p.ld_sr + (col >> 5)]));
-        if constexpr (kCol)
-          p.out_c[f + p.out_shift] =
-              quantize1(y, scale_multiplier(p.s_c[(i >> 5) * p.ld_sc + col]));
+    for (int k = 0; k < T::V; ++k)
+      mc[k] = j + k < g.cols ? scale_multiplier(p.s_c[(row0 >> 5) * p.ld_sc + j + k]) : 0.0f;
+  }
+#pragma unroll 1
+  for (int rb = 0; rb < 32 && row0 + rb < g.rows; rb += kMaskBatch) {
+    uint4 v[kMaskBatch];
+    const uint64_t valid = load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+    if (valid == 0) continue;
+    float mrow[kMaskBatch];
+#pragma unroll
+    for (int r = 0; r < kMaskBatch; ++r) {
+      const int64_t i = row0 + rb + r;
+      mrow[r] = ((valid >> (r * T::V)) & kChunkBits) ? scale_multiplier(p.s_r[i * p.ld_sr + blk]) : 0.0f;
+    }
+#pragma unroll
+    for (int r = 0; r < kMaskBatch; ++r) {
+      const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
+      if (bits == 0) continue;
+      const int64_t i = row0 + rb + r;
+      float y[T::V];
+      model_values<T>(v[r], y);
+      float mr[T::V];
+#pragma unroll
+      for (int k = 0; k < T::V; ++k) mr[k] = mrow[r];
+      const uint2 qr = quantize_chunk<T>(y, mr);
+      uint2 qc = make_uint2(0u, 0u);
+      if constexpr (kCol) qc = quantize_chunk<T>(y, mc);
+      const int64_t o = i * g.cols + j + p.out_shift;
+      if (word_ok && bits == kChunkBits) {
+        store_chunk<T, true>(p.out_r + o, qr);
+        if constexpr (kCol) store_chunk<T, true>(p.out_c + o, qc);
+      } else {
+#pragma unroll
+        for (int k = 0; k < T::V; ++k) {
+          if (bits & (uint64_t(1) << k)) {
+            const int sh = 8 * (k & 3);
+            p.out_r[o + k] = static_cast<uint8_t>((k < 4 ? qr.x : qr.y) >> sh);
+            if constexpr (kCol) p.out_c[o + k] = static_cast<uint8_t>((k < 4 ? qc.x : qc.y) >> sh);
+          }
+        }
       }
     }
   }
 }
 
-template <class T, bool kCol>
-__global__ void __launch_bounds__(kThreads) k_partial_cast(const __grid_constant__ CastParams p) {
+template <class T, bool kCol, bool kShift, bool kVec, int N>
+__global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
+    const __grid_constant__ JobBatch<CastParams, N> b) {
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
+  const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
   const int64_t stride = int64_t(gridDim.x) * kWarps;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < p.g.ntiles; t += stride) {
-    const int64_t row0 = (p.g.band0 + t / p.g.coltiles) * 32;
-    const int64_t col0 = (t % p.g.coltiles) * TW;
-    const int kind = classify_tile(p.g, row0, col0, TW);
+  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
+    int64_t row0, col0;
+    const CastParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
+    const int kind = classify_tile<T>(p.g, row0, col0, TW);
     if (kind == kTileFast) {
-      cast_tile_fast<T, kCol>(p, row0, col0, lane);
+      cast_tile_fast<T, kCol, kShift, kVec>(p, row0, col0, lane);
     } else if (kind == kTileMasked) {
-      cast_tile_masked<T, kCol>(p, row0, col0, lane);
+      cast_tile_masked<T, kCol, kVec>(p, row0, col0, lane);
     }
   }
 }
 
-template <class T, bool kCol>
-cudaError_t launch(const CastParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+template <class T, bool kCol, bool kShift, bool kVec, int N>
+cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_partial_cast<T, kCol>,
-                                                                  kThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, k_partial_cast<T, kCol, kShift, kVec, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
   }
-  const int64_t want = (p.g.ntiles + kWarps - 1) / kWarps;
-  const int64_t cap = int64_t(dev.sms) * occ;
-  const unsigned grid = unsigned(want < cap ? want : cap);
-  k_partial_cast<T, kCol><<<grid, kThreads, 0, stream>>>(p);
+  JobBatch<CastParams, N> b;
+  const int64_t total = fill_batch(b, jobs, n);
+  if (total == 0) return cudaSuccess;
+  const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
+  k_partial_cast<T, kCol, kShift, kVec, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
+}
+
+template <class T, bool kCol, bool kShift, bool kVec>
+cudaError_t launch(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n == 1) return launch_n<T, kCol, kShift, kVec, 1>(jobs, 1, dev, stream);
+  for (int k = 0; k < n; k += kMaxBatchJobs) {
+    const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
+    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <class T, bool kCol>
+cudaError_t launch_variant(const CastParams* jobs, int n, bool shifted, bool vec_out,
+                           const DeviceInfo& dev, cudaStream_t stream) {
+  if (shifted) {
+    return vec_out ? launch<T, kCol, true, true>(jobs, n, dev, stream)
+                   : launch<T, kCol, true, false>(jobs, n, dev, stream);
+  }
+  return vec_out ? launch<T, kCol, false, true>(jobs, n, dev, stream)
+                 : launch<T, kCol, false, false>(jobs, n, dev, stream);
 }
 
 }  // namespace
 
-cudaError_t launch_partial_cast(const CastParams& p, int dtype, bool colwise,
-                                const DeviceInfo& dev, cudaStream_t stream) {
-  if (p.g.ntiles <= 0) return cudaSuccess;
+cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
+                                bool shifted, bool vec_out, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
   if (dtype == 0) {
-    return colwise ? launch<F32T, true>(p, dev, stream) : launch<F32T, false>(p, dev, stream);
+    return colwise ? launch_variant<F32T, true>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<F32T, false>(jobs, n, shifted, vec_out, dev, stream);
   }
-  return colwise ? launch<BF16T, true>(p, dev, stream) : launch<BF16T, false>(p, dev, stream);
+  return colwise ? launch_variant<BF16T, true>(jobs, n, shifted, vec_out, dev, stream)
+                 : launch_variant<BF16T, false>(jobs, n, shifted, vec_out, dev, stream);
 }
 
 }  // namespace mxfp8

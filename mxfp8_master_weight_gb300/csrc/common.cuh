@@ -166,23 +166,40 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------- fragment geometry
-// True when the flat range [a, b) meets the fragment [start, end).
-__device__ __forceinline__ bool meets(int64_t a, int64_t b, int64_t start, int64_t end) {
-  return (a < b) && (a < end) && (start < b);
+// The fragment is every element from (rs, cs) to (re, ce) in row-major order, so row
+// i holds fragment columns [row_lo(i), row_hi(i)] (empty when i is outside
+// [rs, re]) and column c holds fragment rows [col_lo(c), col_hi(c)].
+__device__ __forceinline__ int64_t row_lo(const FragGeom& g, int64_t i) {
+  return i == g.rs ? g.cs : 0;
+}
+__device__ __forceinline__ int64_t row_hi(const FragGeom& g, int64_t i) {
+  return i == g.re ? g.ce : g.cols - 1;
+}
+__device__ __forceinline__ bool row_in(const FragGeom& g, int64_t i) {
+  return i >= g.rs && i <= g.re;
 }
 
-// True when column `col` has a fragment element in rows [r_a, r_b).
-__device__ __forceinline__ bool column_meets(const FragGeom& g, int64_t col, int64_t r_a,
+// True when columns [c0, c1] of row i hold a fragment element.
+__device__ __forceinline__ bool row_span_meets(const FragGeom& g, int64_t i, int64_t c0,
+                                               int64_t c1) {
+  return row_in(g, i) && max(c0, row_lo(g, i)) <= min(c1, row_hi(g, i));
+}
+
+// True when column c has a fragment element in rows [r_a, r_b).
+__device__ __forceinline__ bool column_meets(const FragGeom& g, int64_t c, int64_t r_a,
                                              int64_t r_b) {
-  // rows r with start <= r*cols + col < end form one interval [lo, hi]
-  const int64_t lo = g.start > col ? (g.start - col + g.cols - 1) / g.cols : 0;
-  const int64_t hi = g.end - 1 >= col ? (g.end - 1 - col) / g.cols : -1;
+  const int64_t lo = c >= g.cs ? g.rs : g.rs + 1;
+  const int64_t hi = c <= g.ce ? g.re : g.re - 1;
   return max(lo, r_a) <= min(hi, r_b - 1);
 }
 
 enum TileKind { kTileSkip = 0, kTileFast = 1, kTileMasked = 2 };
 
 // Classify the warp tile whose top-left element is (row0, col0), tw columns wide.
+// A tile is "fast" when it lies inside the matrix and every 16-byte chunk its rows
+// load -- including the chunks a non-zero shift adds before the first and after the
+// last element of each row segment -- lies inside the fragment.
+template <class T>
 __device__ __forceinline__ int classify_tile(const FragGeom& g, int64_t row0, int64_t col0,
                                              int tw) {
   const int64_t row_last = min(row0 + 31, g.rows - 1);
@@ -191,8 +208,144 @@ __device__ __forceinline__ int classify_tile(const FragGeom& g, int64_t row0, in
   const int64_t last = row_last * g.cols + col_last;
   if (last < g.start || first >= g.end) return kTileSkip;
   const bool whole = (row0 + 32 <= g.rows) && (col0 + tw <= g.cols);
-  if (g.fast_ok && whole && first >= g.start && last < g.end) return kTileFast;
+  const int64_t lo = g.shift / T::kBytes;                 // elements loaded before the segment
+  const int64_t hi = g.shift ? T::V - lo : 0;             // elements loaded after it
+  if (g.fast_ok && whole && first - lo >= g.start && last + hi < g.end) return kTileFast;
   return kTileMasked;
+}
+
+// ---------------------------------------------------------------- row loads
+// Chunks of NB consecutive rows of a fast tile for this lane: chunk r holds the V
+// elements (row0 + r, col0 + V*lane ...).  `src` is the lane's element address in
+// the first row.  shift == 0: one aligned 16-byte load per row.  shift != 0 (the
+// fragment's virtual base is not 16-byte aligned): each lane loads the aligned chunk
+// that holds its first element, takes the rest from the next lane's chunk (lane 31
+// loads one extra chunk), and a funnel shift realigns the bytes.  All lanes of the
+// warp must be active.
+__device__ __forceinline__ uint32_t pick4(uint32_t q, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+  return q == 0 ? a : (q == 1 ? b : (q == 2 ? c : d));
+}
+
+__device__ __forceinline__ uint4 realign(const uint4& A, const uint4& B, uint32_t shift) {
+  const uint32_t q = shift >> 2, r = (shift & 3u) * 8u;
+  const uint32_t w0 = pick4(q, A.x, A.y, A.z, A.w);
+  const uint32_t w1 = pick4(q, A.y, A.z, A.w, B.x);
+  const uint32_t w2 = pick4(q, A.z, A.w, B.x, B.y);
+  const uint32_t w3 = pick4(q, A.w, B.x, B.y, B.z);
+  const uint32_t w4 = pick4(q, B.x, B.y, B.z, B.w);
+  uint4 o;
+  o.x = __funnelshift_r(w0, w1, r);
+  o.y = __funnelshift_r(w1, w2, r);
+  o.z = __funnelshift_r(w2, w3, r);
+  o.w = __funnelshift_r(w3, w4, r);
+  return o;
+}
+
+template <int NB>
+__device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64_t row_bytes,
+                                          int lane, uint32_t shift) {
+  if (shift == 0) {
+#pragma unroll
+    for (int r = 0; r < NB; ++r) v[r] = ld_stream16(src + r * row_bytes);
+  } else {
+    const char* a = src - shift;
+    uint4 extra[NB];
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      v[r] = ld_stream16(a + r * row_bytes);
+      extra[r] = lane == 31 ? ld_stream16(a + r * row_bytes + 16) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      uint4 b;
+      b.x = __shfl_down_sync(kFullMask, v[r].x, 1);
+      b.y = __shfl_down_sync(kFullMask, v[r].y, 1);
+      b.z = __shfl_down_sync(kFullMask, v[r].z, 1);
+      b.w = __shfl_down_sync(kFullMask, v[r].w, 1);
+      if (lane == 31) b = extra[r];
+      v[r] = realign(v[r], b, shift);
+    }
+  }
+}
+
+// Chunks of NB consecutive rows of a masked tile: element k of chunk r is loaded only
+// when (row0 + r, j + k) is inside the matrix and the fragment; others read as 0.
+// Chunks that lie wholly inside the fragment take one 16-byte load when the
+// fragment's virtual base is 16-byte aligned.  Bit (r * V + k) of the returned mask
+// marks the loaded elements.
+template <class T, int NB>
+__device__ __forceinline__ uint64_t load_rows_masked(uint4 (&v)[NB], const FragGeom& g,
+                                                     const void* in, int64_t row0, int64_t j) {
+  constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
+  const bool vec = g.fast_ok && g.shift == 0;
+  // byte offset of element (row0, j) from the fragment's first element
+  int64_t off = (row0 * g.cols + j - g.start) * T::kBytes;
+  const int64_t row_bytes = g.cols * T::kBytes;
+  const char* base = static_cast<const char*>(in);
+  uint64_t valid = 0;
+#pragma unroll
+  for (int r = 0; r < NB; ++r, off += row_bytes) {
+    v[r] = make_uint4(0u, 0u, 0u, 0u);
+    const int64_t i = row0 + r;
+    if (!row_in(g, i) || i >= g.rows) continue;
+    const int64_t lo = row_lo(g, i), hi = row_hi(g, i);
+    if (vec && j >= lo && j + T::V - 1 <= hi) {
+      v[r] = *reinterpret_cast<const uint4*>(base + off);
+      valid |= kChunkBits << (r * T::V);
+      continue;
+    }
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) {
+      if (j + k >= lo && j + k <= hi) {
+        chunk_set<T>(v[r], k, load_bits<T>(base + off, k));
+        valid |= uint64_t(1) << (r * T::V + k);
+      }
+    }
+  }
+  return valid;
+}
+
+// Tile t of a job batch, in processing order: all boundary-band tiles of all jobs
+// first (their masked, slower tiles then overlap the streaming of the interior
+// bands instead of trailing it), then all interior tiles.  Returns the job index and
+// the tile's top-left element.
+template <class P, int N>
+__device__ __forceinline__ int batch_tile(const JobBatch<P, N>& b, int64_t t, int tw,
+                                          int64_t& row0, int64_t& col0) {
+  const int n = b.njobs;
+  const bool boundary = t < b.prefix_a[n];
+  const int64_t* prefix = boundary ? b.prefix_a : b.prefix_b;
+  if (!boundary) t -= b.prefix_a[n];
+  int lo = 0, hi = N == 1 ? 1 : n;  // prefix[lo] <= t < prefix[hi]
+  while (N > 1 && hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  const FragGeom& g = b.job[lo].g;
+  const int64_t k = t - prefix[lo];
+  int64_t band;
+  if (boundary) {
+    band = k < g.coltiles ? g.band0 : g.band0 + g.ntiles / g.coltiles - 1;
+  } else {
+    band = g.band0 + 1 + k / g.coltiles;
+  }
+  row0 = band * 32;
+  col0 = (k % g.coltiles) * tw;
+  return lo;
+}
+
+// Blocks for a persistent grid over `ntiles` warp tiles: as many rounds as the
+// resident capacity (`max_blocks` blocks of `warps` warps) needs, then just enough
+// blocks that every warp gets the same number of tiles (within one), instead of a
+// full last round being followed by a mostly idle one.
+inline unsigned balanced_grid(int64_t ntiles, int warps, int64_t max_blocks) {
+  const int64_t cap = max_blocks * warps;
+  const int64_t rounds = (ntiles + cap - 1) / cap;
+  const int64_t warps_needed = (ntiles + rounds - 1) / rounds;
+  int64_t blocks = (warps_needed + warps - 1) / warps;
+  if (blocks < 1) blocks = 1;
+  return unsigned(blocks < max_blocks ? blocks : max_blocks);
 }
 
 }  // namespace mxfp8

@@ -12,10 +12,14 @@ namespace mxfp8 {
 struct FragGeom {
   int64_t rows, cols;
   int64_t start, end;   // flat element range of the fragment
+  int64_t rs, cs;       // (row, col) of the fragment's first element
+  int64_t re, ce;       // (row, col) of its last element
   int64_t band0;        // first 32-row band the fragment touches
   int64_t ntiles;       // bands x coltiles
   int32_t coltiles;     // ceil(cols / TW)
-  int32_t fast_ok;      // 16-byte vector paths are legal for whole tiles
+  int32_t fast_ok;      // cols % V == 0: whole tiles may take the 16-byte vector path
+  int32_t shift;        // (virtual base address of element 0) mod 16, in bytes; the vector
+                        // path then loads aligned chunks and realigns them across lanes
 };
 
 struct AmaxParams {
@@ -39,6 +43,7 @@ struct CastParams {
   uint8_t* out_c;
   int64_t out_shift;   // out_offset - start
   int32_t vec_sc;      // colwise scale rows may be read as V-byte words
+  int32_t vec_out;     // both outputs' virtual bases are V-byte aligned: word stores
 };
 
 // One direction of a scale update: scale[r][c] = E8M0(amax[r][c]), r < nrows, c < ncols.
@@ -54,11 +59,50 @@ struct DeviceInfo {
   int sms;
 };
 
-// dtype: 0 = FP32, 1 = BF16.  Each launcher returns the CUDA launch status.
-cudaError_t launch_partial_amax(const AmaxParams& p, int dtype, bool colwise,
-                                const DeviceInfo& dev, cudaStream_t stream);
-cudaError_t launch_partial_cast(const CastParams& p, int dtype, bool colwise,
-                                const DeviceInfo& dev, cudaStream_t stream);
+// A batch of fragments launched as one kernel: the warp tiles of every job's first
+// and last 32-row bands (the only bands a fragment boundary can cut) come first,
+// numbered by prefix_a, then every job's interior bands, numbered by prefix_b.
+// The table travels in kernel parameter space (no device allocation).
+constexpr int kMaxBatchJobs = 16;
+
+template <class P, int N>
+struct JobBatch {
+  int32_t njobs;
+  int64_t prefix_a[N + 1];
+  int64_t prefix_b[N + 1];
+  P job[N];
+};
+
+// Boundary-band and interior-band tile counts of one fragment.
+inline void band_tiles(const FragGeom& g, int64_t* boundary, int64_t* interior) {
+  const int64_t nbands = g.coltiles > 0 ? g.ntiles / g.coltiles : 0;
+  *boundary = (nbands >= 2 ? 2 : nbands) * int64_t(g.coltiles);
+  *interior = (nbands > 2 ? nbands - 2 : 0) * int64_t(g.coltiles);
+}
+
+template <class P, int N>
+inline int64_t fill_batch(JobBatch<P, N>& b, const P* jobs, int n) {
+  b.njobs = n;
+  b.prefix_a[0] = b.prefix_b[0] = 0;
+  for (int k = 0; k < n; ++k) {
+    int64_t ta, tb;
+    band_tiles(jobs[k].g, &ta, &tb);
+    b.prefix_a[k + 1] = b.prefix_a[k] + ta;
+    b.prefix_b[k + 1] = b.prefix_b[k] + tb;
+    b.job[k] = jobs[k];
+  }
+  return b.prefix_a[n] + b.prefix_b[n];
+}
+
+// dtype: 0 = FP32, 1 = BF16.  Each launcher takes n validated jobs that share the
+// dtype and the template choices (columnwise present, virtual base shifted, output
+// word-aligned), launches them in batches of at most kMaxBatchJobs, and returns the
+// CUDA launch status.
+cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool colwise,
+                                bool shifted, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
+                                bool shifted, bool vec_out, const DeviceInfo& dev,
+                                cudaStream_t stream);
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,

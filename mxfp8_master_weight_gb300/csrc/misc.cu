@@ -16,26 +16,33 @@ namespace {
 
 constexpr int kThreads = 256;
 
+constexpr int kMaxSegments = 32;
+
+struct ScaleBatch {
+  int32_t nseg;
+  ScaleSegment seg[kMaxSegments];
+};
+
+// blockIdx.y selects the segment; blocks stride over its entries.
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constant__ ScaleSegment s0,
-                                                            const __grid_constant__ ScaleSegment s1) {
-  const ScaleSegment& s = blockIdx.y == 0 ? s0 : s1;
+__global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constant__ ScaleBatch b) {
+  const ScaleSegment& s = b.seg[blockIdx.y];
   const int64_t n = s.nrows * s.ncols;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (s.vec) {
     for (int64_t q = tid; q < n / 4; q += stride) {
-      uint32_t b[4];
+      uint32_t w[4];
       if constexpr (T::kBytes == 4) {
         const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(s.amax) + 4 * q);
-        b[0] = a.x; b[1] = a.y; b[2] = a.z; b[3] = a.w;
+        w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
       } else {
         const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(s.amax) + 4 * q);
-        b[0] = a.x & 0xffffu; b[1] = a.x >> 16; b[2] = a.y & 0xffffu; b[3] = a.y >> 16;
+        w[0] = a.x & 0xffffu; w[1] = a.x >> 16; w[2] = a.y & 0xffffu; w[3] = a.y >> 16;
       }
       uint32_t out = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(b[k]) << (8 * k);
+      for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(w[k]) << (8 * k);
       reinterpret_cast<uint32_t*>(s.scale)[q] = out;
     }
   } else {
@@ -85,22 +92,31 @@ unsigned grid_for(int64_t work_items, const DeviceInfo& dev) {
 
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream) {
-  if (nseg <= 0) return cudaSuccess;
-  int64_t work = 0;
-  for (int k = 0; k < nseg; ++k) {
-    const int64_t n = segs[k].nrows * segs[k].ncols;
-    const int64_t items = segs[k].vec ? n / 4 : n;
-    work = items > work ? items : work;
+  for (int k0 = 0; k0 < nseg; k0 += kMaxSegments) {
+    ScaleBatch b;
+    b.nseg = nseg - k0 < kMaxSegments ? nseg - k0 : kMaxSegments;
+    int64_t work = 0;
+    for (int k = 0; k < b.nseg; ++k) {
+      b.seg[k] = segs[k0 + k];
+      const int64_t n = b.seg[k].nrows * b.seg[k].ncols;
+      const int64_t items = b.seg[k].vec ? n / 4 : n;
+      work = items > work ? items : work;
+    }
+    if (work == 0) continue;
+    // spread the SM budget over the segments of this launch
+    int64_t per_seg = (int64_t(dev.sms) * 8 + b.nseg - 1) / b.nseg;
+    int64_t want = (work + kThreads - 1) / kThreads;
+    const unsigned gx = unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg));
+    const dim3 grid(gx, unsigned(b.nseg));
+    if (dtype == 0) {
+      k_update_scales<F32T><<<grid, kThreads, 0, stream>>>(b);
+    } else {
+      k_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(b);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  if (work == 0) return cudaSuccess;
-  const dim3 grid(grid_for(work, dev), unsigned(nseg));
-  const ScaleSegment& s1 = nseg > 1 ? segs[1] : segs[0];
-  if (dtype == 0) {
-    k_update_scales<F32T><<<grid, kThreads, 0, stream>>>(segs[0], s1);
-  } else {
-    k_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(segs[0], s1);
-  }
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,

@@ -104,6 +104,30 @@ class PackedLayout:
         return vr, vc
 
 
+def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs) -> int:
+    """Kernel launches the library issues for one step of these jobs: the batched
+    entries launch once per group of at most 16 jobs sharing dtype, direction set and
+    alignment class (fragment virtual base on a 16-byte boundary; for the cast also
+    the outputs' virtual base on a V-byte boundary)."""
+    def groups(keys, cap):
+        counts = {}
+        for k in keys:
+            counts[k] = counts.get(k, 0) + 1
+        return sum((n + cap - 1) // cap for n in counts.values())
+
+    def vbase(t, start):
+        return t.data_ptr() - start * t.element_size()
+
+    akeys = [(a[0].dtype, a[2] is not None, vbase(a[0], a[5]) % 16 != 0) for a in amax_jobs]
+    ckeys = []
+    for frag, sr, sc, qr, qc, rows, cols, start in cast_jobs:
+        v = 16 // frag.element_size()
+        vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
+        ckeys.append((frag.dtype, qc is not None, vbase(frag, start) % 16 != 0, vec))
+    n_grids = sum(2 if s.colwise else 1 for s in specs)
+    return groups(akeys, 16) + 1 + (n_grids + 31) // 32 + groups(ckeys, 16)
+
+
 def _round_up(x: int, a: int) -> int:
     return (x + a - 1) // a * a
 
@@ -147,9 +171,10 @@ class ShardedCast:
         return len(self.bounds) - 1
 
     def launches_per_step(self) -> int:
-        """Library kernel launches of one step (amax + cast per fragment, reduce, scales)."""
-        frags = sum(len(c) for c in self.plan)
-        return 2 * frags + 1 + len(self.specs)
+        """Library kernel launches of one step: the batched amax and cast take one launch
+        per (direction set, alignment class) group of at most 16 fragments, the
+        reduction one, the batched scale update one per 32 block grids."""
+        return self._launches if hasattr(self, "_launches") else -1
 
     def _check_shards(self, shards) -> None:
         if len(shards) != self.num_shards:
@@ -165,23 +190,29 @@ class ShardedCast:
         if getattr(self, "_cache_key", None) == key:
             return self._cache
         self._check_shards(shards)
-        amax, casts = [], []
+        amax_jobs, cast_jobs = [], []
         for s, cuts in enumerate(self.plan):
             for c in cuts:
                 spec = self.specs[c.weight]
                 frag = shards[s][c.shard_offset:c.shard_offset + c.length]
                 vr, vc = self.layout.views(self.slots[s], c.weight)
-                amax.append(api.prepare_partial_amax(frag, vr, vc, spec.rows, spec.cols, c.start))
+                amax_jobs.append((frag, vr, vc, spec.rows, spec.cols, c.start))
                 sr, sc = self.scales[c.weight]
                 qr, qc = self.outputs[c.weight]
-                casts.append(api.prepare_partial_cast(frag, sr, sc, qr, qc, spec.rows, spec.cols,
-                                                      c.start))
-        reduce = [api.prepare_amax_max_reduce(self.slots, self.reduced)]
-        scales = []
+                cast_jobs.append((frag, sr, sc, qr, qc, spec.rows, spec.cols, c.start))
+        scale_jobs = []
         for w, spec in enumerate(self.specs):
             vr, vc = self.layout.views(self.reduced, w)
             sr, sc = self.scales[w]
-            scales.append(api.prepare_update_scales(vr, vc, sr, sc, spec.rows, spec.cols))
+            scale_jobs.append((vr, vc, sr, sc, spec.rows, spec.cols))
+        # one batched call per phase: every fragment of every shard (each shard writes
+        # its own slot, so no two jobs write the same amax entry), one reduction, every
+        # weight's scales, every fragment's cast
+        self._launches = _count_launches(amax_jobs, cast_jobs, len(scale_jobs), self.specs)
+        amax = [api.prepare_partial_amax_batched(amax_jobs)]
+        reduce = [api.prepare_amax_max_reduce(self.slots, self.reduced)]
+        scales = [api.prepare_update_scales_batched(scale_jobs)]
+        casts = [api.prepare_partial_cast_batched(cast_jobs)]
         self._cache_key, self._cache = key, (amax, reduce, scales, casts)
         return self._cache
 

@@ -194,3 +194,24 @@ def test_flat_indices_beyond_32_bits(start):
     want_qc = np.zeros(length, np.uint8)
     oracle.partial_cast(frag, rows, cols, start, hs_r, hs_c, want_qr, want_qc, 0)
     assert np.array_equal(to_host(qr), want_qr) and np.array_equal(to_host(qc), want_qc)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("colwise", [True, False])
+def test_every_fragment_misalignment(dtype, colwise):
+    """Fragments whose virtual base sits at every possible offset inside a 16-byte
+    chunk (own buffers, as a rank's shard would be): the realigning vector path for
+    interior tiles and the masked path for the tiles at the fragment's two ends."""
+    rows, cols = 96, 2048
+    rng = np.random.default_rng(21)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(3.0) ** rng.integers(-8, 8, rows * cols).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    per_chunk = 4 if dtype == "f32" else 8
+    for k in range(per_chunk):
+        start = 5 * cols + 3 + k
+        length = rows * cols - start - 37
+        frag = np.ascontiguousarray(x[start:start + length])
+        got = gpu_fragment(frag, rows, cols, start, colwise, shift=k)
+        want = oracle_fragment(frag, rows, cols, start, colwise)
+        assert_bitwise(got, want, f"{dtype} misalignment {k}")
