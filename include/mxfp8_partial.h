@@ -196,6 +196,51 @@ int mxfp8_partial_amax_batched(const mxfp8_amax_job* jobs, int32_t njobs, void* 
 int mxfp8_update_scales_batched(const mxfp8_scale_job* jobs, int32_t njobs, void* stream);
 int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream);
 
+/*
+ * One-pass quantisation of a fragment made of WHOLE blocks.  When every row block
+ * (and, with a columnwise output, every column block) that the fragment touches lies
+ * wholly inside it -- a rank that owns whole weights or whole 32-row bands, or a
+ * single rank -- no cross-rank MAX reduction is needed (the MAX over one rank is the
+ * identity), and amax, scale update and cast of the page "Support row-only MXFP8
+ * distributed master-weight casts" (flow diagram) run as ONE kernel that reads the
+ * input from HBM once.  Results are bit-identical to mxfp8_partial_amax ->
+ * mxfp8_update_scales -> mxfp8_partial_cast on the same fragment.
+ *
+ * input, output_rowwise, output_colwise, rows, cols, start_offset, out_offset: as for
+ *                   mxfp8_partial_cast; the columnwise direction is present iff
+ *                   output_colwise is.
+ * amax_rowwise / amax_colwise [out] OPTIONAL grids as for mxfp8_partial_amax; when
+ *                   given, the block maxima are stored too (a columnwise amax grid is
+ *                   ignored without a columnwise output).
+ * scale_inv_rowwise [out] REQUIRED; scale_inv_colwise [out] required iff
+ *                   output_colwise is present.  Entries of blocks the fragment touches
+ *                   are written; others are left untouched.
+ * Precondition (status 1 otherwise): start_offset % cols and (start_offset + len) %
+ * cols are multiples of 32, and with a columnwise output start_offset and
+ * start_offset + len are multiples of 32*cols (the end may also be rows*cols).
+ */
+int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+                                mxfp8_tensor* amax_colwise, mxfp8_tensor* scale_inv_rowwise,
+                                mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
+                                mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
+                                int64_t start_offset, int64_t out_offset, void* stream);
+
+typedef struct {
+  mxfp8_tensor input;
+  mxfp8_tensor amax_rowwise;      /* optional */
+  mxfp8_tensor amax_colwise;      /* optional */
+  mxfp8_tensor scale_inv_rowwise;
+  mxfp8_tensor scale_inv_colwise;
+  mxfp8_tensor output_rowwise;
+  mxfp8_tensor output_colwise;    /* empty => row-only */
+  int64_t rows, cols, start_offset, out_offset;
+} mxfp8_quantize_job;
+
+/* Batched form of mxfp8_quantize_whole_blocks, with the conventions of the other
+ * batched entry points. */
+int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
+                                        void* stream);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 const char* mxfp8_last_error(void);
 

@@ -19,7 +19,8 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "shape mismatch", 3: "dtype m
 
 EXPORTED = ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
             "mxfp8_partial_cast", "mxfp8_partial_amax_batched", "mxfp8_update_scales_batched",
-            "mxfp8_partial_cast_batched", "mxfp8_last_error", "mxfp8_version")
+            "mxfp8_partial_cast_batched", "mxfp8_quantize_whole_blocks",
+            "mxfp8_quantize_whole_blocks_batched", "mxfp8_last_error", "mxfp8_version")
 
 
 class Tensor(ctypes.Structure):
@@ -44,6 +45,14 @@ class CastJob(ctypes.Structure):
 class ScaleJob(ctypes.Structure):
     _fields_ = [("amax_rowwise", Tensor), ("amax_colwise", Tensor), ("scale_inv_rowwise", Tensor),
                 ("scale_inv_colwise", Tensor), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64)]
+
+
+class QuantizeJob(ctypes.Structure):
+    _fields_ = [("input", Tensor), ("amax_rowwise", Tensor), ("amax_colwise", Tensor),
+                ("scale_inv_rowwise", Tensor), ("scale_inv_colwise", Tensor),
+                ("output_rowwise", Tensor), ("output_colwise", Tensor),
+                ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64)]
 
 
 def empty_tensor() -> Tensor:
@@ -82,9 +91,12 @@ def load(path: str | None = None):
         lib.mxfp8_partial_amax_batched.argtypes = [ctypes.POINTER(AmaxJob), i32, vp]
         lib.mxfp8_update_scales_batched.argtypes = [ctypes.POINTER(ScaleJob), i32, vp]
         lib.mxfp8_partial_cast_batched.argtypes = [ctypes.POINTER(CastJob), i32, vp]
+        lib.mxfp8_quantize_whole_blocks.argtypes = [T, T, T, T, T, T, T, i64, i64, i64, i64, vp]
+        lib.mxfp8_quantize_whole_blocks_batched.argtypes = [ctypes.POINTER(QuantizeJob), i32, vp]
         for name in ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
                      "mxfp8_partial_cast", "mxfp8_partial_amax_batched",
                      "mxfp8_update_scales_batched", "mxfp8_partial_cast_batched",
+                     "mxfp8_quantize_whole_blocks", "mxfp8_quantize_whole_blocks_batched",
                      "mxfp8_version"):
             getattr(lib, name).restype = ctypes.c_int
         lib.mxfp8_last_error.argtypes = []

@@ -16,7 +16,8 @@ import ctypes
 import torch
 
 from . import _capi
-from ._capi import DTYPE_BF16, DTYPE_F32, DTYPE_U8, AmaxJob, CastJob, MXFP8Error, ScaleJob, Tensor
+from ._capi import (DTYPE_BF16, DTYPE_F32, DTYPE_U8, AmaxJob, CastJob, MXFP8Error, QuantizeJob,
+                    ScaleJob, Tensor)
 
 _DTYPES = {torch.float32: DTYPE_F32, torch.bfloat16: DTYPE_BF16, torch.uint8: DTYPE_U8,
            torch.float8_e4m3fn: DTYPE_U8}
@@ -166,6 +167,47 @@ def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
           _stream(stream, keep[0] if keep else None))
 
 
+def mxfp8_quantize_whole_blocks(input, amax_rowwise, amax_colwise, scale_inv_rowwise,
+                                scale_inv_colwise, output_rowwise, output_colwise, rows: int,
+                                cols: int, start_offset: int, out_offset: int | None = None,
+                                stream=None) -> None:
+    """One-pass amax -> scales -> cast of a fragment made of whole blocks (amax outputs
+    optional); bit-identical to the split calls on the same fragment."""
+    dev = _device_of(input, output_rowwise, output_colwise)
+    if out_offset is None:
+        out_offset = start_offset
+    names = ("input", "amax_rowwise", "amax_colwise", "scale_inv_rowwise", "scale_inv_colwise",
+             "output_rowwise", "output_colwise")
+    ts = (input, amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
+          output_rowwise, output_colwise)
+    args = [handle(t, n) for t, n in zip(ts, names)]
+    _call("mxfp8_quantize_whole_blocks", dev, *[ctypes.byref(a) for a in args], int(rows),
+          int(cols), int(start_offset), int(out_offset), _stream(stream, input))
+
+
+def _quantize_jobs(jobs):
+    arr = (QuantizeJob * max(1, len(jobs)))()
+    keep = []
+    names = ("input", "amax_rowwise", "amax_colwise", "scale_inv_rowwise", "scale_inv_colwise",
+             "output_rowwise", "output_colwise")
+    for k, job in enumerate(jobs):
+        ts = job[:7]
+        rows, cols, start = job[7:10]
+        out_offset = job[10] if len(job) > 10 and job[10] is not None else start
+        arr[k] = QuantizeJob(*[handle(t, n) for t, n in zip(ts, names)], int(rows), int(cols),
+                             int(start), int(out_offset))
+        keep += [t for t in ts if t is not None]
+    return arr, keep
+
+
+def mxfp8_quantize_whole_blocks_batched(jobs, stream=None) -> None:
+    """``jobs``: sequence of (input, amax_rowwise, amax_colwise, scale_inv_rowwise,
+    scale_inv_colwise, output_rowwise, output_colwise, rows, cols, start_offset[, out_offset])."""
+    arr, keep = _quantize_jobs(jobs)
+    _call("mxfp8_quantize_whole_blocks_batched", _device_of(*keep), arr, len(jobs),
+          _stream(stream, keep[0] if keep else None))
+
+
 class Prepared:
     """One library call with its tensor handles marshalled once.
 
@@ -239,6 +281,11 @@ def prepare_update_scales_batched(jobs) -> Prepared:
 def prepare_partial_cast_batched(jobs) -> Prepared:
     arr, keep = _cast_jobs(jobs)
     return Prepared("mxfp8_partial_cast_batched", [arr], (len(jobs),), keep, job_array=arr)
+
+
+def prepare_quantize_whole_blocks_batched(jobs) -> Prepared:
+    arr, keep = _quantize_jobs(jobs)
+    return Prepared("mxfp8_quantize_whole_blocks_batched", [arr], (len(jobs),), keep, job_array=arr)
 
 
 def block_shapes(rows: int, cols: int):

@@ -17,6 +17,7 @@ using mxfp8::AmaxParams;
 using mxfp8::CastParams;
 using mxfp8::DeviceInfo;
 using mxfp8::FragGeom;
+using mxfp8::FusedParams;
 using mxfp8::ScaleSegment;
 
 thread_local char g_err[512] = {0};
@@ -249,6 +250,56 @@ int prep_cast(const mxfp8_cast_job& job, CastParams* p, int* dtype, bool* colwis
   return MXFP8_OK;
 }
 
+int prep_fused(const mxfp8_quantize_job& job, FusedParams* p, int* dtype, bool* colwise,
+               bool* skip) {
+  // the data side is validated exactly as a partial cast
+  const mxfp8_cast_job cj = {job.input, job.scale_inv_rowwise, job.scale_inv_colwise,
+                             job.output_rowwise, job.output_colwise, job.rows, job.cols,
+                             job.start_offset, job.out_offset};
+  CastParams c;
+  if (int rc = prep_cast(cj, &c, dtype, colwise, skip)) return rc;
+  if (*skip) return MXFP8_OK;
+  const int64_t rows = job.rows, cols = job.cols;
+  const int64_t start = job.start_offset, end = start + numel(&job.input);
+  if ((start % cols) % 32 != 0 || (end % cols) % 32 != 0)
+    return fail(MXFP8_ERR_INVALID,
+                "fragment [%lld, %lld) cuts a 1x32 block: use partial amax, MAX reduction, scale "
+                "update and partial cast", (long long)start, (long long)end);
+  if (*colwise && (start % (32 * cols) != 0 || (end % (32 * cols) != 0 && end != rows * cols)))
+    return fail(MXFP8_ERR_INVALID,
+                "fragment [%lld, %lld) cuts a 32x1 block: use partial amax, MAX reduction, scale "
+                "update and partial cast", (long long)start, (long long)end);
+  const int32_t dt = job.input.dtype;
+  const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
+  const int V = int(16 / elem_bytes(dt));
+  *p = FusedParams{};
+  p->g = c.g;
+  p->in = c.in;
+  p->s_r = static_cast<uint8_t*>(job.scale_inv_rowwise.data);
+  p->ld_sr = c.ld_sr;
+  p->out_r = c.out_r;
+  p->out_shift = c.out_shift;
+  p->vec_out = c.vec_out;
+  if (!is_empty(&job.amax_rowwise)) {
+    if (int rc = check_grid(&job.amax_rowwise, "amax_rowwise", rows, nbr, dt)) return rc;
+    p->amax_r = job.amax_rowwise.data;
+    p->ld_r = job.amax_rowwise.shape[1];
+  }
+  if (*colwise) {
+    p->s_c = static_cast<uint8_t*>(job.scale_inv_colwise.data);
+    p->ld_sc = c.ld_sc;
+    p->out_c = c.out_c;
+    p->vec_sc = c.vec_sc;
+    if (!is_empty(&job.amax_colwise)) {
+      if (int rc = check_grid(&job.amax_colwise, "amax_colwise", nbc, cols, dt)) return rc;
+      p->amax_c = job.amax_colwise.data;
+      p->ld_c = job.amax_colwise.shape[1];
+      p->vec_c = (reinterpret_cast<uintptr_t>(p->amax_c) % 16 == 0) && (p->ld_c % V == 0);
+    }
+  }
+  return MXFP8_OK;
+}
+
 int prep_scales(const mxfp8_scale_job& job, ScaleSegment* segs, int* nseg, int* dtype) {
   const int64_t rows = job.rows, cols = job.cols;
   if (rows <= 0 || cols <= 0) return fail(MXFP8_ERR_INVALID, "rows and cols must be positive");
@@ -413,6 +464,45 @@ int run_scales(const mxfp8_scale_job* jobs, int32_t njobs, void* stream) {
   return ok();
 }
 
+int run_fused(const mxfp8_quantize_job* jobs, int32_t njobs, void* stream) {
+  if (njobs < 0 || (njobs > 0 && jobs == nullptr)) return fail(MXFP8_ERR_INVALID, "bad job array");
+  FusedParams win[kWindow];
+  int key[kWindow];
+  int dt;
+  bool col, skip;
+  int live = 0;
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_fused(jobs[k], &win[0], &dt, &col, &skip)) return njobs > 1 ? job_fail(rc, k) : rc;
+    live += !skip;
+  }
+  if (live == 0) return ok();
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  FusedParams batch[kGroupChunk];
+  for (int base = 0; base < njobs; base += kWindow) {
+    const int m = njobs - base < kWindow ? njobs - base : kWindow;
+    for (int i = 0; i < m; ++i) {
+      prep_fused(jobs[base + i], &win[i], &dt, &col, &skip);
+      key[i] = skip ? -1 : dt * 8 + col * 4 + (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+    }
+    for (int kk = 0; kk < 16; ++kk) {
+      int n = 0;
+      for (int i = 0; i <= m; ++i) {
+        if (i < m && key[i] == kk) batch[n++] = win[i];
+        if (n > 0 && (n == kGroupChunk || i == m)) {
+          if (int rc = cuda_status(mxfp8::launch_fused_quantize(batch, n, kk >> 3, (kk >> 2) & 1,
+                                                                (kk >> 1) & 1, kk & 1, dev,
+                                                                static_cast<cudaStream_t>(stream)),
+                                   "fused quantize launch"))
+            return rc;
+          n = 0;
+        }
+      }
+    }
+  }
+  return ok();
+}
+
 const mxfp8_tensor kEmpty = {nullptr, MXFP8_DTYPE_U8, 1, {0, 0}};
 
 const mxfp8_tensor& or_empty(const mxfp8_tensor* t) { return t ? *t : kEmpty; }
@@ -486,6 +576,23 @@ int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_
 
 int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
   return run_cast(jobs, njobs, stream);
+}
+
+int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+                                mxfp8_tensor* amax_colwise, mxfp8_tensor* scale_inv_rowwise,
+                                mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
+                                mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
+                                int64_t start_offset, int64_t out_offset, void* stream) {
+  const mxfp8_quantize_job job = {or_empty(input), or_empty(amax_rowwise), or_empty(amax_colwise),
+                                  or_empty(scale_inv_rowwise), or_empty(scale_inv_colwise),
+                                  or_empty(output_rowwise), or_empty(output_colwise),
+                                  rows, cols, start_offset, out_offset};
+  return run_fused(&job, 1, stream);
+}
+
+int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
+                                        void* stream) {
+  return run_fused(jobs, njobs, stream);
 }
 
 }  // extern "C"

@@ -30,50 +30,6 @@ constexpr int kMaxDevices = 64;
 #define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
 #endif
 
-// Model-dtype values of one input chunk.
-template <class T>
-__device__ __forceinline__ void model_values(const uint4& c, float (&y)[T::V]) {
-  if constexpr (T::kBytes == 4) {
-    const uint32_t w0 = bf16x2_rn(__uint_as_float(c.x), __uint_as_float(c.y));
-    const uint32_t w1 = bf16x2_rn(__uint_as_float(c.z), __uint_as_float(c.w));
-    y[0] = bf16_lo(w0); y[1] = bf16_hi(w0); y[2] = bf16_lo(w1); y[3] = bf16_hi(w1);
-  } else {
-    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) { y[2 * k] = bf16_lo(w[k]); y[2 * k + 1] = bf16_hi(w[k]); }
-  }
-}
-
-// V E4M3 bytes of y[k] * mult[k] (element k in byte k).
-template <class T>
-__device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
-  uint2 q;
-  q.x = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
-        (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
-  if constexpr (T::V == 8) {
-    q.y = e4m3x2_rn_sat(y[4] * mult[4], y[5] * mult[5]) |
-          (e4m3x2_rn_sat(y[6] * mult[6], y[7] * mult[7]) << 16);
-  } else {
-    q.y = 0;
-  }
-  return q;
-}
-
-// Store V bytes: one 4- or 8-byte word when the destination is aligned, else bytes.
-template <class T, bool kVec>
-__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint2& q) {
-  if constexpr (kVec) {
-    if constexpr (T::V == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = q.x;
-    } else {
-      *reinterpret_cast<uint2*>(dst) = q;
-    }
-  } else {
-#pragma unroll
-    for (int k = 0; k < T::V; ++k) dst[k] = static_cast<uint8_t>((k < 4 ? q.x : q.y) >> (8 * (k & 3)));
-  }
-}
-
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
 __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t row0, int64_t j,

@@ -46,6 +46,27 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   return v;
 }
 
+// L2 cache policies (createpolicy) and a 16-byte load that carries one: a tile read
+// twice in a row keeps its lines in L2 between the reads (evict_last on the first
+// read, evict_first on the second).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint4 ld_hint16(const void* p, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(pol));
+  return v;
+}
+
 // ---------------------------------------------------------------- per-element access
 template <class T>
 __device__ __forceinline__ uint32_t load_bits(const void* base, int64_t idx) {
@@ -165,6 +186,51 @@ __device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// ---------------------------------------------------------------- cast of one chunk
+// Model-dtype values of one input chunk.
+template <class T>
+__device__ __forceinline__ void model_values(const uint4& c, float (&y)[T::V]) {
+  if constexpr (T::kBytes == 4) {
+    const uint32_t w0 = bf16x2_rn(__uint_as_float(c.x), __uint_as_float(c.y));
+    const uint32_t w1 = bf16x2_rn(__uint_as_float(c.z), __uint_as_float(c.w));
+    y[0] = bf16_lo(w0); y[1] = bf16_hi(w0); y[2] = bf16_lo(w1); y[3] = bf16_hi(w1);
+  } else {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) { y[2 * k] = bf16_lo(w[k]); y[2 * k + 1] = bf16_hi(w[k]); }
+  }
+}
+
+// V E4M3 bytes of y[k] * mult[k] (element k in byte k).
+template <class T>
+__device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
+  uint2 q;
+  q.x = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
+        (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
+  if constexpr (T::V == 8) {
+    q.y = e4m3x2_rn_sat(y[4] * mult[4], y[5] * mult[5]) |
+          (e4m3x2_rn_sat(y[6] * mult[6], y[7] * mult[7]) << 16);
+  } else {
+    q.y = 0;
+  }
+  return q;
+}
+
+// Store V bytes: one 4- or 8-byte word when the destination is aligned, else bytes.
+template <class T, bool kVec>
+__device__ __forceinline__ void store_chunk(uint8_t* dst, const uint2& q) {
+  if constexpr (kVec) {
+    if constexpr (T::V == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = q.x;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = q;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) dst[k] = static_cast<uint8_t>((k < 4 ? q.x : q.y) >> (8 * (k & 3)));
+  }
+}
+
 // ---------------------------------------------------------------- fragment geometry
 // The fragment is every element from (rs, cs) to (re, ce) in row-major order, so row
 // i holds fragment columns [row_lo(i), row_hi(i)] (empty when i is outside
@@ -242,19 +308,28 @@ __device__ __forceinline__ uint4 realign(const uint4& A, const uint4& B, uint32_
   return o;
 }
 
-template <int NB>
+template <bool kHint>
+__device__ __forceinline__ uint4 ld_chunk(const void* p, uint64_t pol) {
+  if constexpr (kHint) {
+    return ld_hint16(p, pol);
+  } else {
+    return ld_stream16(p);
+  }
+}
+
+template <int NB, bool kHint = false>
 __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64_t row_bytes,
-                                          int lane, uint32_t shift) {
+                                          int lane, uint32_t shift, uint64_t pol = 0) {
   if (shift == 0) {
 #pragma unroll
-    for (int r = 0; r < NB; ++r) v[r] = ld_stream16(src + r * row_bytes);
+    for (int r = 0; r < NB; ++r) v[r] = ld_chunk<kHint>(src + r * row_bytes, pol);
   } else {
     const char* a = src - shift;
     uint4 extra[NB];
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
-      v[r] = ld_stream16(a + r * row_bytes);
-      extra[r] = lane == 31 ? ld_stream16(a + r * row_bytes + 16) : make_uint4(0u, 0u, 0u, 0u);
+      v[r] = ld_chunk<kHint>(a + r * row_bytes, pol);
+      extra[r] = lane == 31 ? ld_chunk<kHint>(a + r * row_bytes + 16, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {

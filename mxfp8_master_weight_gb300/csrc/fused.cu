@@ -1,0 +1,298 @@
+// One-pass MXFP8 quantisation of fragments made of whole blocks.
+//
+// When every 1x32 (and, for a bidirectional weight, every 32x1) block a fragment
+// touches lies wholly inside it -- a rank that owns whole weights or whole 32-row
+// bands, or a single rank -- the block maxima need no cross-rank reduction, and the
+// four steps of "Support row-only MXFP8 distributed master-weight casts" (amax,
+// MAX reduction, scale update, cast; flow diagram) collapse into one kernel with
+// the same results: the MAX over one rank is the identity.
+//
+// Each warp owns a 32-row tile, as in the split kernels, and reads it twice: pass 1
+// folds the block maxima, derives and stores the E8M0 scales (and, on request, the
+// amaxes); pass 2 re-reads the tile and writes the E4M3 data.  Pass 1 loads carry an
+// L2 evict_last policy and pass 2 loads evict_first, so the second read is served
+// from L2 and HBM sees the input once: 4 + 2 bytes per FP32 element (bidirectional)
+// instead of 4 + 4 + 2 for the split amax and cast kernels.
+#include <atomic>
+
+#include "common.cuh"
+
+namespace mxfp8 {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowBatch = 8;
+constexpr int kShiftBatch = 4;
+constexpr int kMaskBatch = 4;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxGroups = 8;  // row blocks per warp tile (BF16: 256 columns / 32)
+// Resident blocks per SM the register allocation must allow: the two passes of a tile
+// run back to back in one warp, so latency is hidden only across warps.
+#ifndef MXFP8_FUSED_MIN_BLOCKS
+#define MXFP8_FUSED_MIN_BLOCKS 3
+#endif
+constexpr int kFusedMinBlocks = MXFP8_FUSED_MIN_BLOCKS;
+
+// E8M0 bytes of the 32 rows' row blocks of each warp's tile, handed from pass 1 to pass 2.
+struct RowScales {
+  uint8_t b[kWarps][32][kMaxGroups];
+};
+
+template <class T, bool kCol>
+__device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t row0, int64_t j,
+                                                const uint4& colmax, float (&mc)[T::V]) {
+  const int64_t band = row0 >> 5;
+  uint32_t sb[T::V];
+#pragma unroll
+  for (int k = 0; k < T::V; ++k) {
+    sb[k] = e8m0_from_bits<T>(chunk_get<T>(colmax, k));
+    mc[k] = scale_multiplier(sb[k]);
+  }
+  if (p.amax_c != nullptr) {
+    const int64_t base = band * p.ld_c + j;
+    if (p.vec_c) {
+      *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = colmax;
+    } else {
+#pragma unroll
+      for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(colmax, k));
+    }
+  }
+  uint8_t* dst = p.s_c + band * p.ld_sc + j;
+  if (p.vec_sc) {
+    uint2 w = make_uint2(0u, 0u);
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) (k < 4 ? w.x : w.y) |= sb[k] << (8 * (k & 3));
+    if constexpr (T::V == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = w.x;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) dst[k] = static_cast<uint8_t>(sb[k]);
+  }
+}
+
+template <class T, bool kCol, bool kShift, bool kVec>
+__device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t row0, int64_t col0,
+                                                int lane, RowScales& rsc, int warp) {
+  const int64_t cols = p.g.cols;
+  const int64_t j = col0 + lane * T::V;
+  const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
+  const int64_t row_bytes = cols * T::kBytes;
+  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
+  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
+  const int grp = lane / T::G;
+  const bool writer = (lane % T::G) == 0;
+  const int64_t blk = j >> 5;
+  const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+
+  // pass 1: block maxima -> scales
+  uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int rb = 0; rb < 32; rb += NB) {
+    uint4 v[NB];
+    load_rows<NB, true>(v, src + rb * row_bytes, row_bytes, lane, shift, keep);
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      const uint4 a = chunk_abs<T>(v[r]);
+      if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
+      const uint32_t m = group_max<T>(chunk_reduce<T>(a));
+      if (writer) {
+        const int64_t i = row0 + rb + r;
+        const uint32_t e = e8m0_from_bits<T>(m);
+        rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
+        p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
+        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, m);
+      }
+    }
+  }
+  float mc[T::V];
+  if constexpr (kCol) store_col_stats<T, kCol>(p, row0, j, colmax, mc);
+  __syncwarp();
+
+  // pass 2: cast (the tile's lines are still in L2)
+  const int64_t o0 = row0 * cols + j + p.out_shift;
+#pragma unroll 1
+  for (int rb = 0; rb < 32; rb += NB) {
+    uint4 v[NB];
+    load_rows<NB, true>(v, src + rb * row_bytes, row_bytes, lane, shift, drop);
+#pragma unroll
+    for (int r = 0; r < NB; ++r) {
+      float y[T::V];
+      model_values<T>(v[r], y);
+      float mr[T::V];
+      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
+#pragma unroll
+      for (int k = 0; k < T::V; ++k) mr[k] = m;
+      const int64_t o = o0 + (rb + r) * cols;
+      store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
+      if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
+    }
+  }
+  __syncwarp();
+}
+
+// Tile cut by the fragment boundary or the matrix edge.  Every block the fragment
+// touches is whole, so the maxima over the loaded elements are the block maxima.
+template <class T, bool kCol, bool kVec>
+__device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row0, int64_t col0,
+                                               int lane, RowScales& rsc, int warp) {
+  constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
+  const FragGeom& g = p.g;
+  const int64_t j = col0 + lane * T::V;
+  const int grp = lane / T::G;
+  const bool writer = (lane % T::G) == 0;
+  const int64_t b0 = j & ~int64_t(31);
+  const bool word_ok = kVec && g.fast_ok;
+  uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int rb = 0; rb < 32; rb += kMaskBatch) {  // warp-uniform
+    uint4 v[kMaskBatch];
+    load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+#pragma unroll
+    for (int r = 0; r < kMaskBatch; ++r) {
+      const uint4 a = chunk_abs<T>(v[r]);
+      if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
+      const uint32_t m = group_max<T>(chunk_reduce<T>(a));
+      const int64_t i = row0 + rb + r;
+      const uint32_t e = e8m0_from_bits<T>(m);
+      if (writer) rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
+      if (writer && i < g.rows && b0 < g.cols &&
+          row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1))) {
+        p.s_r[i * p.ld_sr + (b0 >> 5)] = static_cast<uint8_t>(e);
+        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), m);
+      }
+    }
+  }
+  float mc[T::V];
+  if constexpr (kCol) {
+    const int64_t r_end = min(row0 + 32, g.rows);
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) {
+      const int64_t col = j + k;
+      const uint32_t m = chunk_get<T>(colmax, k);
+      const uint32_t e = e8m0_from_bits<T>(m);
+      mc[k] = scale_multiplier(e);
+      if (col < g.cols && column_meets(g, col, row0, r_end)) {
+        p.s_c[(row0 >> 5) * p.ld_sc + col] = static_cast<uint8_t>(e);
+        if (p.amax_c != nullptr) store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, m);
+      }
+    }
+  }
+  __syncwarp();
+#pragma unroll 1
+  for (int rb = 0; rb < 32 && row0 + rb < g.rows; rb += kMaskBatch) {
+    uint4 v[kMaskBatch];
+    const uint64_t valid = load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+    if (valid == 0) continue;
+#pragma unroll
+    for (int r = 0; r < kMaskBatch; ++r) {
+      const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
+      if (bits == 0) continue;
+      float y[T::V];
+      model_values<T>(v[r], y);
+      float mr[T::V];
+      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
+#pragma unroll
+      for (int k = 0; k < T::V; ++k) mr[k] = m;
+      const uint2 qr = quantize_chunk<T>(y, mr);
+      uint2 qc = make_uint2(0u, 0u);
+      if constexpr (kCol) qc = quantize_chunk<T>(y, mc);
+      const int64_t o = (row0 + rb + r) * g.cols + j + p.out_shift;
+      if (word_ok && bits == kChunkBits) {
+        store_chunk<T, true>(p.out_r + o, qr);
+        if constexpr (kCol) store_chunk<T, true>(p.out_c + o, qc);
+      } else {
+#pragma unroll
+        for (int k = 0; k < T::V; ++k) {
+          if (bits & (uint64_t(1) << k)) {
+            const int sh = 8 * (k & 3);
+            p.out_r[o + k] = static_cast<uint8_t>((k < 4 ? qr.x : qr.y) >> sh);
+            if constexpr (kCol) p.out_c[o + k] = static_cast<uint8_t>((k < 4 ? qc.x : qc.y) >> sh);
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <class T, bool kCol, bool kShift, bool kVec, int N>
+__global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
+    const __grid_constant__ JobBatch<FusedParams, N> b) {
+  __shared__ RowScales rsc;
+  constexpr int TW = tile_width<T>();
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
+  const int64_t stride = int64_t(gridDim.x) * kWarps;
+  for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < total; t += stride) {
+    int64_t row0, col0;
+    const FusedParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
+    const int kind = classify_tile<T>(p.g, row0, col0, TW);
+    if (kind == kTileFast) {
+      fused_tile_fast<T, kCol, kShift, kVec>(p, row0, col0, lane, rsc, warp);
+    } else if (kind == kTileMasked) {
+      fused_tile_masked<T, kCol, kVec>(p, row0, col0, lane, rsc, warp);
+    }
+  }
+}
+
+template <class T, bool kCol, bool kShift, bool kVec, int N>
+cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
+  static std::atomic<int> occupancy[kMaxDevices];
+  int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
+  if (occ == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        &occ, k_fused_quantize<T, kCol, kShift, kVec, N>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
+  }
+  JobBatch<FusedParams, N> b;
+  const int64_t total = fill_batch(b, jobs, n);
+  if (total == 0) return cudaSuccess;
+  const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
+  k_fused_quantize<T, kCol, kShift, kVec, N><<<grid, kThreads, 0, stream>>>(b);
+  return cudaGetLastError();
+}
+
+template <class T, bool kCol, bool kShift, bool kVec>
+cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n == 1) return launch_n<T, kCol, kShift, kVec, 1>(jobs, 1, dev, stream);
+  for (int k = 0; k < n; k += kMaxBatchJobs) {
+    const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
+    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+template <class T, bool kCol>
+cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool vec_out,
+                           const DeviceInfo& dev, cudaStream_t stream) {
+  if (shifted) {
+    return vec_out ? launch<T, kCol, true, true>(jobs, n, dev, stream)
+                   : launch<T, kCol, true, false>(jobs, n, dev, stream);
+  }
+  return vec_out ? launch<T, kCol, false, true>(jobs, n, dev, stream)
+                 : launch<T, kCol, false, false>(jobs, n, dev, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
+                                  bool shifted, bool vec_out, const DeviceInfo& dev,
+                                  cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (dtype == 0) {
+    return colwise ? launch_variant<F32T, true>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<F32T, false>(jobs, n, shifted, vec_out, dev, stream);
+  }
+  return colwise ? launch_variant<BF16T, true>(jobs, n, shifted, vec_out, dev, stream)
+                 : launch_variant<BF16T, false>(jobs, n, shifted, vec_out, dev, stream);
+}
+
+}  // namespace mxfp8

@@ -46,6 +46,27 @@ struct CastParams {
   int32_t vec_out;     // both outputs' virtual bases are V-byte aligned: word stores
 };
 
+// One-pass quantisation of a fragment made of whole blocks: block maxima, E8M0
+// scales and E4M3 data from one kernel (amax outputs optional).
+struct FusedParams {
+  FragGeom g;
+  const void* in;
+  void* amax_r;        // [rows][ld_r] or nullptr
+  int64_t ld_r;
+  void* amax_c;        // [ceil(rows/32)][ld_c] or nullptr
+  int64_t ld_c;
+  uint8_t* s_r;        // [rows][ld_sr] E8M0
+  int64_t ld_sr;
+  uint8_t* s_c;        // [ceil(rows/32)][ld_sc] E8M0 (colwise kernel only)
+  int64_t ld_sc;
+  uint8_t* out_r;      // byte of flat element f lives at out + (f + out_shift)
+  uint8_t* out_c;
+  int64_t out_shift;
+  int32_t vec_c;       // colwise amax rows may take 16-byte stores
+  int32_t vec_sc;      // colwise scale rows may take V-byte stores
+  int32_t vec_out;     // outputs' virtual bases are V-byte aligned
+};
+
 // One direction of a scale update: scale[r][c] = E8M0(amax[r][c]), r < nrows, c < ncols.
 struct ScaleSegment {
   const void* amax;
@@ -103,6 +124,9 @@ cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool c
 cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
                                 bool shifted, bool vec_out, const DeviceInfo& dev,
                                 cudaStream_t stream);
+cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
+                                  bool shifted, bool vec_out, const DeviceInfo& dev,
+                                  cudaStream_t stream);
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,

@@ -151,3 +151,24 @@ def test_binding_raises_without_library(tmp_path):
             _capi.load(str(tmp_path / "nope.so"))
         finally:
             _capi._lib = saved
+
+
+def fused(lib, inp, ar, ac, sr, sc, qr, qc, rows, cols, start, out_off):
+    return lib.mxfp8_quantize_whole_blocks(*[ctypes.byref(t) for t in (inp, ar, ac, sr, sc, qr, qc)],
+                                           rows, cols, start, out_off, None)
+
+
+def test_fused_rejects_fragments_that_cut_blocks(lib):
+    rows, cols = 64, 256
+    sr, sc = T(P, U8, rows, 8), T(P, U8, 2, cols)
+    q = T(P, U8, rows * cols)
+    # row-only: the fragment must start and end on 1x32 block boundaries
+    assert fused(lib, T(P, F32, 100), E(), E(), sr, E(), q, E(), rows, cols, 0, 0) == 1
+    assert b"cuts a 1x32 block" in lib.mxfp8_last_error()
+    assert fused(lib, T(P, F32, 64), E(), E(), sr, E(), q, E(), rows, cols, 17, 17) == 1
+    # bidirectional: whole 32-row bands
+    assert fused(lib, T(P, F32, 256), E(), E(), sr, sc, q, q, rows, cols, 256, 256) == 1
+    assert b"cuts a 32x1 block" in lib.mxfp8_last_error()
+    # missing columnwise scales for a columnwise output, wrong amax dtype
+    assert fused(lib, T(P, F32, 32 * cols), E(), E(), sr, E(), q, q, rows, cols, 0, 0) == 4
+    assert fused(lib, T(P, F32, 32 * cols), T(P, BF16, rows, 8), E(), sr, sc, q, q, rows, cols, 0, 0) == 3

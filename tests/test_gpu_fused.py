@@ -1,0 +1,142 @@
+"""One-pass quantisation of fragments made of whole blocks: bit-identical to the oracle's
+whole-weight cast (and so to the split amax -> scales -> cast path) on the seeded
+workloads, ragged shapes, band-aligned and row-aligned fragments, misaligned fragment
+buffers and fragment-sized outputs."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp8_master_weight_gb300 import api
+from mxfp8_master_weight_gb300 import workloads as wl
+
+from flows import assert_bitwise, to_device, to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _fused(frag, rows, cols, start, colwise, *, shift=0, with_amax=True, out_offset=None):
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    dt = torch.float32 if frag.dtype == np.float32 else torch.bfloat16
+    x = to_device(frag, shift)
+    ar = torch.zeros((rr, rc), dtype=dt, device="cuda") if with_amax else None
+    ac = torch.zeros((cr, cc), dtype=dt, device="cuda") if (with_amax and colwise) else None
+    sr = torch.full((rr, rc), 0xEE, dtype=torch.uint8, device="cuda")
+    sc = torch.full((cr, cc), 0xEE, dtype=torch.uint8, device="cuda") if colwise else None
+    if out_offset is None:
+        out_offset, size = start, rows * cols
+    else:
+        size = frag.size + out_offset
+    qr = torch.full((size,), 0xA5, dtype=torch.uint8, device="cuda")
+    qc = torch.full((size,), 0xA5, dtype=torch.uint8, device="cuda") if colwise else None
+    api.mxfp8_quantize_whole_blocks(x, ar, ac, sr, sc, qr, qc, rows, cols, start, out_offset)
+    torch.cuda.synchronize()
+    h = lambda t: None if t is None else to_host(t)
+    return h(ar), h(ac), h(sr), h(sc), h(qr), h(qc)
+
+
+def _oracle_fragment(frag, rows, cols, start, colwise, out_offset=None):
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    ar = np.zeros((rr, rc), frag.dtype)
+    ac = np.zeros((cr, cc), frag.dtype) if colwise else None
+    oracle.partial_amax(frag, rows, cols, start, ar, ac)
+    sr = np.full((rr, rc), 0xEE, np.uint8)
+    sc = np.full((cr, cc), 0xEE, np.uint8) if colwise else None
+    # only blocks the fragment touches get a scale (untouched entries keep 0xEE)
+    touched_r = np.zeros((rr, rc), bool)
+    touched_c = np.zeros((cr, cc), bool)
+    k = np.arange(start, start + frag.size)
+    touched_r[k // cols, (k % cols) // 32] = True
+    touched_c[(k // cols) // 32, k % cols] = True
+    full_sr = np.zeros((rr, rc), np.uint8)
+    oracle.update_scales(ar, rr, rc, full_sr)
+    sr[touched_r] = full_sr[touched_r]
+    if colwise:
+        full_sc = np.zeros((cr, cc), np.uint8)
+        oracle.update_scales(ac, cr, cc, full_sc)
+        sc[touched_c] = full_sc[touched_c]
+    if out_offset is None:
+        out_offset, size = start, rows * cols
+    else:
+        size = frag.size + out_offset
+    qr = np.full(size, 0xA5, np.uint8)
+    qc = np.full(size, 0xA5, np.uint8) if colwise else None
+    oracle.partial_cast(frag, rows, cols, start, sr, sc, qr, qc, out_offset)
+    return ar, ac, sr, sc, qr, qc
+
+
+@pytest.mark.parametrize("colwise", [True, False])
+def test_fused_cfg4_headline(colwise):
+    w = wl.cfg4_headline()
+    got = _fused(w.data, w.rows, w.cols, 0, colwise)
+    want = oracle.full_cast(w.data, w.rows, w.cols, colwise)
+    assert_bitwise(got, want, f"fused cfg4 colwise={colwise}")
+
+
+@pytest.mark.parametrize("cfg", ["cfg1", "cfg3"])
+def test_fused_full_weights(cfg):
+    w = wl.cfg_by_name(cfg)
+    got = _fused(w.data, w.rows, w.cols, 0, True, with_amax=False)
+    want = oracle.full_cast(w.data, w.rows, w.cols, True)
+    assert_bitwise(got[2:], want[2:], f"fused {cfg}")
+    assert got[0] is None and got[1] is None
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(33, 65), (100, 70), (64, 4096 + 40), (97, 256), (1, 1)])
+def test_fused_ragged_full_weights(dtype, rows, cols):
+    rng = np.random.default_rng(rows + 1000 * cols)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(10.0) ** rng.uniform(-3, 3, rows * cols).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    for shift in (0, 1, 3):
+        got = _fused(x, rows, cols, 0, True, shift=shift)
+        want = oracle.full_cast(x, rows, cols, True)
+        assert_bitwise(got, want, f"fused {dtype} {rows}x{cols} shift {shift}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shift", [0, 1, 2, 5])
+def test_fused_band_and_row_aligned_fragments(dtype, shift):
+    rows, cols = 256, 1024
+    rng = np.random.default_rng(40 + shift)
+    x = wl.normal_f32(rng, rows * cols)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    # bidirectional: whole 32-row bands
+    start, end = 32 * cols * 2, 32 * cols * 7
+    frag = np.ascontiguousarray(x[start:end])
+    assert_bitwise(_fused(frag, rows, cols, start, True, shift=shift),
+                   _oracle_fragment(frag, rows, cols, start, True), f"bands {dtype} {shift}")
+    # row-only: start and end on 1x32 block boundaries inside rows and bands
+    start, end = 5 * cols + 64, 77 * cols + 992
+    frag = np.ascontiguousarray(x[start:end])
+    assert_bitwise(_fused(frag, rows, cols, start, False, shift=shift),
+                   _oracle_fragment(frag, rows, cols, start, False), f"rows {dtype} {shift}")
+    # fragment-sized output
+    assert_bitwise(_fused(frag, rows, cols, start, False, shift=shift, out_offset=0),
+                   _oracle_fragment(frag, rows, cols, start, False, out_offset=0),
+                   f"fragment output {dtype} {shift}")
+
+
+def test_fused_batched_equals_single():
+    rng = np.random.default_rng(44)
+    jobs, singles = [], []
+    for rows, cols, col in ((64, 512, True), (96, 256, False), (128, 1024, True)):
+        x = to_device(wl.normal_f32(rng, rows * cols))
+        (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+        outs = []
+        for _ in range(2):
+            outs.append([torch.zeros((rr, rc), dtype=torch.uint8, device="cuda"),
+                         torch.zeros((cr, cc), dtype=torch.uint8, device="cuda") if col else None,
+                         torch.zeros(rows * cols, dtype=torch.uint8, device="cuda"),
+                         torch.zeros(rows * cols, dtype=torch.uint8, device="cuda") if col else None])
+        a, b = outs
+        jobs.append((x, None, None, a[0], a[1], a[2], a[3], rows, cols, 0))
+        api.mxfp8_quantize_whole_blocks(x, None, None, b[0], b[1], b[2], b[3], rows, cols, 0)
+        singles.append((a, b))
+    api.mxfp8_quantize_whole_blocks_batched(jobs)
+    torch.cuda.synchronize()
+    for a, b in singles:
+        for u, v in zip(a, b):
+            assert (u is None and v is None) or torch.equal(u, v)
