@@ -175,6 +175,11 @@ typedef struct {
   int64_t rows, cols, start_offset;
 } mxfp8_amax_job;
 
+/* Model dtype the master values are rounded through before quantisation ("rounding
+ * through the model dtype", section "Changes").  The single-fragment entry points
+ * use BF16; jobs carry the choice (a zero-initialised job means BF16). */
+enum { MXFP8_MODEL_BF16 = 0, MXFP8_MODEL_F16 = 1 };
+
 typedef struct {
   mxfp8_tensor input;
   mxfp8_tensor scale_inv_rowwise;
@@ -182,6 +187,7 @@ typedef struct {
   mxfp8_tensor output_rowwise;
   mxfp8_tensor output_colwise; /* empty => row-only */
   int64_t rows, cols, start_offset, out_offset;
+  int32_t model_dtype;         /* MXFP8_MODEL_BF16 (0) or MXFP8_MODEL_F16 */
 } mxfp8_cast_job;
 
 typedef struct {
@@ -234,6 +240,7 @@ typedef struct {
   mxfp8_tensor output_rowwise;
   mxfp8_tensor output_colwise;    /* empty => row-only */
   int64_t rows, cols, start_offset, out_offset;
+  int32_t model_dtype;            /* MXFP8_MODEL_BF16 (0) or MXFP8_MODEL_F16 */
 } mxfp8_quantize_job;
 
 /* Batched form of mxfp8_quantize_whole_blocks, with the conventions of the other

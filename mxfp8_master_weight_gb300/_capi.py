@@ -39,7 +39,8 @@ class CastJob(ctypes.Structure):
     _fields_ = [("input", Tensor), ("scale_inv_rowwise", Tensor), ("scale_inv_colwise", Tensor),
                 ("output_rowwise", Tensor), ("output_colwise", Tensor),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
-                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64)]
+                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64),
+                ("model_dtype", ctypes.c_int32)]
 
 
 class ScaleJob(ctypes.Structure):
@@ -52,7 +53,12 @@ class QuantizeJob(ctypes.Structure):
                 ("scale_inv_rowwise", Tensor), ("scale_inv_colwise", Tensor),
                 ("output_rowwise", Tensor), ("output_colwise", Tensor),
                 ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
-                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64)]
+                ("start_offset", ctypes.c_int64), ("out_offset", ctypes.c_int64),
+                ("model_dtype", ctypes.c_int32)]
+
+
+MODEL_BF16, MODEL_F16 = 0, 1
+MODELS = {"bf16": MODEL_BF16, "f16": MODEL_F16, MODEL_BF16: MODEL_BF16, MODEL_F16: MODEL_F16}
 
 
 def empty_tensor() -> Tensor:

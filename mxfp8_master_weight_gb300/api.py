@@ -95,12 +95,18 @@ def mxfp8_update_scales(amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv
 
 def mxfp8_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
                        output_colwise, rows: int, cols: int, start_offset: int,
-                       out_offset: int | None = None, stream=None) -> None:
+                       out_offset: int | None = None, stream=None, model_dtype="bf16") -> None:
     """E4M3 bytes of the fragment into the outputs (out_offset defaults to start_offset:
-    a full-size output written in place; pass 0 for a fragment-sized output)."""
-    dev = _device_of(input, output_rowwise, output_colwise)
+    a full-size output written in place; pass 0 for a fragment-sized output).
+    ``model_dtype``: "bf16" (default) or "f16", the dtype values are rounded through."""
     if out_offset is None:
         out_offset = start_offset
+    if _capi.MODELS[model_dtype] != _capi.MODEL_BF16:
+        mxfp8_partial_cast_batched([(input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
+                                     output_colwise, rows, cols, start_offset, out_offset,
+                                     model_dtype)], stream=stream)
+        return
+    dev = _device_of(input, output_rowwise, output_colwise)
     args = [handle(input, "input"), handle(scale_inv_rowwise, "scale_inv_rowwise"),
             handle(scale_inv_colwise, "scale_inv_colwise"),
             handle(output_rowwise, "output_rowwise"), handle(output_colwise, "output_colwise")]
@@ -124,10 +130,11 @@ def _cast_jobs(jobs):
     for k, job in enumerate(jobs):
         inp, sr, sc, qr, qc, rows, cols, start = job[:8]
         out_offset = job[8] if len(job) > 8 and job[8] is not None else start
+        model = _capi.MODELS[job[9]] if len(job) > 9 else _capi.MODEL_BF16
         arr[k] = CastJob(handle(inp, "input"), handle(sr, "scale_inv_rowwise"),
                          handle(sc, "scale_inv_colwise"), handle(qr, "output_rowwise"),
                          handle(qc, "output_colwise"), int(rows), int(cols), int(start),
-                         int(out_offset))
+                         int(out_offset), model)
         keep += [t for t in (inp, sr, sc, qr, qc) if t is not None]
     return arr, keep
 
@@ -170,12 +177,18 @@ def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
 def mxfp8_quantize_whole_blocks(input, amax_rowwise, amax_colwise, scale_inv_rowwise,
                                 scale_inv_colwise, output_rowwise, output_colwise, rows: int,
                                 cols: int, start_offset: int, out_offset: int | None = None,
-                                stream=None) -> None:
+                                stream=None, model_dtype="bf16") -> None:
     """One-pass amax -> scales -> cast of a fragment made of whole blocks (amax outputs
     optional); bit-identical to the split calls on the same fragment."""
-    dev = _device_of(input, output_rowwise, output_colwise)
     if out_offset is None:
         out_offset = start_offset
+    if _capi.MODELS[model_dtype] != _capi.MODEL_BF16:
+        mxfp8_quantize_whole_blocks_batched(
+            [(input, amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
+              output_rowwise, output_colwise, rows, cols, start_offset, out_offset, model_dtype)],
+            stream=stream)
+        return
+    dev = _device_of(input, output_rowwise, output_colwise)
     names = ("input", "amax_rowwise", "amax_colwise", "scale_inv_rowwise", "scale_inv_colwise",
              "output_rowwise", "output_colwise")
     ts = (input, amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
@@ -194,8 +207,9 @@ def _quantize_jobs(jobs):
         ts = job[:7]
         rows, cols, start = job[7:10]
         out_offset = job[10] if len(job) > 10 and job[10] is not None else start
+        model = _capi.MODELS[job[11]] if len(job) > 11 else _capi.MODEL_BF16
         arr[k] = QuantizeJob(*[handle(t, n) for t, n in zip(ts, names)], int(rows), int(cols),
-                             int(start), int(out_offset))
+                             int(start), int(out_offset), model)
         keep += [t for t in ts if t is not None]
     return arr, keep
 

@@ -202,6 +202,8 @@ int prep_cast(const mxfp8_cast_job& job, CastParams* p, int* dtype, bool* colwis
   const int32_t dt = input->dtype;
   if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
     return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
+  if (job.model_dtype != MXFP8_MODEL_BF16 && job.model_dtype != MXFP8_MODEL_F16)
+    return fail(MXFP8_ERR_INVALID, "model_dtype must be MXFP8_MODEL_BF16 or MXFP8_MODEL_F16");
   if (is_empty(&job.scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
   if (is_empty(&job.output_rowwise)) return fail(MXFP8_ERR_MISSING, "output_rowwise is required");
   const int64_t rows = job.rows, cols = job.cols, out_offset = job.out_offset;
@@ -255,7 +257,7 @@ int prep_fused(const mxfp8_quantize_job& job, FusedParams* p, int* dtype, bool* 
   // the data side is validated exactly as a partial cast
   const mxfp8_cast_job cj = {job.input, job.scale_inv_rowwise, job.scale_inv_colwise,
                              job.output_rowwise, job.output_colwise, job.rows, job.cols,
-                             job.start_offset, job.out_offset};
+                             job.start_offset, job.out_offset, job.model_dtype};
   CastParams c;
   if (int rc = prep_cast(cj, &c, dtype, colwise, skip)) return rc;
   if (*skip) return MXFP8_OK;
@@ -413,15 +415,16 @@ int run_cast(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_cast(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : dt * 8 + col * 4 + (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+      key[i] = skip ? -1 : jobs[base + i].model_dtype * 16 + dt * 8 + col * 4 +
+                               (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
     }
-    for (int kk = 0; kk < 16; ++kk) {  // dtype x colwise x shifted x aligned output
+    for (int kk = 0; kk < 32; ++kk) {  // model x dtype x colwise x shifted x aligned output
       int n = 0;
       for (int i = 0; i <= m; ++i) {
         if (i < m && key[i] == kk) batch[n++] = win[i];
         if (n > 0 && (n == kGroupChunk || i == m)) {
-          if (int rc = cuda_status(mxfp8::launch_partial_cast(batch, n, kk >> 3, (kk >> 2) & 1,
-                                                              (kk >> 1) & 1, kk & 1, dev,
+          if (int rc = cuda_status(mxfp8::launch_partial_cast(batch, n, (kk >> 3) & 1, (kk >> 2) & 1,
+                                                              (kk >> 1) & 1, kk & 1, kk >> 4, dev,
                                                               static_cast<cudaStream_t>(stream)),
                                    "partial cast launch"))
             return rc;
@@ -483,15 +486,16 @@ int run_fused(const mxfp8_quantize_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_fused(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : dt * 8 + col * 4 + (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+      key[i] = skip ? -1 : jobs[base + i].model_dtype * 16 + dt * 8 + col * 4 +
+                               (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
     }
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 0; kk < 32; ++kk) {
       int n = 0;
       for (int i = 0; i <= m; ++i) {
         if (i < m && key[i] == kk) batch[n++] = win[i];
         if (n > 0 && (n == kGroupChunk || i == m)) {
-          if (int rc = cuda_status(mxfp8::launch_fused_quantize(batch, n, kk >> 3, (kk >> 2) & 1,
-                                                                (kk >> 1) & 1, kk & 1, dev,
+          if (int rc = cuda_status(mxfp8::launch_fused_quantize(batch, n, (kk >> 3) & 1, (kk >> 2) & 1,
+                                                                (kk >> 1) & 1, kk & 1, kk >> 4, dev,
                                                                 static_cast<cudaStream_t>(stream)),
                                    "fused quantize launch"))
             return rc;
@@ -570,7 +574,8 @@ int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_
                        int64_t start_offset, int64_t out_offset, void* stream) {
   const mxfp8_cast_job job = {or_empty(input), or_empty(scale_inv_rowwise),
                               or_empty(scale_inv_colwise), or_empty(output_rowwise),
-                              or_empty(output_colwise), rows, cols, start_offset, out_offset};
+                              or_empty(output_colwise), rows, cols, start_offset, out_offset,
+                              MXFP8_MODEL_BF16};
   return run_cast(&job, 1, stream);
 }
 
@@ -586,7 +591,7 @@ int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_ro
   const mxfp8_quantize_job job = {or_empty(input), or_empty(amax_rowwise), or_empty(amax_colwise),
                                   or_empty(scale_inv_rowwise), or_empty(scale_inv_colwise),
                                   or_empty(output_rowwise), or_empty(output_colwise),
-                                  rows, cols, start_offset, out_offset};
+                                  rows, cols, start_offset, out_offset, MXFP8_MODEL_BF16};
   return run_fused(&job, 1, stream);
 }
 

@@ -56,7 +56,7 @@ __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t
 
 // Whole tile inside the fragment: 16-byte loads (realigned for a shifted virtual
 // base), one scale byte per row, word stores when the outputs are aligned.
-template <class T, bool kCol, bool kShift, bool kVec>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -79,7 +79,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float y[T::V];
-      model_values<T>(v[r], y);
+      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = scale_multiplier(sb[r]);
 #pragma unroll
@@ -95,7 +95,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
 // time (16-byte loads for chunks wholly inside the fragment, predicated per-element
 // loads otherwise), one scale byte per row and block, and stores only the
 // fragment's elements (a word per whole chunk when the output is aligned).
-template <class T, bool kCol, bool kVec>
+template <class T, bool kCol, bool kVec, int kModel>
 __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0, int64_t col0,
                                               int lane) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
@@ -127,7 +127,7 @@ __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0,
       if (bits == 0) continue;
       const int64_t i = row0 + rb + r;
       float y[T::V];
-      model_values<T>(v[r], y);
+      model_values<T, kModel>(v[r], y);
       float mr[T::V];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = mrow[r];
@@ -152,7 +152,7 @@ __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0,
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int N>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
 __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   constexpr int TW = tile_width<T>();
@@ -164,20 +164,20 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
     const CastParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
     if (kind == kTileFast) {
-      cast_tile_fast<T, kCol, kShift, kVec>(p, row0, col0, lane);
+      cast_tile_fast<T, kCol, kShift, kVec, kModel>(p, row0, col0, lane);
     } else if (kind == kTileMasked) {
-      cast_tile_masked<T, kCol, kVec>(p, row0, col0, lane);
+      cast_tile_masked<T, kCol, kVec, kModel>(p, row0, col0, lane);
     }
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int N>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
 cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_partial_cast<T, kCol, kShift, kVec, N>, kThreads, 0);
+        &occ, k_partial_cast<T, kCol, kShift, kVec, kModel, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
@@ -186,44 +186,56 @@ cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaS
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  k_partial_cast<T, kCol, kShift, kVec, N><<<grid, kThreads, 0, stream>>>(b);
+  k_partial_cast<T, kCol, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
-template <class T, bool kCol, bool kShift, bool kVec>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 cudaError_t launch(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  if (n == 1) return launch_n<T, kCol, kShift, kVec, 1>(jobs, 1, dev, stream);
+  // single-job kernels only for the BF16 model dtype (the common case); FP16-model
+  // jobs always go through the batch kernel
+  if constexpr (kModel == kModelBF16) {
+    if (n == 1) return launch_n<T, kCol, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+  }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
     const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
-    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-template <class T, bool kCol>
+template <class T, bool kCol, int kModel>
 cudaError_t launch_variant(const CastParams* jobs, int n, bool shifted, bool vec_out,
                            const DeviceInfo& dev, cudaStream_t stream) {
   if (shifted) {
-    return vec_out ? launch<T, kCol, true, true>(jobs, n, dev, stream)
-                   : launch<T, kCol, true, false>(jobs, n, dev, stream);
+    return vec_out ? launch<T, kCol, true, true, kModel>(jobs, n, dev, stream)
+                   : launch<T, kCol, true, false, kModel>(jobs, n, dev, stream);
   }
-  return vec_out ? launch<T, kCol, false, true>(jobs, n, dev, stream)
-                 : launch<T, kCol, false, false>(jobs, n, dev, stream);
+  return vec_out ? launch<T, kCol, false, true, kModel>(jobs, n, dev, stream)
+                 : launch<T, kCol, false, false, kModel>(jobs, n, dev, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
-                                bool shifted, bool vec_out, const DeviceInfo& dev,
-                                cudaStream_t stream) {
+                                  bool shifted, bool vec_out, int model, const DeviceInfo& dev,
+                                  cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  if (dtype == 0) {
-    return colwise ? launch_variant<F32T, true>(jobs, n, shifted, vec_out, dev, stream)
-                   : launch_variant<F32T, false>(jobs, n, shifted, vec_out, dev, stream);
+  if (model == kModelF16) {
+    if (dtype == 0) {
+      return colwise ? launch_variant<F32T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
+                     : launch_variant<F32T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
+    }
+    return colwise ? launch_variant<BF16T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<BF16T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
   }
-  return colwise ? launch_variant<BF16T, true>(jobs, n, shifted, vec_out, dev, stream)
-                 : launch_variant<BF16T, false>(jobs, n, shifted, vec_out, dev, stream);
+  if (dtype == 0) {
+    return colwise ? launch_variant<F32T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<F32T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
+  }
+  return colwise ? launch_variant<BF16T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
+                 : launch_variant<BF16T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
 }
 
 }  // namespace mxfp8

@@ -187,17 +187,54 @@ __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w 
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // ---------------------------------------------------------------- cast of one chunk
-// Model-dtype values of one input chunk.
-template <class T>
+// Model dtypes the master values are rounded through before quantisation.
+constexpr int kModelBF16 = 0;
+constexpr int kModelF16 = 1;
+
+// Two FP32 values rounded to IEEE FP16 (nearest-even, overflow to infinity); lo in
+// the low half.
+__device__ __forceinline__ uint32_t f16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ float f16_lo(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, l; }" : "=f"(f) : "r"(w));
+  return f;
+}
+__device__ __forceinline__ float f16_hi(uint32_t w) {
+  float f;
+  asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.f32.f16 %0, h; }" : "=f"(f) : "r"(w));
+  return f;
+}
+
+// Model-dtype values of one input chunk: BF16 (identity for BF16 input) or FP16.
+template <class T, int kModel = kModelBF16>
 __device__ __forceinline__ void model_values(const uint4& c, float (&y)[T::V]) {
   if constexpr (T::kBytes == 4) {
-    const uint32_t w0 = bf16x2_rn(__uint_as_float(c.x), __uint_as_float(c.y));
-    const uint32_t w1 = bf16x2_rn(__uint_as_float(c.z), __uint_as_float(c.w));
-    y[0] = bf16_lo(w0); y[1] = bf16_hi(w0); y[2] = bf16_lo(w1); y[3] = bf16_hi(w1);
+    const uint32_t w0 = kModel == kModelF16 ? f16x2_rn(__uint_as_float(c.x), __uint_as_float(c.y))
+                                            : bf16x2_rn(__uint_as_float(c.x), __uint_as_float(c.y));
+    const uint32_t w1 = kModel == kModelF16 ? f16x2_rn(__uint_as_float(c.z), __uint_as_float(c.w))
+                                            : bf16x2_rn(__uint_as_float(c.z), __uint_as_float(c.w));
+    if constexpr (kModel == kModelF16) {
+      y[0] = f16_lo(w0); y[1] = f16_hi(w0); y[2] = f16_lo(w1); y[3] = f16_hi(w1);
+    } else {
+      y[0] = bf16_lo(w0); y[1] = bf16_hi(w0); y[2] = bf16_lo(w1); y[3] = bf16_hi(w1);
+    }
   } else {
     const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) { y[2 * k] = bf16_lo(w[k]); y[2 * k + 1] = bf16_hi(w[k]); }
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (kModel == kModelF16) {
+        const uint32_t h = f16x2_rn(bf16_lo(w[k]), bf16_hi(w[k]));
+        y[2 * k] = f16_lo(h);
+        y[2 * k + 1] = f16_hi(h);
+      } else {
+        y[2 * k] = bf16_lo(w[k]);
+        y[2 * k + 1] = bf16_hi(w[k]);
+      }
+    }
   }
 }
 

@@ -74,7 +74,7 @@ __device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t ro
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t row0, int64_t col0,
                                                 int lane, RowScales& rsc, int warp) {
   const int64_t cols = p.g.cols;
@@ -121,7 +121,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float y[T::V];
-      model_values<T>(v[r], y);
+      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
 #pragma unroll
@@ -136,7 +136,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 
 // Tile cut by the fragment boundary or the matrix edge.  Every block the fragment
 // touches is whole, so the maxima over the loaded elements are the block maxima.
-template <class T, bool kCol, bool kVec>
+template <class T, bool kCol, bool kVec, int kModel>
 __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row0, int64_t col0,
                                                int lane, RowScales& rsc, int warp) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
@@ -192,7 +192,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
       if (bits == 0) continue;
       float y[T::V];
-      model_values<T>(v[r], y);
+      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
 #pragma unroll
@@ -219,7 +219,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
   __syncwarp();
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int N>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
 __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const __grid_constant__ JobBatch<FusedParams, N> b) {
   __shared__ RowScales rsc;
@@ -233,20 +233,20 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const FusedParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
     if (kind == kTileFast) {
-      fused_tile_fast<T, kCol, kShift, kVec>(p, row0, col0, lane, rsc, warp);
+      fused_tile_fast<T, kCol, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
     } else if (kind == kTileMasked) {
-      fused_tile_masked<T, kCol, kVec>(p, row0, col0, lane, rsc, warp);
+      fused_tile_masked<T, kCol, kVec, kModel>(p, row0, col0, lane, rsc, warp);
     }
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int N>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
 cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_fused_quantize<T, kCol, kShift, kVec, N>, kThreads, 0);
+        &occ, k_fused_quantize<T, kCol, kShift, kVec, kModel, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
@@ -255,44 +255,56 @@ cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cuda
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  k_fused_quantize<T, kCol, kShift, kVec, N><<<grid, kThreads, 0, stream>>>(b);
+  k_fused_quantize<T, kCol, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
-template <class T, bool kCol, bool kShift, bool kVec>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  if (n == 1) return launch_n<T, kCol, kShift, kVec, 1>(jobs, 1, dev, stream);
+  // single-job kernels only for the BF16 model dtype (the common case); FP16-model
+  // jobs always go through the batch kernel
+  if constexpr (kModel == kModelBF16) {
+    if (n == 1) return launch_n<T, kCol, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+  }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
     const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
-    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-template <class T, bool kCol>
+template <class T, bool kCol, int kModel>
 cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool vec_out,
                            const DeviceInfo& dev, cudaStream_t stream) {
   if (shifted) {
-    return vec_out ? launch<T, kCol, true, true>(jobs, n, dev, stream)
-                   : launch<T, kCol, true, false>(jobs, n, dev, stream);
+    return vec_out ? launch<T, kCol, true, true, kModel>(jobs, n, dev, stream)
+                   : launch<T, kCol, true, false, kModel>(jobs, n, dev, stream);
   }
-  return vec_out ? launch<T, kCol, false, true>(jobs, n, dev, stream)
-                 : launch<T, kCol, false, false>(jobs, n, dev, stream);
+  return vec_out ? launch<T, kCol, false, true, kModel>(jobs, n, dev, stream)
+                 : launch<T, kCol, false, false, kModel>(jobs, n, dev, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
-                                  bool shifted, bool vec_out, const DeviceInfo& dev,
+                                  bool shifted, bool vec_out, int model, const DeviceInfo& dev,
                                   cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  if (dtype == 0) {
-    return colwise ? launch_variant<F32T, true>(jobs, n, shifted, vec_out, dev, stream)
-                   : launch_variant<F32T, false>(jobs, n, shifted, vec_out, dev, stream);
+  if (model == kModelF16) {
+    if (dtype == 0) {
+      return colwise ? launch_variant<F32T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
+                     : launch_variant<F32T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
+    }
+    return colwise ? launch_variant<BF16T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<BF16T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
   }
-  return colwise ? launch_variant<BF16T, true>(jobs, n, shifted, vec_out, dev, stream)
-                 : launch_variant<BF16T, false>(jobs, n, shifted, vec_out, dev, stream);
+  if (dtype == 0) {
+    return colwise ? launch_variant<F32T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
+                   : launch_variant<F32T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
+  }
+  return colwise ? launch_variant<BF16T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
+                 : launch_variant<BF16T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
 }
 
 }  // namespace mxfp8

@@ -121,11 +121,12 @@ inline int64_t fill_batch(JobBatch<P, N>& b, const P* jobs, int n) {
 // CUDA launch status.
 cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool colwise,
                                 bool shifted, const DeviceInfo& dev, cudaStream_t stream);
+// model: 0 = round through BF16, 1 = round through FP16.
 cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
-                                bool shifted, bool vec_out, const DeviceInfo& dev,
+                                bool shifted, bool vec_out, int model, const DeviceInfo& dev,
                                 cudaStream_t stream);
 cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
-                                  bool shifted, bool vec_out, const DeviceInfo& dev,
+                                  bool shifted, bool vec_out, int model, const DeviceInfo& dev,
                                   cudaStream_t stream);
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);

@@ -52,6 +52,9 @@ def _load():
             lib.oracle_update_scales.argtypes = [vp, ctypes.c_int, i64, i64, i64, vp, i64]
             lib.oracle_partial_cast.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, vp, i64, vp, i64,
                                                 vp, vp, i64]
+            lib.oracle_partial_cast_model.argtypes = [vp, ctypes.c_int, ctypes.c_int, i64, i64, i64, i64,
+                                                      vp, i64, vp, i64, vp, vp, i64]
+            lib.oracle_f16_bits_array.argtypes = [vp, vp, i64]
             lib.oracle_bf16_rne_bits_array.argtypes = [vp, vp, i64]
             lib.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
             lib.oracle_e8m0_array.argtypes = [vp, vp, i64]
@@ -89,6 +92,17 @@ def bf16_rne_bits(x: np.ndarray) -> np.ndarray:
     out = np.empty(x.shape, np.uint16)
     _load().oracle_bf16_rne_bits_array(_ptr(x), _ptr(out), x.size)
     return out
+
+
+def f16_bits(v: np.ndarray) -> np.ndarray:
+    """IEEE FP16 bit patterns of float64 values, round to nearest, ties to even."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint16)
+    _load().oracle_f16_bits_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+MODELS = {"bf16": 0, "f16": 1}
 
 
 def e4m3_encode(v: np.ndarray) -> np.ndarray:
@@ -155,8 +169,10 @@ def update_scales(amax: np.ndarray, nrows: int, ncols: int, scale: np.ndarray) -
 
 def partial_cast(frag: np.ndarray, rows: int, cols: int, start: int,
                  scale_r: np.ndarray, scale_c: np.ndarray | None,
-                 out_r: np.ndarray, out_c: np.ndarray | None, out_offset: int) -> None:
-    """In place: E4M3 bytes of the fragment into out_r / out_c at out_offset + (k - start)."""
+                 out_r: np.ndarray, out_c: np.ndarray | None, out_offset: int,
+                 model: str = "bf16") -> None:
+    """In place: E4M3 bytes of the fragment into out_r / out_c at out_offset + (k - start);
+    values are first rounded to the model dtype (``"bf16"`` or ``"f16"``)."""
     frag = _c(np.ascontiguousarray(frag))
     for o in (out_r, out_c):
         if o is not None:
@@ -165,8 +181,8 @@ def partial_cast(frag: np.ndarray, rows: int, cols: int, start: int,
                 raise ValueError("output too small")
     if out_c is not None and scale_c is None:
         raise ValueError("columnwise scales are required for a columnwise output")
-    _load().oracle_partial_cast(_ptr(frag), _dtype_code(frag), rows, cols, start, frag.size,
-                                _ptr(scale_r), scale_r.shape[1],
+    _load().oracle_partial_cast_model(_ptr(frag), _dtype_code(frag), MODELS[model], rows, cols,
+                                      start, frag.size, _ptr(scale_r), scale_r.shape[1],
                                 _ptr(scale_c) if out_c is not None else None,
                                 scale_c.shape[1] if out_c is not None else 0,
                                 _ptr(out_r), _ptr(out_c), out_offset)
@@ -178,7 +194,7 @@ def block_dims(rows: int, cols: int):
     return (rows, (cols + 31) // 32), ((rows + 31) // 32, cols)
 
 
-def full_cast(x: np.ndarray, rows: int, cols: int, colwise: bool = True):
+def full_cast(x: np.ndarray, rows: int, cols: int, colwise: bool = True, model: str = "bf16"):
     """Whole-weight flow: amax over every element, scales, cast.
 
     Returns (amax_r, amax_c, scale_r, scale_c, q_r, q_c); the columnwise items are
@@ -197,5 +213,5 @@ def full_cast(x: np.ndarray, rows: int, cols: int, colwise: bool = True):
         update_scales(amax_c, *cdim, scale_c)
     q_r = np.zeros(rows * cols, np.uint8)
     q_c = np.zeros(rows * cols, np.uint8) if colwise else None
-    partial_cast(x, rows, cols, 0, scale_r, scale_c, q_r, q_c, 0)
+    partial_cast(x, rows, cols, 0, scale_r, scale_c, q_r, q_c, 0, model=model)
     return amax_r, amax_c, scale_r, scale_c, q_r, q_c

@@ -42,6 +42,8 @@
 
 #define ORACLE_F32 0
 #define ORACLE_BF16 1
+#define ORACLE_MODEL_BF16 0
+#define ORACLE_MODEL_F16 1
 
 /* ---------- element access ---------------------------------------------------- */
 
@@ -92,6 +94,35 @@ double oracle_bf16_round(float x) {
     double r = nearbyint(a / quantum) * quantum;  /* a/quantum is exact in double */
     if (r >= ldexp(1.0, 128)) r = INFINITY;       /* past the largest finite BF16 */
     return v < 0 ? -r : r;
+}
+
+/* Round a value to IEEE FP16 (11 significant bits, normal exponents -14..15,
+ * subnormal spacing 2^-24), nearest with ties to even; past the largest finite
+ * value 65504 by half a unit (65520) the result is infinite.  Returns a double.
+ * The model dtype may be FP16 instead of BF16 ("rounding through the model dtype",
+ * section "Changes"). */
+double oracle_f16_round(double v) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    double a = fabs(v);
+    int p = floor_log2(a);
+    if (p < -14) p = -14;                 /* subnormals share the spacing 2^-24 */
+    double quantum = ldexp(1.0, p - 10);  /* 11 significant bits */
+    double r = nearbyint(a / quantum) * quantum;
+    if (r > 65504.0) r = INFINITY;
+    return v < 0 ? -r : r;
+}
+
+/* FP16 bit pattern of oracle_f16_round(x) (for the pins). */
+uint16_t oracle_f16_bits(double v) {
+    double r = oracle_f16_round(v);
+    uint16_t sign = signbit(r) ? 0x8000 : 0;
+    double a = fabs(r);
+    if (isnan(r)) return 0x7E00;
+    if (isinf(a)) return sign | 0x7C00;
+    if (a == 0.0) return sign;
+    int p = floor_log2(a);
+    if (p < -14) return sign | (uint16_t)(a / ldexp(1.0, -24));            /* subnormal */
+    return sign | (uint16_t)(((p + 15) << 10) | (int)(ldexp(a, -p) * 1024.0 - 1024.0));
 }
 
 /* BF16 bit pattern of oracle_bf16_round(x). */
@@ -246,27 +277,38 @@ int oracle_update_scales(const void *amax, int dtype, int64_t nrows, int64_t nco
 
 /* ---------- step 4: partial cast --------------------------------------------- */
 
-/* For every fragment element k (element (i, j) of the weight): y = BF16 rounding
- * of the master value (identity for BF16 input); rowwise byte = E4M3 of
+/* For every fragment element k (element (i, j) of the weight): y = the master value
+ * rounded to the model dtype (BF16: identity for BF16 input; FP16: IEEE half); rowwise byte = E4M3 of
  * y * 2^-e with the scale of row block (i, j/32); columnwise byte (only when
  * out_c is non-NULL) with the scale of column block (i/32, j).  Byte k is
  * written at out_offset + (k - start); nothing else is written.
  * scale_c is ignored when out_c is NULL. */
-int oracle_partial_cast(const void *frag, int dtype, int64_t rows, int64_t cols,
-                        int64_t start, int64_t len,
-                        const uint8_t *scale_r, int64_t ld_sr,
-                        const uint8_t *scale_c, int64_t ld_sc,
-                        uint8_t *out_r, uint8_t *out_c, int64_t out_offset) {
+int oracle_partial_cast_model(const void *frag, int dtype, int model, int64_t rows, int64_t cols,
+                              int64_t start, int64_t len,
+                              const uint8_t *scale_r, int64_t ld_sr,
+                              const uint8_t *scale_c, int64_t ld_sc,
+                              uint8_t *out_r, uint8_t *out_c, int64_t out_offset) {
     (void)rows;
     for (int64_t k = start; k < start + len; ++k) {
         int64_t i = k / cols, j = k % cols;
         double x = load_value(frag, dtype, k - start);
-        double y = (dtype == ORACLE_F32) ? oracle_bf16_round((float)x) : x;
+        double y;
+        if (model == ORACLE_MODEL_F16) y = oracle_f16_round(x);
+        else y = (dtype == ORACLE_F32) ? oracle_bf16_round((float)x) : x;
         int64_t o = out_offset + (k - start);
         out_r[o] = oracle_quantize(y, scale_r[i * ld_sr + j / 32]);
         if (out_c) out_c[o] = oracle_quantize(y, scale_c[(i / 32) * ld_sc + j]);
     }
     return 0;
+}
+
+int oracle_partial_cast(const void *frag, int dtype, int64_t rows, int64_t cols,
+                        int64_t start, int64_t len,
+                        const uint8_t *scale_r, int64_t ld_sr,
+                        const uint8_t *scale_c, int64_t ld_sc,
+                        uint8_t *out_r, uint8_t *out_c, int64_t out_offset) {
+    return oracle_partial_cast_model(frag, dtype, ORACLE_MODEL_BF16, rows, cols, start, len,
+                                     scale_r, ld_sr, scale_c, ld_sc, out_r, out_c, out_offset);
 }
 
 /* ---------- element-wise batch helpers for the pins -------------------------- */
@@ -277,6 +319,10 @@ void oracle_bf16_rne_bits_array(const float *x, uint16_t *out, int64_t n) {
 
 void oracle_e4m3_encode_array(const double *v, uint8_t *out, int64_t n) {
     for (int64_t k = 0; k < n; ++k) out[k] = oracle_e4m3_encode(v[k]);
+}
+
+void oracle_f16_bits_array(const double *v, uint16_t *out, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_f16_bits(v[k]);
 }
 
 void oracle_e8m0_array(const double *amax, uint8_t *out, int64_t n) {

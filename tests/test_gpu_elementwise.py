@@ -104,3 +104,32 @@ def test_max_reduce_nan_propagates():
     api.mxfp8_amax_max_reduce(d, out)
     h = to_host(out)
     assert np.isnan(h[5]) and np.isinf(h[6]) and h[0] == 0.0
+
+
+def _cast_with_scales_model(x, rows, cols, s_r, s_c, model):
+    xd = to_device(x)
+    qr = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    qc = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    api.mxfp8_partial_cast(xd, torch.from_numpy(s_r).cuda(), torch.from_numpy(s_c).cuda(), qr, qc,
+                           rows, cols, 0, model_dtype=model)
+    want_r = np.zeros(rows * cols, np.uint8)
+    want_c = np.zeros(rows * cols, np.uint8)
+    oracle.partial_cast(x, rows, cols, 0, s_r, s_c, want_r, want_c, 0, model=model)
+    return to_host(qr), to_host(qc), want_r, want_c
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_cast_f16_model_dtype(dtype):
+    """Rounding through an FP16 model dtype: every BF16 pattern / random FP32 patterns."""
+    rows, cols = 16, 65536
+    rng = np.random.default_rng(5)
+    if dtype == "bf16":
+        x = np.tile(np.arange(65536, dtype=np.uint16), rows)
+    else:
+        bits = rng.integers(0, 2 ** 32, rows * cols, dtype=np.uint64).astype(np.uint32)
+        mod = rng.standard_normal(rows * cols // 2).astype(np.float32) * 2.0 ** rng.integers(-30, 20, rows * cols // 2)
+        bits[: mod.size] = mod.astype(np.float32).view(np.uint32)
+        x = rng.permutation(bits).view(np.float32)
+    s_r, s_c = _scale_grids(rows, cols, 6)
+    gr, gc, wr, wc = _cast_with_scales_model(x, rows, cols, s_r, s_c, "f16")
+    assert_bitwise((gr, gc), (wr, wc), f"f16 model {dtype}")

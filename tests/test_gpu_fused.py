@@ -140,3 +140,40 @@ def test_fused_batched_equals_single():
     for a, b in singles:
         for u, v in zip(a, b):
             assert (u is None and v is None) or torch.equal(u, v)
+
+
+@pytest.mark.parametrize("colwise", [True, False])
+def test_fused_f16_model(colwise):
+    rows, cols = 512, 2048
+    rng = np.random.default_rng(45)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(2.0) ** rng.integers(-20, 20, rows * cols).astype(np.float32)
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    xd = to_device(x)
+    sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda") if colwise else None
+    qr = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    qc = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda") if colwise else None
+    api.mxfp8_quantize_whole_blocks(xd, None, None, sr, sc, qr, qc, rows, cols, 0, model_dtype="f16")
+    torch.cuda.synchronize()
+    want = oracle.full_cast(x, rows, cols, colwise, model="f16")
+    got = (None, None, to_host(sr), None if sc is None else to_host(sc), to_host(qr),
+           None if qc is None else to_host(qc))
+    assert_bitwise(got[2:], want[2:], f"fused f16 colwise={colwise}")
+
+
+def test_batched_cast_mixed_model_dtypes():
+    rows, cols = 64, 512
+    rng = np.random.default_rng(46)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(1e3)
+    xd = to_device(x)
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    sr = torch.full((rr, rc), 120, dtype=torch.uint8, device="cuda")
+    outs = {m: torch.zeros(rows * cols, dtype=torch.uint8, device="cuda") for m in ("bf16", "f16")}
+    api.mxfp8_partial_cast_batched([(xd, sr, None, outs["bf16"], None, rows, cols, 0, None, "bf16"),
+                                    (xd, sr, None, outs["f16"], None, rows, cols, 0, None, "f16")])
+    torch.cuda.synchronize()
+    hs = to_host(sr)
+    for m, q in outs.items():
+        want = np.zeros(rows * cols, np.uint8)
+        oracle.partial_cast(x, rows, cols, 0, hs, None, want, None, 0, model=m)
+        assert np.array_equal(to_host(q), want), m

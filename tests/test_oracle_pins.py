@@ -368,3 +368,48 @@ def test_scale_ff_and_nan_conventions(oracle_mod):
     assert oracle_mod.quantize(float("inf"), 119) == 0x7E
     assert oracle_mod.quantize(float("-inf"), 119) == 0xFE
     assert oracle_mod.quantize(-1e-30, 119) == 0x80
+
+
+# ------------------------------------------------------------------ FP16 model dtype
+
+def test_f16_golden_points(oracle_mod):
+    # hand-derived from the IEEE half-precision definition
+    pts = {1.0: 0x3C00, 65504.0: 0x7BFF, 65519.99: 0x7BFF, 65520.0: 0x7C00, 2.0 ** -24: 0x0001,
+           2.0 ** -25: 0x0000, 3 * 2.0 ** -26: 0x0001, -0.0: 0x8000, 0.1: 0x2E66, 2.0 ** -14: 0x0400,
+           1.0 + 2.0 ** -11: 0x3C00, 1.0 + 3 * 2.0 ** -11: 0x3C02, -2.5: 0xC100}
+    got = oracle_mod.f16_bits(np.array(list(pts.keys())))
+    assert [int(g) for g in got] == list(pts.values())
+
+
+def test_f16_vs_torch_and_neighbours(oracle_mod):
+    rng = np.random.default_rng(12)
+    bits = rng.integers(0, 2 ** 32, 1_000_000, dtype=np.uint64).astype(np.uint32)
+    x = bits.view(np.float32)
+    x = x[np.isfinite(x)]
+    mod = (rng.standard_normal(500_000) * 2.0 ** rng.uniform(-30, 18, 500_000)).astype(np.float32)
+    x = np.concatenate([x, mod])
+    got = oracle_mod.f16_bits(x.astype(np.float64))
+    ref = torch.from_numpy(x.copy()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+    # independent: nearest of the two FP16 values bracketing x (np.float16 grid), ties to even
+    small = mod[np.abs(mod) < 60000].astype(np.float64)
+    lo = np.abs(small).astype(np.float16)  # some neighbour; refine by stepping
+    cand = np.stack([np.nextafter(lo, np.float16(0)), lo, np.nextafter(lo, np.float16(np.inf))]).astype(np.float64)
+    d = np.abs(cand - np.abs(small))
+    best = d.min(axis=0)
+    assert np.all(np.abs(oracle_mod.f16_bits(np.abs(small)).view(np.float16).astype(np.float64)
+                         - np.abs(small)) == best)
+
+
+def test_cast_with_f16_model(oracle_mod):
+    rng = np.random.default_rng(13)
+    rows, cols = 64, 96
+    x = wl.normal_f32(rng, rows * cols) * np.float32(2.0) ** rng.integers(-20, 20, rows * cols).astype(np.float32)
+    a = oracle_mod.full_cast(x, rows, cols, True, model="f16")
+    yh = oracle_mod.f16_bits(x.astype(np.float64)).view(np.float16).astype(np.float64).reshape(rows, cols)
+    ii, jj = np.meshgrid(np.arange(rows), np.arange(cols), indexing="ij")
+    v = yh * 2.0 ** (127 - a[2][ii, jj // 32].astype(np.float64))
+    assert np.array_equal(a[4], oracle_mod.e4m3_encode(v.ravel()))
+    # the amax and scales do not depend on the model dtype
+    b = oracle_mod.full_cast(x, rows, cols, True, model="bf16")
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
