@@ -248,6 +248,26 @@ typedef struct {
 int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
                                         void* stream);
 
+/*
+ * Scale layout for GEMM consumers.  Rearranges a compact E8M0 grid into the layout in
+ * which block-scaled tensor-core GEMMs read scale factors: the logical matrix L (the
+ * grid when transpose == 0; its transpose when transpose == 1, e.g. a columnwise
+ * [ceil(rows/32)][cols] grid consumed as [cols][ceil(rows/32)]) is padded with zero
+ * bytes to multiples of 128 rows and 4 columns and cut into 128x4 tiles, stored in
+ * row-major tile order, 512 bytes each; inside a tile element (r, c) sits at byte
+ * (r % 32) * 16 + (r / 32) * 4 + c.  (An output format next to the path: the pages
+ * only require padded scale grids.)
+ *
+ * scale_inv [in]  U8 2-D [>= nrows][>= ncols] (row stride shape[1]).
+ * out       [out] U8, numel >= mxfp8_swizzled_scales_size(nrows, ncols, transpose).
+ * Errors: 1 bad sizes or transpose flag, 2 out too small, 3 dtype, 4 missing tensor.
+ */
+int mxfp8_swizzle_scales(const mxfp8_tensor* scale_inv, mxfp8_tensor* out, int64_t nrows,
+                         int64_t ncols, int32_t transpose, void* stream);
+
+/* Bytes of the GEMM layout of an nrows x ncols grid (transpose as above). */
+int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 const char* mxfp8_last_error(void);
 

@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "shape mismatch", 3: "dtype m
 EXPORTED = ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
             "mxfp8_partial_cast", "mxfp8_partial_amax_batched", "mxfp8_update_scales_batched",
             "mxfp8_partial_cast_batched", "mxfp8_quantize_whole_blocks",
-            "mxfp8_quantize_whole_blocks_batched", "mxfp8_last_error", "mxfp8_version")
+            "mxfp8_quantize_whole_blocks_batched", "mxfp8_swizzle_scales",
+            "mxfp8_swizzled_scales_size", "mxfp8_last_error", "mxfp8_version")
 
 
 class Tensor(ctypes.Structure):
@@ -99,11 +100,14 @@ def load(path: str | None = None):
         lib.mxfp8_partial_cast_batched.argtypes = [ctypes.POINTER(CastJob), i32, vp]
         lib.mxfp8_quantize_whole_blocks.argtypes = [T, T, T, T, T, T, T, i64, i64, i64, i64, vp]
         lib.mxfp8_quantize_whole_blocks_batched.argtypes = [ctypes.POINTER(QuantizeJob), i32, vp]
+        lib.mxfp8_swizzle_scales.argtypes = [T, T, i64, i64, i32, vp]
+        lib.mxfp8_swizzled_scales_size.argtypes = [i64, i64, i32]
+        lib.mxfp8_swizzled_scales_size.restype = i64
         for name in ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",
                      "mxfp8_partial_cast", "mxfp8_partial_amax_batched",
                      "mxfp8_update_scales_batched", "mxfp8_partial_cast_batched",
                      "mxfp8_quantize_whole_blocks", "mxfp8_quantize_whole_blocks_batched",
-                     "mxfp8_version"):
+                     "mxfp8_swizzle_scales", "mxfp8_version"):
             getattr(lib, name).restype = ctypes.c_int
         lib.mxfp8_last_error.argtypes = []
         lib.mxfp8_last_error.restype = ctypes.c_char_p

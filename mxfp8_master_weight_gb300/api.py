@@ -222,6 +222,20 @@ def mxfp8_quantize_whole_blocks_batched(jobs, stream=None) -> None:
           _stream(stream, keep[0] if keep else None))
 
 
+def mxfp8_swizzled_scales_size(nrows: int, ncols: int, transpose: bool = False) -> int:
+    """Bytes of the GEMM scale layout of an nrows x ncols E8M0 grid."""
+    return int(_capi.load().mxfp8_swizzled_scales_size(int(nrows), int(ncols), int(bool(transpose))))
+
+
+def mxfp8_swizzle_scales(scale_inv, out, nrows: int, ncols: int, transpose: bool = False,
+                         stream=None) -> None:
+    """E8M0 grid -> the 128x4-tile layout block-scaled GEMMs read (see the C header)."""
+    dev = _device_of(scale_inv, out)
+    args = [handle(scale_inv, "scale_inv"), handle(out, "out")]
+    _call("mxfp8_swizzle_scales", dev, *[ctypes.byref(a) for a in args], int(nrows), int(ncols),
+          int(bool(transpose)), _stream(stream, scale_inv))
+
+
 class Prepared:
     """One library call with its tensor handles marshalled once.
 

@@ -19,6 +19,7 @@ using mxfp8::DeviceInfo;
 using mxfp8::FragGeom;
 using mxfp8::FusedParams;
 using mxfp8::ScaleSegment;
+using mxfp8::SwizzleParams;
 
 thread_local char g_err[512] = {0};
 
@@ -598,6 +599,43 @@ int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_ro
 int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
                                         void* stream) {
   return run_fused(jobs, njobs, stream);
+}
+
+int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose) {
+  if (nrows < 0 || ncols < 0) return -1;
+  const int64_t lr = transpose ? ncols : nrows, lc = transpose ? nrows : ncols;
+  return (lr + 127) / 128 * 128 * ((lc + 3) / 4 * 4);
+}
+
+int mxfp8_swizzle_scales(const mxfp8_tensor* scale_inv, mxfp8_tensor* out, int64_t nrows,
+                         int64_t ncols, int32_t transpose, void* stream) {
+  if (nrows <= 0 || ncols <= 0) return fail(MXFP8_ERR_INVALID, "nrows and ncols must be positive");
+  if (transpose != 0 && transpose != 1) return fail(MXFP8_ERR_INVALID, "transpose must be 0 or 1");
+  if (nrows > (int64_t(1) << 40) || ncols > (int64_t(1) << 40))
+    return fail(MXFP8_ERR_INVALID, "grid too large");
+  if (is_empty(scale_inv)) return fail(MXFP8_ERR_MISSING, "scale_inv is required");
+  if (is_empty(out)) return fail(MXFP8_ERR_MISSING, "out is required");
+  if (int rc = check_grid(scale_inv, "scale_inv", nrows, ncols, MXFP8_DTYPE_U8)) return rc;
+  if (int rc = check_tensor(out, "out")) return rc;
+  if (out->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "out: dtype must be U8");
+  const int64_t need = mxfp8_swizzled_scales_size(nrows, ncols, transpose);
+  if (numel(out) < need)
+    return fail(MXFP8_ERR_SHAPE, "out holds %lld bytes, the layout needs %lld",
+                (long long)numel(out), (long long)need);
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  SwizzleParams p{};
+  p.s = static_cast<const uint8_t*>(scale_inv->data);
+  p.ld = scale_inv->shape[1];
+  p.out = static_cast<uint8_t*>(out->data);
+  p.lr = transpose ? ncols : nrows;
+  p.lc = transpose ? nrows : ncols;
+  p.pr = (p.lr + 127) / 128 * 128;
+  p.pc = (p.lc + 3) / 4 * 4;
+  p.transpose = transpose;
+  p.vec = reinterpret_cast<uintptr_t>(p.out) % 16 == 0;
+  return cuda_status(mxfp8::launch_swizzle_scales(p, dev, static_cast<cudaStream_t>(stream)),
+                     "swizzle scales launch");
 }
 
 }  // extern "C"

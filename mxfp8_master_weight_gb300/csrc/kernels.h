@@ -75,6 +75,17 @@ struct ScaleSegment {
   int32_t vec;  // dense (ld == ncols), 4 | nrows*ncols and aligned: 4 entries per thread
 };
 
+// E8M0 grid -> the 128x4-tile layout block-scaled tensor-core GEMMs read.
+struct SwizzleParams {
+  const uint8_t* s;     // grid [nr][ld]
+  int64_t ld;
+  uint8_t* out;         // PR * PC bytes
+  int64_t lr, lc;       // logical matrix (the grid or its transpose)
+  int64_t pr, pc;       // padded to multiples of 128 rows and 4 columns
+  int32_t transpose;
+  int32_t vec;          // out is 16-byte aligned
+};
+
 struct DeviceInfo {
   int device;
   int sms;
@@ -130,6 +141,8 @@ cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, boo
                                   cudaStream_t stream);
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
+                                  cudaStream_t stream);
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,
                               int dtype, const DeviceInfo& dev, cudaStream_t stream);
 

@@ -7,7 +7,12 @@
 //
 // Packed MAX reduction: the page's single packed-amax MAX all-reduce, with the
 // ranks emulated as S slots of one device buffer: out[k] = max_s |slot_s[k]|.
-// Both kernels are streaming element-wise passes: 16-byte loads, grid-stride
+// GEMM scale layout: the E8M0 grid (or its transpose) padded to 128 x 4 and cut into
+// 128x4 tiles of 512 bytes in row-major tile order; inside a tile element (r, c) sits
+// at (r % 32) * 16 + (r / 32) * 4 + c -- the layout block-scaled tensor-core GEMMs
+// read their scale factors in.  One thread writes one 16-byte line of a tile (rows
+// j, j+32, j+64, j+96 x 4 columns), so a tile leaves as 32 contiguous 16-byte stores.
+// The kernels are streaming element-wise passes: 16-byte loads, grid-stride
 // loops over a grid that is a multiple of the SM count.
 #include "common.cuh"
 
@@ -82,6 +87,38 @@ __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict_
   }
 }
 
+__global__ void __launch_bounds__(kThreads) k_swizzle_scales(const __grid_constant__ SwizzleParams p) {
+  const int64_t tiles_c = p.pc / 4;
+  const int64_t lines = (p.pr / 128) * tiles_c * 32;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  for (int64_t g = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; g < lines; g += stride) {
+    const int64_t tile = g >> 5;
+    const int j = int(g & 31);
+    const int64_t r0 = (tile / tiles_c) * 128 + j, c0 = (tile % tiles_c) * 4;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int64_t r = r0 + 32 * i;
+      uint32_t word = 0;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int64_t c = c0 + cc;
+        uint32_t v = 0;
+        if (r < p.lr && c < p.lc) v = p.transpose ? p.s[c * p.ld + r] : p.s[r * p.ld + c];
+        word |= v << (8 * cc);
+      }
+      w[i] = word;
+    }
+    uint8_t* dst = p.out + tile * 512 + j * 16;
+    if (p.vec) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+#pragma unroll
+      for (int b = 0; b < 16; ++b) dst[b] = static_cast<uint8_t>(w[b >> 2] >> (8 * (b & 3)));
+    }
+  }
+}
+
 unsigned grid_for(int64_t work_items, const DeviceInfo& dev) {
   const int64_t want = (work_items + kThreads - 1) / kThreads;
   const int64_t cap = int64_t(dev.sms) * 8;  // 8 x 256 threads resident per SM
@@ -117,6 +154,14 @@ cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
+                                  cudaStream_t stream) {
+  const int64_t lines = (p.pr / 128) * (p.pc / 4) * 32;
+  if (lines == 0) return cudaSuccess;
+  k_swizzle_scales<<<grid_for(lines, dev), kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,

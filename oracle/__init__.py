@@ -55,6 +55,7 @@ def _load():
             lib.oracle_partial_cast_model.argtypes = [vp, ctypes.c_int, ctypes.c_int, i64, i64, i64, i64,
                                                       vp, i64, vp, i64, vp, vp, i64]
             lib.oracle_f16_bits_array.argtypes = [vp, vp, i64]
+            lib.oracle_swizzle_scales.argtypes = [vp, i64, i64, i64, ctypes.c_int, vp]
             lib.oracle_bf16_rne_bits_array.argtypes = [vp, vp, i64]
             lib.oracle_e4m3_encode_array.argtypes = [vp, vp, i64]
             lib.oracle_e8m0_array.argtypes = [vp, vp, i64]
@@ -186,6 +187,19 @@ def partial_cast(frag: np.ndarray, rows: int, cols: int, start: int,
                                 _ptr(scale_c) if out_c is not None else None,
                                 scale_c.shape[1] if out_c is not None else 0,
                                 _ptr(out_r), _ptr(out_c), out_offset)
+
+
+def swizzled_size(nr: int, nc: int, transpose: bool) -> int:
+    lr, lc = (nc, nr) if transpose else (nr, nc)
+    return ((lr + 127) // 128 * 128) * ((lc + 3) // 4 * 4)
+
+
+def swizzle_scales(S: np.ndarray, nr: int, nc: int, transpose: bool = False) -> np.ndarray:
+    """The E8M0 grid S[:nr, :nc] in the 128x4-tile layout of block-scaled GEMMs."""
+    _c(S)
+    out = np.empty(swizzled_size(nr, nc, transpose), np.uint8)
+    _load().oracle_swizzle_scales(_ptr(S), nr, nc, S.shape[1], int(transpose), _ptr(out))
+    return out
 
 
 # ---------------------------------------------------------------- whole flows

@@ -311,6 +311,31 @@ int oracle_partial_cast(const void *frag, int dtype, int64_t rows, int64_t cols,
                                      scale_r, ld_sr, scale_c, ld_sc, out_r, out_c, out_offset);
 }
 
+/* ---------- scale layout for GEMM consumers ---------------------------------- */
+
+/* Rearrange an E8M0 grid into the layout block-scaled tensor-core GEMMs read.  The
+ * logical matrix L is the grid itself (transpose == 0, L[r][c] = S[r][c], LR = nr,
+ * LC = nc) or its transpose (transpose == 1, L[r][c] = S[c][r], LR = nc, LC = nr).
+ * L is padded with zero bytes to PR = ceil(LR/128)*128 rows and PC = ceil(LC/4)*4
+ * columns and cut into 128x4 tiles stored in row-major tile order, 512 bytes each;
+ * inside a tile, element (r, c) sits at (r % 32) * 16 + (r / 32) * 4 + c. */
+int oracle_swizzle_scales(const uint8_t *S, int64_t nr, int64_t nc, int64_t ld, int transpose,
+                          uint8_t *out) {
+    int64_t LR = transpose ? nc : nr, LC = transpose ? nr : nc;
+    int64_t PR = (LR + 127) / 128 * 128, PC = (LC + 3) / 4 * 4;
+    int64_t tiles_per_row = PC / 4;
+    for (int64_t r = 0; r < PR; ++r) {
+        for (int64_t c = 0; c < PC; ++c) {
+            uint8_t v = 0;
+            if (r < LR && c < LC) v = transpose ? S[c * ld + r] : S[r * ld + c];
+            int64_t tile = (r / 128) * tiles_per_row + c / 4;
+            int64_t rr = r % 128, cc = c % 4;
+            out[tile * 512 + (rr % 32) * 16 + (rr / 32) * 4 + cc] = v;
+        }
+    }
+    return 0;
+}
+
 /* ---------- element-wise batch helpers for the pins -------------------------- */
 
 void oracle_bf16_rne_bits_array(const float *x, uint16_t *out, int64_t n) {

@@ -172,3 +172,16 @@ def test_fused_rejects_fragments_that_cut_blocks(lib):
     # missing columnwise scales for a columnwise output, wrong amax dtype
     assert fused(lib, T(P, F32, 32 * cols), E(), E(), sr, E(), q, q, rows, cols, 0, 0) == 4
     assert fused(lib, T(P, F32, 32 * cols), T(P, BF16, rows, 8), E(), sr, sc, q, q, rows, cols, 0, 0) == 3
+
+
+def test_swizzle_size_and_validation(lib):
+    assert lib.mxfp8_swizzled_scales_size(16384, 192, 0) == 16384 * 192
+    assert lib.mxfp8_swizzled_scales_size(130, 6, 0) == 256 * 8
+    assert lib.mxfp8_swizzled_scales_size(130, 6, 1) == 128 * 132
+    sw = lib.mxfp8_swizzle_scales
+    s = T(P, U8, 130, 6)
+    assert sw(ctypes.byref(s), ctypes.byref(T(P + 8192, U8, 2047)), 130, 6, 0, None) == 2
+    assert sw(ctypes.byref(s), ctypes.byref(T(P + 8192, U8, 2048)), 130, 6, 2, None) == 1
+    assert sw(ctypes.byref(T(P, F32, 130, 6)), ctypes.byref(T(P + 8192, U8, 2048)), 130, 6, 0, None) == 3
+    assert sw(ctypes.byref(s), ctypes.byref(E()), 130, 6, 0, None) == 4
+    assert sw(ctypes.byref(T(P, U8, 129, 6)), ctypes.byref(T(P + 8192, U8, 2048)), 130, 6, 0, None) == 2

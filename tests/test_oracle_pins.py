@@ -413,3 +413,39 @@ def test_cast_with_f16_model(oracle_mod):
     # the amax and scales do not depend on the model dtype
     b = oracle_mod.full_cast(x, rows, cols, True, model="bf16")
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[2], b[2])
+
+
+# ------------------------------------------------------------------ GEMM scale layout
+
+def test_swizzle_hand_points_and_bijection(oracle_mod):
+    # 130 x 6 grid -> padded 256 x 8: two row tiles x two column tiles of 512 bytes
+    nr, nc = 130, 6
+    S = ((np.arange(nr)[:, None] * 7 + np.arange(nc)[None, :] * 3) % 251 + 1).astype(np.uint8)
+    out = oracle_mod.swizzle_scales(S, nr, nc)
+    assert out.size == 256 * 8
+    # hand-derived offsets: tile (r//128, c//4) in row-major tile order (2 tiles per tile row),
+    # inside the tile (r%32)*16 + ((r%128)//32)*4 + c%4
+    assert out[0] == S[0, 0]
+    assert out[1 * 16 + 0 * 4 + 1] == S[1, 1]
+    assert out[0 * 16 + 1 * 4 + 2] == S[32, 2]
+    assert out[31 * 16 + 3 * 4 + 3] == S[127, 3]
+    assert out[1 * 512 + 5 * 16 + 2 * 4 + 1] == S[69, 5]
+    assert out[2 * 512 + 1 * 16 + 0 * 4 + 0] == S[129, 0]
+    # padding is zero and every entry of S appears exactly once
+    assert np.count_nonzero(out) == nr * nc
+    assert sorted(out[out != 0].tolist()) == sorted(S.ravel().tolist())
+
+
+def test_swizzle_matches_reshape_formulation(oracle_mod):
+    """Independent formulation: pad, split into 128x4 tiles, within a tile view rows as
+    (4 groups of 32) and order bytes as (row%32, group, col)."""
+    rng = np.random.default_rng(14)
+    for nr, nc, tr in ((300, 10, False), (64, 512, True), (1, 1, False), (513, 257, True)):
+        S = rng.integers(1, 255, (nr, nc + 3), dtype=np.uint8)  # padded leading dimension
+        L = S[:nr, :nc].T if tr else S[:nr, :nc]
+        pr, pc = -(-L.shape[0] // 128) * 128, -(-L.shape[1] // 4) * 4
+        P = np.zeros((pr, pc), np.uint8)
+        P[:L.shape[0], :L.shape[1]] = L
+        tiles = P.reshape(pr // 128, 128, pc // 4, 4).transpose(0, 2, 1, 3)  # (tr, tc, 128, 4)
+        want = tiles.reshape(pr // 128, pc // 4, 4, 32, 4).transpose(0, 1, 3, 2, 4).ravel()
+        assert np.array_equal(oracle_mod.swizzle_scales(np.ascontiguousarray(S), nr, nc, tr), want)
