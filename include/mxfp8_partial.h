@@ -268,6 +268,18 @@ int mxfp8_swizzle_scales(const mxfp8_tensor* scale_inv, mxfp8_tensor* out, int64
 /* Bytes of the GEMM layout of an nrows x ncols grid (transpose as above). */
 int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose);
 
+/*
+ * Host memory.  Every entry point takes device-accessible pointers.  On this platform
+ * (unified virtual addressing; Grace-Blackwell's coherent CPU-GPU link) page-locked
+ * host memory from cudaHostAlloc / cudaHostRegister is device-accessible through the
+ * same pointer, so the kernels can read master weights from, and write E4M3 data to,
+ * host memory directly.  mxfp8_device_can_access returns 1 when the current device can
+ * dereference [ptr, ptr + bytes) (device, managed, or mapped page-locked host memory)
+ * and 0 otherwise (e.g. pageable host memory); language bindings check host buffers
+ * with it before passing them.  It enqueues nothing.
+ */
+int mxfp8_device_can_access(const void* ptr, int64_t bytes);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 const char* mxfp8_last_error(void);
 

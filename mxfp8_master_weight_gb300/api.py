@@ -25,12 +25,24 @@ if hasattr(torch, "float8_e8m0fnu"):
     _DTYPES[torch.float8_e8m0fnu] = DTYPE_U8
 
 
-def handle(t: torch.Tensor | None, name: str) -> Tensor:
-    """mxfp8_tensor for a CUDA tensor; None / zero-element tensors give an empty handle."""
+def device_can_access(t: torch.Tensor) -> bool:
+    """True when the current CUDA device can dereference the tensor's storage directly
+    (device memory, or page-locked host memory mapped into the device's address space)."""
+    nbytes = t.numel() * t.element_size()
+    return bool(_capi.load().mxfp8_device_can_access(ctypes.c_void_p(t.data_ptr()), nbytes))
+
+
+def handle(t: torch.Tensor | None, name: str, allow_host: bool = False) -> Tensor:
+    """mxfp8_tensor for a CUDA tensor; None / zero-element tensors give an empty handle.
+    With ``allow_host``, a page-locked CPU tensor is accepted when the device can access
+    it directly (checked by the library)."""
     if t is None or t.numel() == 0:
         return _capi.empty_tensor()
     if not t.is_cuda:
-        raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+        if not allow_host:
+            raise ValueError(f"{name}: expected a CUDA tensor, got device {t.device}")
+        if not t.is_pinned() or not device_can_access(t):
+            raise ValueError(f"{name}: host tensor is not page-locked memory the device can access")
     if not t.is_contiguous():
         raise MXFP8Error(5, f"{name}: tensor must be contiguous")
     if t.dtype not in _DTYPES:
@@ -177,25 +189,32 @@ def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
 def mxfp8_quantize_whole_blocks(input, amax_rowwise, amax_colwise, scale_inv_rowwise,
                                 scale_inv_colwise, output_rowwise, output_colwise, rows: int,
                                 cols: int, start_offset: int, out_offset: int | None = None,
-                                stream=None, model_dtype="bf16") -> None:
+                                stream=None, model_dtype="bf16", allow_host=False) -> None:
     """One-pass amax -> scales -> cast of a fragment made of whole blocks (amax outputs
-    optional); bit-identical to the split calls on the same fragment."""
+    optional); bit-identical to the split calls on the same fragment.  With
+    ``allow_host``, any tensor may be page-locked host memory the device can access
+    (zero-copy: the kernel reads and writes host memory over the CPU-GPU link)."""
     if out_offset is None:
         out_offset = start_offset
     if _capi.MODELS[model_dtype] != _capi.MODEL_BF16:
+        if allow_host:
+            raise ValueError("host buffers are supported with the BF16 model dtype only")
         mxfp8_quantize_whole_blocks_batched(
             [(input, amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
               output_rowwise, output_colwise, rows, cols, start_offset, out_offset, model_dtype)],
             stream=stream)
         return
-    dev = _device_of(input, output_rowwise, output_colwise)
     names = ("input", "amax_rowwise", "amax_colwise", "scale_inv_rowwise", "scale_inv_colwise",
              "output_rowwise", "output_colwise")
     ts = (input, amax_rowwise, amax_colwise, scale_inv_rowwise, scale_inv_colwise,
           output_rowwise, output_colwise)
-    args = [handle(t, n) for t, n in zip(ts, names)]
+    dev = _device_of(*ts)
+    if dev is None and allow_host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    args = [handle(t, n, allow_host) for t, n in zip(ts, names)]
     _call("mxfp8_quantize_whole_blocks", dev, *[ctypes.byref(a) for a in args], int(rows),
-          int(cols), int(start_offset), int(out_offset), _stream(stream, input))
+          int(cols), int(start_offset), int(out_offset),
+          _stream(stream, input if input.is_cuda else None))
 
 
 def _quantize_jobs(jobs):

@@ -601,6 +601,28 @@ int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t 
   return run_fused(jobs, njobs, stream);
 }
 
+int mxfp8_device_can_access(const void* ptr, int64_t bytes) {
+  if (ptr == nullptr || bytes < 0) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const char* first = static_cast<const char*>(ptr);
+  const char* last = first + (bytes > 0 ? bytes - 1 : 0);
+  for (const char* q : {first, last}) {
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+      cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+      return 0;
+    }
+    if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+      if (a.type == cudaMemoryTypeDevice && a.device != dev) return 0;
+      continue;
+    }
+    if (a.type == cudaMemoryTypeHost && a.devicePointer == static_cast<const void*>(q)) continue;
+    return 0;
+  }
+  return 1;
+}
+
 int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose) {
   if (nrows < 0 || ncols < 0) return -1;
   const int64_t lr = transpose ? ncols : nrows, lc = transpose ? nrows : ncols;
