@@ -280,6 +280,43 @@ int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpo
  */
 int mxfp8_device_can_access(const void* ptr, int64_t bytes);
 
+/*
+ * Sharded update of one weight without any device allocation.  The source pages have
+ * no counterpart of this entry point.
+ *
+ * It is for callers that cannot allocate device memory at the moment they need the
+ * update -- a memory-pool allocator running its own maintenance, a framework that has
+ * reserved all device memory up front, or code where a cudaMalloc would synchronise
+ * the device.  The update needs working memory for one amax slot per fragment and for
+ * the reduced amax; here that memory is one file-scope device array of 64 MiB, which
+ * every GPU that loads this library holds until the process exits.
+ *
+ * fragments[f]      [in]  fragment f of the rows x cols weight (F32 or BF16, one dtype
+ *                         for all; empty fragments are skipped), starting at flat
+ *                         element start_offsets[f].  Fragments must not overlap.
+ * scale_inv_rowwise [out] REQUIRED U8 [>= rows][>= ceil(cols/32)].
+ * scale_inv_colwise [out] U8 [>= ceil(rows/32)][>= cols]; required iff output_colwise.
+ * output_rowwise    [out] REQUIRED U8, full size (rows*cols), written where the
+ *                         fragments are.
+ * output_colwise    [out] OPTIONAL U8 full size; empty => row-only.
+ * Results equal mxfp8_partial_amax of every fragment into its own zeroed slot,
+ * mxfp8_amax_max_reduce over the slots, mxfp8_update_scales and mxfp8_partial_cast of
+ * every fragment (it runs exactly those entry points), with BF16 as the model dtype.
+ * Limits: 1..64 fragments and (nfrags + 1) amax slots of rows*ceil(cols/32) (+
+ * ceil(rows/32)*cols when columnwise) entries, each rounded up to 256 bytes, within
+ * the 64 MiB; a larger request fails with status 2 and a message giving the bytes
+ * needed.  The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  Every call uses
+ * the same array and leaves its contents behind (slots are cleared at the start of
+ * each call); calls that overlap on the GPU -- on different streams or from
+ * different threads -- race on it.
+ */
+int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments, const int64_t* start_offsets,
+                                 int32_t nfrags, mxfp8_tensor* scale_inv_rowwise,
+                                 mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
+                                 mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
+                                 void* stream);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 const char* mxfp8_last_error(void);
 

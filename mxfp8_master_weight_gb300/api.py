@@ -255,6 +255,29 @@ def mxfp8_swizzle_scales(scale_inv, out, nrows: int, ncols: int, transpose: bool
           int(bool(transpose)), _stream(stream, scale_inv))
 
 
+def mxfp8_sharded_update_noalloc(fragments, start_offsets, scale_inv_rowwise, scale_inv_colwise,
+                                 output_rowwise, output_colwise, rows: int, cols: int,
+                                 stream=None) -> None:
+    """Sharded update of one weight (amax of every fragment, MAX reduction, scales, casts)
+    for callers that cannot allocate device memory: the library keeps the amax working
+    memory in a fixed 64 MiB device array of its own (limits and sharing rules in the C
+    header).  ``fragments``: one tensor per shard; ``start_offsets``: their flat starts."""
+    lib = _capi.load()
+    fn = lib.mxfp8_sharded_update_noalloc
+    T = ctypes.POINTER(Tensor)
+    fn.argtypes = [T, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32, T, T, T, T,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    n = len(fragments)
+    frs = (Tensor * max(1, n))(*[handle(f, "fragment") for f in fragments])
+    starts = (ctypes.c_int64 * max(1, n))(*[int(s) for s in start_offsets])
+    outs = [handle(scale_inv_rowwise, "scale_inv_rowwise"), handle(scale_inv_colwise, "scale_inv_colwise"),
+            handle(output_rowwise, "output_rowwise"), handle(output_colwise, "output_colwise")]
+    dev = _device_of(*fragments, scale_inv_rowwise, output_rowwise)
+    _call("mxfp8_sharded_update_noalloc", dev, frs, starts, n, *[ctypes.byref(o) for o in outs],
+          int(rows), int(cols), _stream(stream, output_rowwise))
+
+
 class Prepared:
     """One library call with its tensor handles marshalled once.
 

@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libmxfp8_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-UNITS = ["capi.cu", "amax.cu", "cast.cu", "fused.cu", "misc.cu"]
+UNITS = ["capi.cu", "amax.cu", "cast.cu", "fused.cu", "misc.cu", "noalloc.cu"]
 
 
 def _nvcc() -> str:

@@ -514,6 +514,10 @@ const mxfp8_tensor& or_empty(const mxfp8_tensor* t) { return t ? *t : kEmpty; }
 
 }  // namespace
 
+namespace mxfp8 {
+int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+}  // namespace mxfp8
+
 extern "C" {
 
 const char* mxfp8_last_error(void) { return g_err; }

@@ -146,6 +146,10 @@ cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,
                               int dtype, const DeviceInfo& dev, cudaStream_t stream);
 
+// Record `msg` as the calling thread's last error (returned by mxfp8_last_error) and
+// return `code`.  For entry points defined outside capi.cu.
+int report_error(int code, const char* msg);
+
 // Tile width (columns per warp tile) for a dtype.
 inline int tile_width_for(int dtype) { return dtype == 0 ? 128 : 256; }
 
