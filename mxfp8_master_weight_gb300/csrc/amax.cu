@@ -114,7 +114,7 @@ __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0,
   }
 }
 
-template <class T, bool kCol, bool kShift, int N>
+template <class T, int kDirs, bool kShift, int N>
 __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
   constexpr int TW = tile_width<T>();
@@ -125,21 +125,30 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
     int64_t row0, col0;
     const AmaxParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
+    const bool col = kDirs == kMixed ? p.amax_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
-      amax_tile_fast<T, kCol, kShift>(p, row0, col0, lane);
+      if (col) {
+        if constexpr (kDirs != kRowOnly) amax_tile_fast<T, true, kShift>(p, row0, col0, lane);
+      } else {
+        if constexpr (kDirs != kBidir) amax_tile_fast<T, false, kShift>(p, row0, col0, lane);
+      }
     } else if (kind == kTileMasked) {
-      amax_tile_masked<T, kCol>(p, row0, col0, lane);
+      if (col) {
+        if constexpr (kDirs != kRowOnly) amax_tile_masked<T, true>(p, row0, col0, lane);
+      } else {
+        if constexpr (kDirs != kBidir) amax_tile_masked<T, false>(p, row0, col0, lane);
+      }
     }
   }
 }
 
-template <class T, bool kCol, bool kShift, int N>
+template <class T, int kDirs, bool kShift, int N>
 cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_partial_amax<T, kCol, kShift, N>, kThreads, 0);
+        &occ, k_partial_amax<T, kDirs, kShift, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
@@ -148,16 +157,27 @@ cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaS
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  k_partial_amax<T, kCol, kShift, N><<<grid, kThreads, 0, stream>>>(b);
+  k_partial_amax<T, kDirs, kShift, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
-template <class T, bool kCol, bool kShift>
+// One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's
+// direction set; single jobs use the one-entry job table.
+template <class T, bool kShift>
 cudaError_t launch(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  if (n == 1) return launch_n<T, kCol, kShift, 1>(jobs, 1, dev, stream);
+  auto colwise = [](const AmaxParams& p) { return p.amax_c != nullptr; };
+  if (n == 1) {
+    return colwise(jobs[0]) ? launch_n<T, kBidir, kShift, 1>(jobs, 1, dev, stream)
+                            : launch_n<T, kRowOnly, kShift, 1>(jobs, 1, dev, stream);
+  }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
     const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
-    const cudaError_t e = launch_n<T, kCol, kShift, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    cudaError_t e;
+    switch (batch_dirs(jobs + k, m, colwise)) {
+      case kRowOnly: e = launch_n<T, kRowOnly, kShift, kMaxBatchJobs>(jobs + k, m, dev, stream); break;
+      case kBidir: e = launch_n<T, kBidir, kShift, kMaxBatchJobs>(jobs + k, m, dev, stream); break;
+      default: e = launch_n<T, kMixed, kShift, kMaxBatchJobs>(jobs + k, m, dev, stream); break;
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -165,19 +185,13 @@ cudaError_t launch(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStr
 
 }  // namespace
 
-cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool colwise,
-                                bool shifted, const DeviceInfo& dev, cudaStream_t stream) {
+cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool shifted,
+                                const DeviceInfo& dev, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   if (dtype == 0) {
-    if (colwise) return shifted ? launch<F32T, true, true>(jobs, n, dev, stream)
-                                : launch<F32T, true, false>(jobs, n, dev, stream);
-    return shifted ? launch<F32T, false, true>(jobs, n, dev, stream)
-                   : launch<F32T, false, false>(jobs, n, dev, stream);
+    return shifted ? launch<F32T, true>(jobs, n, dev, stream) : launch<F32T, false>(jobs, n, dev, stream);
   }
-  if (colwise) return shifted ? launch<BF16T, true, true>(jobs, n, dev, stream)
-                              : launch<BF16T, true, false>(jobs, n, dev, stream);
-  return shifted ? launch<BF16T, false, true>(jobs, n, dev, stream)
-                 : launch<BF16T, false, false>(jobs, n, dev, stream);
+  return shifted ? launch<BF16T, true>(jobs, n, dev, stream) : launch<BF16T, false>(jobs, n, dev, stream);
 }
 
 }  // namespace mxfp8

@@ -346,7 +346,7 @@ int prep_scales(const mxfp8_scale_job& job, ScaleSegment* segs, int* nseg, int* 
 // Prefix the last error message with the failing job's index.
 int job_fail(int rc, int k) {
   char tmp[sizeof g_err];
-  std::snprintf(tmp, sizeof tmp, "job %d: %s", k, g_err);
+  std::snprintf(tmp, sizeof tmp, "job %d: %.480s", k, g_err);
   std::snprintf(g_err, sizeof g_err, "%s", tmp);
   return rc;
 }
@@ -378,15 +378,15 @@ int run_amax(const mxfp8_amax_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_amax(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : dt * 4 + col * 2 + (win[i].g.shift != 0);
+      key[i] = skip ? -1 : dt * 2 + (win[i].g.shift != 0);
     }
-    for (int kk = 0; kk < 8; ++kk) {  // dtype x colwise x shifted
+    for (int kk = 0; kk < 4; ++kk) {  // dtype x shifted (direction sets may mix)
       int n = 0;
       for (int i = 0; i <= m; ++i) {
         if (i < m && key[i] == kk) batch[n++] = win[i];
         if (n > 0 && (n == kGroupChunk || i == m)) {
-          if (int rc = cuda_status(mxfp8::launch_partial_amax(batch, n, kk >> 2, (kk >> 1) & 1, kk & 1,
-                                                              dev, static_cast<cudaStream_t>(stream)),
+          if (int rc = cuda_status(mxfp8::launch_partial_amax(batch, n, kk >> 1, kk & 1, dev,
+                                                              static_cast<cudaStream_t>(stream)),
                                    "partial amax launch"))
             return rc;
           n = 0;
@@ -416,16 +416,16 @@ int run_cast(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_cast(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : jobs[base + i].model_dtype * 16 + dt * 8 + col * 4 +
-                               (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+      key[i] = skip ? -1 : jobs[base + i].model_dtype * 8 + dt * 4 + (win[i].g.shift != 0) * 2 +
+                               (win[i].vec_out != 0);
     }
-    for (int kk = 0; kk < 32; ++kk) {  // model x dtype x colwise x shifted x aligned output
+    for (int kk = 0; kk < 16; ++kk) {  // model x dtype x shifted x aligned output
       int n = 0;
       for (int i = 0; i <= m; ++i) {
         if (i < m && key[i] == kk) batch[n++] = win[i];
         if (n > 0 && (n == kGroupChunk || i == m)) {
-          if (int rc = cuda_status(mxfp8::launch_partial_cast(batch, n, (kk >> 3) & 1, (kk >> 2) & 1,
-                                                              (kk >> 1) & 1, kk & 1, kk >> 4, dev,
+          if (int rc = cuda_status(mxfp8::launch_partial_cast(batch, n, (kk >> 2) & 1, (kk >> 1) & 1,
+                                                              kk & 1, kk >> 3, dev,
                                                               static_cast<cudaStream_t>(stream)),
                                    "partial cast launch"))
             return rc;
@@ -487,16 +487,16 @@ int run_fused(const mxfp8_quantize_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_fused(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : jobs[base + i].model_dtype * 16 + dt * 8 + col * 4 +
-                               (win[i].g.shift != 0) * 2 + (win[i].vec_out != 0);
+      key[i] = skip ? -1 : jobs[base + i].model_dtype * 8 + dt * 4 + (win[i].g.shift != 0) * 2 +
+                               (win[i].vec_out != 0);
     }
-    for (int kk = 0; kk < 32; ++kk) {
+    for (int kk = 0; kk < 16; ++kk) {  // model x dtype x shifted x aligned output
       int n = 0;
       for (int i = 0; i <= m; ++i) {
         if (i < m && key[i] == kk) batch[n++] = win[i];
         if (n > 0 && (n == kGroupChunk || i == m)) {
-          if (int rc = cuda_status(mxfp8::launch_fused_quantize(batch, n, (kk >> 3) & 1, (kk >> 2) & 1,
-                                                                (kk >> 1) & 1, kk & 1, kk >> 4, dev,
+          if (int rc = cuda_status(mxfp8::launch_fused_quantize(batch, n, (kk >> 2) & 1, (kk >> 1) & 1,
+                                                                kk & 1, kk >> 3, dev,
                                                                 static_cast<cudaStream_t>(stream)),
                                    "fused quantize launch"))
             return rc;

@@ -13,6 +13,8 @@
 // L2 evict_last policy and pass 2 loads evict_first, so the second read is served
 // from L2 and HBM sees the input once: 4 + 2 bytes per FP32 element (bidirectional)
 // instead of 4 + 4 + 2 for the split amax and cast kernels.
+#pragma once
+
 #include <atomic>
 
 #include "common.cuh"
@@ -219,7 +221,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
   __syncwarp();
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const __grid_constant__ JobBatch<FusedParams, N> b) {
   __shared__ RowScales rsc;
@@ -232,21 +234,30 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     int64_t row0, col0;
     const FusedParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
+    const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
-      fused_tile_fast<T, kCol, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      if (col) {
+        if constexpr (kDirs != kRowOnly) fused_tile_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      } else {
+        if constexpr (kDirs != kBidir) fused_tile_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      }
     } else if (kind == kTileMasked) {
-      fused_tile_masked<T, kCol, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      if (col) {
+        if constexpr (kDirs != kRowOnly) fused_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      } else {
+        if constexpr (kDirs != kBidir) fused_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      }
     }
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int kModel, int N>
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_fused_quantize<T, kCol, kShift, kVec, kModel, N>, kThreads, 0);
+        &occ, k_fused_quantize<T, kDirs, kShift, kVec, kModel, N>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
@@ -255,56 +266,60 @@ cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cuda
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  k_fused_quantize<T, kCol, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
+  k_fused_quantize<T, kDirs, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+// One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's
+// direction set; single BF16-model jobs use the one-entry job table.
+template <class T, bool kShift, bool kVec, int kModel>
 cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  // single-job kernels only for the BF16 model dtype (the common case); FP16-model
-  // jobs always go through the batch kernel
+  auto colwise = [](const FusedParams& p) { return p.out_c != nullptr; };
   if constexpr (kModel == kModelBF16) {
-    if (n == 1) return launch_n<T, kCol, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+    if (n == 1) {
+      return colwise(jobs[0]) ? launch_n<T, kBidir, kShift, kVec, kModel, 1>(jobs, 1, dev, stream)
+                              : launch_n<T, kRowOnly, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+    }
   }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
     const int m = n - k < kMaxBatchJobs ? n - k : kMaxBatchJobs;
-    const cudaError_t e = launch_n<T, kCol, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+    cudaError_t e;
+    switch (batch_dirs(jobs + k, m, colwise)) {
+      case kRowOnly:
+        e = launch_n<T, kRowOnly, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        break;
+      case kBidir:
+        e = launch_n<T, kBidir, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        break;
+      default:
+        e = launch_n<T, kMixed, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        break;
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
-template <class T, bool kCol, int kModel>
+template <class T, int kModel>
 cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool vec_out,
                            const DeviceInfo& dev, cudaStream_t stream) {
   if (shifted) {
-    return vec_out ? launch<T, kCol, true, true, kModel>(jobs, n, dev, stream)
-                   : launch<T, kCol, true, false, kModel>(jobs, n, dev, stream);
+    return vec_out ? launch<T, true, true, kModel>(jobs, n, dev, stream)
+                   : launch<T, true, false, kModel>(jobs, n, dev, stream);
   }
-  return vec_out ? launch<T, kCol, false, true, kModel>(jobs, n, dev, stream)
-                 : launch<T, kCol, false, false, kModel>(jobs, n, dev, stream);
+  return vec_out ? launch<T, false, true, kModel>(jobs, n, dev, stream)
+                 : launch<T, false, false, kModel>(jobs, n, dev, stream);
+}
+
+// All launches for one input dtype T (instantiated by that dtype's translation unit).
+template <class T>
+cudaError_t launch_for_dtype(const FusedParams* jobs, int n, bool shifted, bool vec_out, int model,
+                             const DeviceInfo& dev, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  if (model == kModelF16) return launch_variant<T, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
+  return launch_variant<T, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
 }
 
 }  // namespace
-
-cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
-                                  bool shifted, bool vec_out, int model, const DeviceInfo& dev,
-                                  cudaStream_t stream) {
-  if (n <= 0) return cudaSuccess;
-  if (model == kModelF16) {
-    if (dtype == 0) {
-      return colwise ? launch_variant<F32T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
-                     : launch_variant<F32T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
-    }
-    return colwise ? launch_variant<BF16T, true, kModelF16>(jobs, n, shifted, vec_out, dev, stream)
-                   : launch_variant<BF16T, false, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
-  }
-  if (dtype == 0) {
-    return colwise ? launch_variant<F32T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
-                   : launch_variant<F32T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
-  }
-  return colwise ? launch_variant<BF16T, true, kModelBF16>(jobs, n, shifted, vec_out, dev, stream)
-                 : launch_variant<BF16T, false, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
-}
 
 }  // namespace mxfp8

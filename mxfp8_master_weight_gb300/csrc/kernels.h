@@ -91,6 +91,11 @@ struct DeviceInfo {
   int sms;
 };
 
+// Direction sets a kernel instantiation handles: only rowwise, rowwise + columnwise,
+// or a mix (each job's columnwise pointer picks, per tile, one of the two
+// compile-time specialisations, so the inner loops stay specialised).
+enum Dirs { kRowOnly = 0, kBidir = 1, kMixed = 2 };
+
 // A batch of fragments launched as one kernel: the warp tiles of every job's first
 // and last 32-row bands (the only bands a fragment boundary can cut) come first,
 // numbered by prefix_a, then every job's interior bands, numbered by prefix_b.
@@ -127,18 +132,38 @@ inline int64_t fill_batch(JobBatch<P, N>& b, const P* jobs, int n) {
 }
 
 // dtype: 0 = FP32, 1 = BF16.  Each launcher takes n validated jobs that share the
-// dtype and the template choices (columnwise present, virtual base shifted, output
-// word-aligned), launches them in batches of at most kMaxBatchJobs, and returns the
+// dtype and the template choices (virtual base shifted, output word-aligned, model
+// dtype), launches them in batches of at most kMaxBatchJobs -- each batch with the
+// kernel for its direction set (row-only, bidirectional or mixed) -- and returns the
 // CUDA launch status.
-cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool colwise,
-                                bool shifted, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_amax(const AmaxParams* jobs, int n, int dtype, bool shifted,
+                                const DeviceInfo& dev, cudaStream_t stream);
 // model: 0 = round through BF16, 1 = round through FP16.
-cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool colwise,
-                                bool shifted, bool vec_out, int model, const DeviceInfo& dev,
+cudaError_t launch_partial_cast(const CastParams* jobs, int n, int dtype, bool shifted,
+                                bool vec_out, int model, const DeviceInfo& dev,
                                 cudaStream_t stream);
-cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool colwise,
-                                  bool shifted, bool vec_out, int model, const DeviceInfo& dev,
+cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, bool shifted,
+                                  bool vec_out, int model, const DeviceInfo& dev,
                                   cudaStream_t stream);
+
+// Per-input-dtype halves of the two launchers above (separate translation units).
+cudaError_t launch_partial_cast_f32(const CastParams* jobs, int n, bool shifted, bool vec_out,
+                                    int model, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast_bf16(const CastParams* jobs, int n, bool shifted, bool vec_out,
+                                     int model, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_fused_quantize_f32(const FusedParams* jobs, int n, bool shifted, bool vec_out,
+                                      int model, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_fused_quantize_bf16(const FusedParams* jobs, int n, bool shifted,
+                                       bool vec_out, int model, const DeviceInfo& dev,
+                                       cudaStream_t stream);
+
+// Direction set of a batch of jobs (colwise(job) tells whether a job has one).
+template <class P, class F>
+inline int batch_dirs(const P* jobs, int n, F colwise) {
+  int col = 0;
+  for (int k = 0; k < n; ++k) col += colwise(jobs[k]) ? 1 : 0;
+  return col == 0 ? kRowOnly : (col == n ? kBidir : kMixed);
+}
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,

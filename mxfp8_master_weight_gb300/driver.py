@@ -106,9 +106,9 @@ class PackedLayout:
 
 def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
-    entries launch once per group of at most 16 jobs sharing dtype, direction set and
-    alignment class (fragment virtual base on a 16-byte boundary; for the cast also
-    the outputs' virtual base on a V-byte boundary)."""
+    entries launch once per group of at most 16 jobs sharing dtype and alignment class
+    (fragment virtual base on a 16-byte boundary; for the cast also the outputs'
+    virtual base on a V-byte boundary); row-only and bidirectional jobs share launches."""
     def groups(keys, cap):
         counts = {}
         for k in keys:
@@ -118,12 +118,12 @@ def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs) -> int:
     def vbase(t, start):
         return t.data_ptr() - start * t.element_size()
 
-    akeys = [(a[0].dtype, a[2] is not None, vbase(a[0], a[5]) % 16 != 0) for a in amax_jobs]
+    akeys = [(a[0].dtype, vbase(a[0], a[5]) % 16 != 0) for a in amax_jobs]
     ckeys = []
     for frag, sr, sc, qr, qc, rows, cols, start in cast_jobs:
         v = 16 // frag.element_size()
         vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
-        ckeys.append((frag.dtype, qc is not None, vbase(frag, start) % 16 != 0, vec))
+        ckeys.append((frag.dtype, vbase(frag, start) % 16 != 0, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
     return groups(akeys, 16) + 1 + (n_grids + 31) // 32 + groups(ckeys, 16)
 
