@@ -41,6 +41,13 @@
 
 #include <stdint.h>
 
+/* Every entry point below is exported; everything else in the library is hidden. */
+#if defined(__GNUC__)
+#define MXFP8_API __attribute__((visibility("default")))
+#else
+#define MXFP8_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -92,7 +99,7 @@ enum {
  * 3 if an amax dtype differs from the input dtype or the input is not F32/BF16;
  * 4 if amax_rowwise is empty (and len > 0).
  */
-int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+MXFP8_API int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
                        mxfp8_tensor* amax_colwise, int64_t rows, int64_t cols,
                        int64_t start_offset, void* stream);
 
@@ -106,7 +113,7 @@ int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
  * out[k] = max over s of |slots[s][k]|; NaN propagates.  S == 1 copies |.|.
  * out may not overlap slots.  Errors: 2 numel mismatch, 3 dtype, 4 empty out.
  */
-int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* stream);
+MXFP8_API int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* stream);
 
 /*
  * Scale update (page "Support row-only MXFP8 distributed master-weight casts",
@@ -121,7 +128,7 @@ int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* st
  * Writes the E8M0 byte of every entry of the compact block grid
  * (rows x ceil(cols/32) and ceil(rows/32) x cols); padding is left untouched.
  */
-int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
+MXFP8_API int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
                         mxfp8_tensor* scale_inv_rowwise, mxfp8_tensor* scale_inv_colwise,
                         int64_t rows, int64_t cols, void* stream);
 
@@ -148,7 +155,7 @@ int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* am
  * Errors: 1 bad offsets/sizes; 2 output or scale too small; 3 dtype;
  * 4 rowwise scale/output missing, or columnwise output without columnwise scales.
  */
-int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_rowwise,
+MXFP8_API int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_inv_rowwise,
                        const mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
                        mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                        int64_t start_offset, int64_t out_offset, void* stream);
@@ -198,9 +205,28 @@ typedef struct {
   int64_t rows, cols;
 } mxfp8_scale_job;
 
-int mxfp8_partial_amax_batched(const mxfp8_amax_job* jobs, int32_t njobs, void* stream);
-int mxfp8_update_scales_batched(const mxfp8_scale_job* jobs, int32_t njobs, void* stream);
-int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream);
+MXFP8_API int mxfp8_partial_amax_batched(const mxfp8_amax_job* jobs, int32_t njobs, void* stream);
+MXFP8_API int mxfp8_update_scales_batched(const mxfp8_scale_job* jobs, int32_t njobs, void* stream);
+
+/*
+ * Packed MAX reduction fused with the scale update (the reduction of
+ * mxfp8_amax_max_reduce and the scale update of mxfp8_update_scales_batched in one
+ * pass over the packed buffer, for the slots of ranks emulated on one GPU).
+ *
+ * slots   [in]  2-D [S][P] F32 or BF16 packed amax buffers.
+ * reduced [out] P entries, same dtype.
+ * jobs    [in]  njobs scale jobs (see mxfp8_scale_job) whose amax grids are views
+ *               INTO `reduced`; entry (r, c) of such a view at reduced offset o is
+ *               reduced[o] = max_s |slots[s][o]|, and its E8M0 byte goes to the job's
+ *               scale grid.  Entries of `reduced` outside every view are not written.
+ * Results equal mxfp8_amax_max_reduce followed by mxfp8_update_scales_batched.
+ * Errors: as those two; 1 if a view does not lie inside `reduced`.
+ */
+MXFP8_API int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor* reduced,
+                                        const mxfp8_scale_job* jobs, int32_t njobs,
+                                        void* stream);
+
+MXFP8_API int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream);
 
 /*
  * One-pass quantisation of a fragment made of WHOLE blocks.  When every row block
@@ -225,7 +251,7 @@ int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* 
  * cols are multiples of 32, and with a columnwise output start_offset and
  * start_offset + len are multiples of 32*cols (the end may also be rows*cols).
  */
-int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+MXFP8_API int mxfp8_quantize_whole_blocks(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
                                 mxfp8_tensor* amax_colwise, mxfp8_tensor* scale_inv_rowwise,
                                 mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
                                 mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
@@ -245,7 +271,7 @@ typedef struct {
 
 /* Batched form of mxfp8_quantize_whole_blocks, with the conventions of the other
  * batched entry points. */
-int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
+MXFP8_API int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t njobs,
                                         void* stream);
 
 /*
@@ -262,11 +288,11 @@ int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t 
  * out       [out] U8, numel >= mxfp8_swizzled_scales_size(nrows, ncols, transpose).
  * Errors: 1 bad sizes or transpose flag, 2 out too small, 3 dtype, 4 missing tensor.
  */
-int mxfp8_swizzle_scales(const mxfp8_tensor* scale_inv, mxfp8_tensor* out, int64_t nrows,
+MXFP8_API int mxfp8_swizzle_scales(const mxfp8_tensor* scale_inv, mxfp8_tensor* out, int64_t nrows,
                          int64_t ncols, int32_t transpose, void* stream);
 
 /* Bytes of the GEMM layout of an nrows x ncols grid (transpose as above). */
-int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose);
+MXFP8_API int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpose);
 
 /*
  * Host memory.  Every entry point takes device-accessible pointers.  On this platform
@@ -278,7 +304,7 @@ int64_t mxfp8_swizzled_scales_size(int64_t nrows, int64_t ncols, int32_t transpo
  * and 0 otherwise (e.g. pageable host memory); language bindings check host buffers
  * with it before passing them.  It enqueues nothing.
  */
-int mxfp8_device_can_access(const void* ptr, int64_t bytes);
+MXFP8_API int mxfp8_device_can_access(const void* ptr, int64_t bytes);
 
 /*
  * Sharded update of one weight without any device allocation.  The source pages have
@@ -311,17 +337,17 @@ int mxfp8_device_can_access(const void* ptr, int64_t bytes);
  * each call); calls that overlap on the GPU -- on different streams or from
  * different threads -- race on it.
  */
-int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments, const int64_t* start_offsets,
+MXFP8_API int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments, const int64_t* start_offsets,
                                  int32_t nfrags, mxfp8_tensor* scale_inv_rowwise,
                                  mxfp8_tensor* scale_inv_colwise, mxfp8_tensor* output_rowwise,
                                  mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                                  void* stream);
 
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
-const char* mxfp8_last_error(void);
+MXFP8_API const char* mxfp8_last_error(void);
 
 /* Library version as major*10000 + minor*100 + patch. */
-int mxfp8_version(void);
+MXFP8_API int mxfp8_version(void);
 
 #ifdef __cplusplus
 }

@@ -178,6 +178,16 @@ def mxfp8_update_scales_batched(jobs, stream=None) -> None:
           _stream(stream, keep[0] if keep else None))
 
 
+def mxfp8_amax_max_reduce_update_scales(slots, reduced, jobs, stream=None) -> None:
+    """One pass: reduced = max over the slots of the packed amax, and the E8M0 scales of
+    every job, whose amax grids are views into ``reduced``.  ``jobs`` as for
+    mxfp8_update_scales_batched."""
+    arr, keep = _scale_jobs(jobs)
+    hs = [handle(slots, "slots"), handle(reduced, "reduced")]
+    _call("mxfp8_amax_max_reduce_update_scales", _device_of(slots, reduced),
+          ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs), _stream(stream, reduced))
+
+
 def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
     """``jobs``: sequence of (input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
     output_colwise, rows, cols, start_offset[, out_offset])."""
@@ -346,6 +356,15 @@ def prepare_partial_amax_batched(jobs) -> Prepared:
 def prepare_update_scales_batched(jobs) -> Prepared:
     arr, keep = _scale_jobs(jobs)
     return Prepared("mxfp8_update_scales_batched", [arr], (len(jobs),), keep, job_array=arr)
+
+
+def prepare_amax_max_reduce_update_scales(slots, reduced, jobs) -> Prepared:
+    arr, keep = _scale_jobs(jobs)
+    hs = [handle(slots, "slots"), handle(reduced, "reduced")]
+    pr = Prepared("mxfp8_amax_max_reduce_update_scales", hs, (), keep + [slots, reduced])
+    pr.args = (ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs))
+    pr.handles = hs + [arr]
+    return pr
 
 
 def prepare_partial_cast_batched(jobs) -> Prepared:

@@ -50,7 +50,7 @@ def source_digest() -> str:
 
 
 def cflags(extra=()):
-    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
+    return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                    f"-I{INCLUDE}", f"-I{CSRC}", *extra]
 
 

@@ -18,6 +18,7 @@ using mxfp8::CastParams;
 using mxfp8::DeviceInfo;
 using mxfp8::FragGeom;
 using mxfp8::FusedParams;
+using mxfp8::ReduceScaleSegment;
 using mxfp8::ScaleSegment;
 using mxfp8::SwizzleParams;
 
@@ -559,6 +560,81 @@ int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* st
                                               dt == MXFP8_DTYPE_F32 ? 0 : 1, dev,
                                               static_cast<cudaStream_t>(stream)),
                      "max reduce launch");
+}
+
+int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor* reduced,
+                                        const mxfp8_scale_job* jobs, int32_t njobs,
+                                        void* stream) {
+  if (is_empty(reduced)) return fail(MXFP8_ERR_MISSING, "reduced is required");
+  if (int rc = check_tensor(reduced, "reduced")) return rc;
+  if (is_empty(slots)) return fail(MXFP8_ERR_MISSING, "slots is required");
+  if (int rc = check_tensor(slots, "slots")) return rc;
+  if (slots->ndim != 2) return fail(MXFP8_ERR_SHAPE, "slots must be 2-D [S][P]");
+  const int32_t dt = slots->dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "slots: dtype must be F32 or BF16");
+  if (reduced->dtype != dt) return fail(MXFP8_ERR_DTYPE, "reduced: dtype must equal the slots dtype");
+  const int64_t S = slots->shape[0], P = slots->shape[1];
+  if (numel(reduced) != P)
+    return fail(MXFP8_ERR_SHAPE, "reduced numel %lld != slot size %lld", (long long)numel(reduced), (long long)P);
+  if (S > 1024) return fail(MXFP8_ERR_INVALID, "too many slots");
+  const int64_t eb = elem_bytes(dt);
+  const uintptr_t s0 = reinterpret_cast<uintptr_t>(slots->data), r0 = reinterpret_cast<uintptr_t>(reduced->data);
+  if (r0 < s0 + uintptr_t(S * P * eb) && s0 < r0 + uintptr_t(P * eb))
+    return fail(MXFP8_ERR_INVALID, "reduced overlaps slots");
+  if (njobs < 0 || (njobs > 0 && jobs == nullptr)) return fail(MXFP8_ERR_INVALID, "bad job array");
+  ScaleSegment segs[2];
+  int nseg, jdt;
+  // validate every job and that each amax view lies inside `reduced`
+  auto inside = [&](const ScaleSegment& g, int64_t* begin) {
+    const intptr_t d = reinterpret_cast<intptr_t>(g.amax) - intptr_t(r0);
+    if (d < 0 || d % eb != 0) return false;
+    *begin = d / eb;
+    return *begin + (g.nrows - 1) * g.ld_a + g.ncols <= P;
+  };
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_scales(jobs[k], segs, &nseg, &jdt)) return njobs > 1 ? job_fail(rc, k) : rc;
+    if (jdt != (dt == MXFP8_DTYPE_F32 ? 0 : 1)) return job_fail(fail(MXFP8_ERR_DTYPE, "amax dtype differs from the slots"), k);
+    for (int q = 0; q < nseg; ++q) {
+      int64_t b;
+      if (!inside(segs[q], &b)) return job_fail(fail(MXFP8_ERR_INVALID, "amax view is not inside `reduced`"), k);
+    }
+  }
+  if (njobs == 0) return ok();
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  ReduceScaleSegment batch[64];
+  int n = 0;
+  for (int k = 0; k <= njobs; ++k) {
+    if (k < njobs) {
+      prep_scales(jobs[k], segs, &nseg, &jdt);
+      for (int q = 0; q < nseg; ++q) {
+        int64_t b;
+        inside(segs[q], &b);
+        ReduceScaleSegment& r = batch[n++];
+        r = ReduceScaleSegment{};
+        r.slot0 = static_cast<const char*>(slots->data) + b * eb;
+        r.slot_stride = P;
+        r.nslots = int32_t(S);
+        r.reduced = const_cast<void*>(segs[q].amax);
+        r.scale = segs[q].scale;
+        r.nrows = segs[q].nrows;
+        r.ncols = segs[q].ncols;
+        r.ld_a = segs[q].ld_a;
+        r.ld_s = segs[q].ld_s;
+        r.vec = segs[q].vec && (P % 4 == 0) &&
+                (reinterpret_cast<uintptr_t>(r.slot0) % uintptr_t(4 * eb) == 0);
+      }
+    }
+    if (n > 0 && (n > 62 || k == njobs)) {
+      if (int rc = cuda_status(mxfp8::launch_reduce_update_scales(batch, n, dt == MXFP8_DTYPE_F32 ? 0 : 1,
+                                                                  dev, static_cast<cudaStream_t>(stream)),
+                               "reduce and update scales launch"))
+        return rc;
+      n = 0;
+    }
+  }
+  return ok();
 }
 
 int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,

@@ -86,6 +86,18 @@ struct SwizzleParams {
   int32_t vec;          // out is 16-byte aligned
 };
 
+// Fused MAX reduction + scale update of one block grid that is a view into the packed
+// reduced buffer: reduced[r][c] = max_s |slot_s[r][c]|, scale[r][c] = E8M0(reduced).
+struct ReduceScaleSegment {
+  const void* slot0;     // the grid's first entry inside slot 0 of the packed slots
+  int64_t slot_stride;   // entries between consecutive slots
+  int32_t nslots;
+  int32_t vec;           // dense grid, 4 | entries, 16-byte (F32) / 8-byte (BF16) aligned
+  void* reduced;         // the grid's view inside the reduced buffer [nrows][ld_a]
+  uint8_t* scale;        // [nrows][ld_s]
+  int64_t nrows, ncols, ld_a, ld_s;
+};
+
 struct DeviceInfo {
   int device;
   int sms;
@@ -166,6 +178,8 @@ inline int batch_dirs(const P* jobs, int n, F colwise) {
 }
 cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
                                  const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg, int dtype,
+                                       const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
                                   cudaStream_t stream);
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,

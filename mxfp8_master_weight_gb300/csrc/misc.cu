@@ -59,6 +59,59 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
   }
 }
 
+// Fused packed MAX reduction + scale update (blockIdx.y selects the grid).
+struct ReduceScaleBatch {
+  int32_t nseg;
+  ReduceScaleSegment seg[kMaxSegments];
+};
+
+template <class T>
+__global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
+    const __grid_constant__ ReduceScaleBatch b) {
+  const ReduceScaleSegment& s = b.seg[blockIdx.y];
+  const int64_t n = s.nrows * s.ncols;
+  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+  constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
+  if (s.vec) {
+    const char* src = static_cast<const char*>(s.slot0);
+    const int64_t slot_bytes = s.slot_stride * T::kBytes;
+    for (int64_t q = tid; q < n / 4; q += stride) {
+      uint32_t m[4] = {0u, 0u, 0u, 0u};
+      for (int k = 0; k < s.nslots; ++k) {
+        const char* p = src + k * slot_bytes + q * 4 * T::kBytes;
+        if constexpr (T::kBytes == 4) {
+          const uint4 a = *reinterpret_cast<const uint4*>(p);
+          m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], a.y & kAbs);
+          m[2] = max(m[2], a.z & kAbs); m[3] = max(m[3], a.w & kAbs);
+        } else {
+          const uint2 a = *reinterpret_cast<const uint2*>(p);
+          m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], (a.x >> 16) & kAbs);
+          m[2] = max(m[2], a.y & kAbs); m[3] = max(m[3], (a.y >> 16) & kAbs);
+        }
+      }
+      if constexpr (T::kBytes == 4) {
+        reinterpret_cast<uint4*>(s.reduced)[q] = make_uint4(m[0], m[1], m[2], m[3]);
+      } else {
+        reinterpret_cast<uint2*>(s.reduced)[q] = make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
+      }
+      uint32_t out = 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[k]) << (8 * k);
+      reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+    }
+  } else {
+    for (int64_t e = tid; e < n; e += stride) {
+      const int64_t r = e / s.ncols, c = e % s.ncols;
+      const int64_t idx = r * s.ld_a + c;
+      uint32_t m = 0;
+      for (int k = 0; k < s.nslots; ++k) m = max(m, load_bits<T>(s.slot0, k * s.slot_stride + idx) & kAbs);
+      store_bits<T>(s.reduced, idx, m);
+      s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(m));
+    }
+  }
+}
+
 template <class T>
 __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict__ slots,
                                                          void* __restrict__ out, int64_t elems,
@@ -149,6 +202,34 @@ cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
       k_update_scales<F32T><<<grid, kThreads, 0, stream>>>(b);
     } else {
       k_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(b);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg, int dtype,
+                                       const DeviceInfo& dev, cudaStream_t stream) {
+  for (int k0 = 0; k0 < nseg; k0 += kMaxSegments) {
+    ReduceScaleBatch b;
+    b.nseg = nseg - k0 < kMaxSegments ? nseg - k0 : kMaxSegments;
+    int64_t work = 0;
+    for (int k = 0; k < b.nseg; ++k) {
+      b.seg[k] = segs[k0 + k];
+      const int64_t n = b.seg[k].nrows * b.seg[k].ncols;
+      const int64_t items = b.seg[k].vec ? n / 4 : n;
+      work = items > work ? items : work;
+    }
+    if (work == 0) continue;
+    const int64_t per_seg = (int64_t(dev.sms) * 8 + b.nseg - 1) / b.nseg;
+    const int64_t want = (work + kThreads - 1) / kThreads;
+    const unsigned gx = unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg));
+    const dim3 grid(gx, unsigned(b.nseg));
+    if (dtype == 0) {
+      k_reduce_update_scales<F32T><<<grid, kThreads, 0, stream>>>(b);
+    } else {
+      k_reduce_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(b);
     }
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;

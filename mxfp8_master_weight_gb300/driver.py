@@ -104,7 +104,7 @@ class PackedLayout:
         return vr, vc
 
 
-def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs) -> int:
+def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs, fused_reduce=False) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
     entries launch once per group of at most 16 jobs sharing dtype and alignment class
     (fragment virtual base on a 16-byte boundary; for the cast also the outputs'
@@ -125,7 +125,8 @@ def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs) -> int:
         vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
         ckeys.append((frag.dtype, vbase(frag, start) % 16 != 0, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
-    return groups(akeys, 16) + 1 + (n_grids + 31) // 32 + groups(ckeys, 16)
+    reduce_and_scales = (n_grids + 31) // 32 if fused_reduce else 1 + (n_grids + 31) // 32
+    return groups(akeys, 16) + reduce_and_scales + groups(ckeys, 16)
 
 
 def _round_up(x: int, a: int) -> int:
@@ -141,12 +142,15 @@ class ShardedCast:
     always, columnwise only for bidirectional weights).
     """
 
-    def __init__(self, specs, bounds, device, dtype=torch.float32):
+    def __init__(self, specs, bounds, device, dtype=torch.float32, fuse_reduce_scales=True):
         self.specs = [s if isinstance(s, WeightSpec) else WeightSpec(*s) for s in specs]
         self.bounds = list(bounds)
         self.plan = plan_fragments(self.specs, self.bounds)
         self.layout = PackedLayout(self.specs)
         self.dtype = dtype
+        # the emulated all-reduce and the scale update in one pass over the packed buffer
+        # (mxfp8_amax_max_reduce_update_scales) or as two calls
+        self.fuse_reduce_scales = fuse_reduce_scales
         S = len(self.bounds) - 1
         self.slots = torch.zeros((S, self.layout.total), dtype=dtype, device=device)
         self.reduced = torch.zeros(self.layout.total, dtype=dtype, device=device)
@@ -208,10 +212,15 @@ class ShardedCast:
         # one batched call per phase: every fragment of every shard (each shard writes
         # its own slot, so no two jobs write the same amax entry), one reduction, every
         # weight's scales, every fragment's cast
-        self._launches = _count_launches(amax_jobs, cast_jobs, len(scale_jobs), self.specs)
+        self._launches = _count_launches(amax_jobs, cast_jobs, len(scale_jobs), self.specs,
+                                         self.fuse_reduce_scales)
         amax = [api.prepare_partial_amax_batched(amax_jobs)]
-        reduce = [api.prepare_amax_max_reduce(self.slots, self.reduced)]
-        scales = [api.prepare_update_scales_batched(scale_jobs)]
+        if self.fuse_reduce_scales:
+            reduce = [api.prepare_amax_max_reduce_update_scales(self.slots, self.reduced, scale_jobs)]
+            scales = []
+        else:
+            reduce = [api.prepare_amax_max_reduce(self.slots, self.reduced)]
+            scales = [api.prepare_update_scales_batched(scale_jobs)]
         casts = [api.prepare_partial_cast_batched(cast_jobs)]
         self._cache_key, self._cache = key, (amax, reduce, scales, casts)
         return self._cache
@@ -220,7 +229,8 @@ class ShardedCast:
         """One distributed update: partial amax -> one packed MAX reduce -> scales -> casts.
 
         ``events``: optional five CUDA events recorded on the stream before the amax
-        phase and after the amax, reduce, scale and cast phases (for timing).
+        phase and after the amax, reduce, scale and cast phases (for timing; with the
+        fused reduction + scale update the scale phase is empty).
         """
         phases = self._prepared(shards)
         with torch.cuda.device(self.slots.device):

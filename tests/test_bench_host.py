@@ -16,6 +16,7 @@ def test_algorithmic_bytes_per_element():
     assert b["amax"] / n == pytest.approx(4.25)        # read 4 B, write 2 x 4 B / 32
     assert b["cast"] / n == pytest.approx(6.0625)      # read 4 B + 2 scale B / 32, write 2 B
     assert b["amax"] == 427_819_008 and b["cast"] == 610_271_232
+    assert b["reduce_scales"] == b["reduce"] + n // 16
     ro = bench.algorithmic_bytes(n, colwise=False)
     assert ro["cast"] / n == pytest.approx(4 + 1 / 32 + 1)
 

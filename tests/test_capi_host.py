@@ -25,7 +25,8 @@ def _declared_symbols():
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
         text = open(h).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names.update(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(mxfp8_\w+)\s*\(", text, flags=re.M))
+        names.update(re.findall(r"^\s*(?:MXFP8_API\s+)?(?:const\s+)?\w+\s*\*?\s*(mxfp8_\w+)\s*\(",
+                                text, flags=re.M))
     return sorted(names)
 
 
@@ -37,9 +38,20 @@ def test_header_declares_entry_points():
 
 
 def test_every_declared_symbol_is_exported(lib):
-    for n in _declared_symbols():
+    names = _declared_symbols()
+    assert len(names) >= 16
+    for n in names:
         assert hasattr(lib, n), n
     assert lib.mxfp8_version() >= 100
+
+
+def test_only_the_c_abi_is_exported():
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _capi.LIB_PATH], capture_output=True, text=True)
+    if out.returncode != 0:
+        pytest.skip("nm not available")
+    text_syms = [l.split()[-1] for l in out.stdout.splitlines() if " T " in l]
+    assert set(text_syms) == set(_declared_symbols())
 
 
 def T(ptr, dtype, *shape):

@@ -90,3 +90,44 @@ def test_bf16_batch_with_empty_and_single_element_shards():
     sc, shards = _run(batch, torch.bfloat16)
     sc.step(shards)
     _check_against_full(batch, sc)
+
+
+@pytest.mark.parametrize("fuse", [False, True])
+def test_cfg5_small_both_reduction_paths(fuse):
+    batch = wl.cfg5_sharded_batch(seed=3, scale=8)
+    specs = [driver.WeightSpec(w.rows, w.cols, w.colwise) for w in batch.weights]
+    sc = driver.ShardedCast(specs, batch.bounds, "cuda", fuse_reduce_scales=fuse)
+    shards = [to_device(np.ascontiguousarray(batch.shard(s))) for s in range(sc.num_shards)]
+    sc.step(shards)
+    _check_against_full(batch, sc)
+
+
+def test_fused_reduce_scales_entry_with_padded_views():
+    from mxfp8_master_weight_gb300 import _capi, api
+    rng = np.random.default_rng(7)
+    S, rows, cols = 3, 96, 200
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    # packed buffer with padded leading dimensions: rowwise [96][9], colwise [3][203]
+    P = rr * 9 + 64 + cr * 203
+    slots_h = np.abs(wl.normal_f32(rng, (S, P)))
+    slots = torch.from_numpy(slots_h).cuda()
+    reduced = torch.zeros(P, device="cuda")
+    vr = reduced[:rr * 9].view(rr, 9)
+    vc = reduced[rr * 9 + 64:].view(cr, 203)
+    sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda")
+    api.mxfp8_amax_max_reduce_update_scales(slots, reduced, [(vr, vc, sr, sc, rows, cols)])
+    torch.cuda.synchronize()
+    want = oracle.max_reduce(slots_h)
+    got = to_host(reduced)
+    wr = want[:rr * 9].reshape(rr, 9)[:, :rc]
+    wc = want[rr * 9 + 64:].reshape(cr, 203)[:, :cc]
+    assert np.array_equal(got[:rr * 9].reshape(rr, 9)[:, :rc], wr)
+    assert np.array_equal(got[rr * 9 + 64:].reshape(cr, 203)[:, :cc], wc)
+    assert np.all(got[rr * 9:rr * 9 + 64] == 0)  # entries outside every view untouched
+    assert np.array_equal(to_host(sr), oracle.e8m0_from_amax(wr.astype(np.float64)))
+    assert np.array_equal(to_host(sc), oracle.e8m0_from_amax(wc.astype(np.float64)))
+    outside = torch.zeros((rr, rc), device="cuda")  # not a view into `reduced`
+    with pytest.raises(_capi.MXFP8Error) as e:
+        api.mxfp8_amax_max_reduce_update_scales(slots, reduced, [(outside, None, sr, None, rows, cols)])
+    assert e.value.status == 1
