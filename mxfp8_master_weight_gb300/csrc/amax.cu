@@ -12,10 +12,9 @@
 // tile: the column maxima stay in the lane's registers, the row-block maximum is
 // a butterfly over the G lanes of the block.  Tiles fully inside the fragment take
 // 16-byte loads with no per-element tests; tiles cut by the fragment boundary or
-// the matrix edge take per-element predicated loads.  The grid is persistent
-// (a multiple of the SM count) and walks tiles in band-major order.
-#include <atomic>
-
+// the matrix edge take per-element predicated loads.  The grid has one tile per
+// warp (the block scheduler balances uneven tiles); tiles are numbered band-major,
+// boundary bands first.
 #include "common.cuh"
 
 namespace mxfp8 {
@@ -26,7 +25,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
 constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
-constexpr int kMaxDevices = 64;
 #ifndef MXFP8_MIN_BLOCKS
 #define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
 #endif
@@ -144,19 +142,11 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
 
 template <class T, int kDirs, bool kShift, int N>
 cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  static std::atomic<int> occupancy[kMaxDevices];
-  int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
-  if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_partial_amax<T, kDirs, kShift, N>, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
-  }
+  (void)dev;
   JobBatch<AmaxParams, N> b;
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
-  const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
+  const unsigned grid = tile_grid(total, kWarps);
   k_partial_amax<T, kDirs, kShift, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }

@@ -15,8 +15,6 @@
 // lane's V columns are loaded once per tile; the rowwise multiplier once per row.
 #pragma once
 
-#include <atomic>
-
 #include "common.cuh"
 
 namespace mxfp8 {
@@ -27,7 +25,6 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
 constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
-constexpr int kMaxDevices = 64;
 #ifndef MXFP8_MIN_BLOCKS
 #define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
 #endif
@@ -184,19 +181,11 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  static std::atomic<int> occupancy[kMaxDevices];
-  int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
-  if (occ == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_partial_cast<T, kDirs, kShift, kVec, kModel, N>, kThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) occ = 1;
-    if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
-  }
+  (void)dev;
   JobBatch<CastParams, N> b;
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
-  const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
+  const unsigned grid = tile_grid(total, kWarps);
   k_partial_cast<T, kDirs, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
   return cudaGetLastError();
 }

@@ -460,4 +460,13 @@ inline unsigned balanced_grid(int64_t ntiles, int warps, int64_t max_blocks) {
   return unsigned(blocks < max_blocks ? blocks : max_blocks);
 }
 
+// Blocks for one tile per warp: the hardware block scheduler then hands out tiles
+// dynamically, which absorbs uneven per-tile cost (tiles cut by a fragment boundary,
+// row-only next to bidirectional jobs in one batch) better than a static persistent
+// assignment.  The kernels' grid-stride loop covers anything beyond the 2^31-1 cap.
+inline unsigned tile_grid(int64_t ntiles, int warps) {
+  const int64_t blocks = (ntiles + warps - 1) / warps;
+  return unsigned(blocks < 1 ? 1 : (blocks < 2147483647 ? blocks : 2147483647));
+}
+
 }  // namespace mxfp8
