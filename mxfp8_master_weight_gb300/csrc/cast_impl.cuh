@@ -1,12 +1,14 @@
-// Partial cast kernel: master values of a contiguous fragment -> BF16 (model
-// dtype, nearest-even) -> E4M3 (nearest-even, saturating at 448), scaled by the
-// E8M0 block scales, written in place into the rowwise and (optionally)
-// columnwise outputs.
+// Partial cast kernel templates: master values of a contiguous fragment -> model
+// dtype (BF16, or FP16; nearest-even) -> E4M3 (nearest-even, saturating at 448),
+// scaled by the E8M0 block scales, written in place into the rowwise and
+// (optionally) columnwise outputs.  cast_f32.cu and cast_bf16.cu instantiate them
+// for FP32 and BF16 master values.
 //
 // Follows "Support row-only MXFP8 distributed master-weight casts" (sections
 // "Changes" and the flow diagram): rounding goes through the model dtype, the
 // rowwise output is always written, and the columnwise output -- with every read
-// of its scales -- is removed at compile time when the weight has none.
+// of its scales -- is removed at compile time when the weight has none (a batch
+// mixing row-only and bidirectional weights picks the specialisation per tile).
 //
 // Work unit and tile classes as in the amax kernel: one warp per 32 x (32*V)
 // tile, one 16-byte input chunk per lane per row; a row's V output bytes per

@@ -1,11 +1,12 @@
-// Device helpers shared by the partial-amax, scale and cast kernels (sm_103a).
+// Device helpers shared by the partial-amax, scale, cast and one-pass kernels
+// (sm_103a).
 //
 // Everything here is bit-level: |x| and block maxima are taken on the raw bit
 // patterns with the sign cleared (for non-negative IEEE values unsigned integer
 // order equals numeric order, and NaN patterns sort above +Inf, so a NaN member
-// propagates); the E8M0 exponent is read from the exponent field; the two
-// roundings of the cast are the documented PTX conversions cvt.rn.bf16x2.f32
-// and cvt.rn.satfinite.e4m3x2.f32.
+// propagates); the E8M0 exponent is read from the exponent field; the roundings of
+// the cast are the documented PTX conversions cvt.rn.bf16x2.f32 (or cvt.rn.f16x2.f32
+// for an FP16 model dtype) and cvt.rn.satfinite.e4m3x2.f32.
 #pragma once
 
 #include <cstdint>
@@ -270,8 +271,9 @@ __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint2& q) {
 
 // ---------------------------------------------------------------- fragment geometry
 // The fragment is every element from (rs, cs) to (re, ce) in row-major order, so row
-// i holds fragment columns [row_lo(i), row_hi(i)] (empty when i is outside
-// [rs, re]) and column c holds fragment rows [col_lo(c), col_hi(c)].
+// i holds fragment columns [row_lo(i), row_hi(i)] (none when i is outside [rs, re])
+// and column c holds the fragment rows from rs (rs + 1 when c < cs) to re (re - 1
+// when c > ce).
 __device__ __forceinline__ int64_t row_lo(const FragGeom& g, int64_t i) {
   return i == g.rs ? g.cs : 0;
 }

@@ -62,3 +62,13 @@ def test_aggregate_over_two_gloo_ranks():
 
 def test_single_rank_aggregation_is_identity():
     assert bench.aggregate_over_ranks(0.5, 7.0, 1) == (0.5, 7.0)
+
+
+def test_sharded_step_bytes():
+    from mxfp8_master_weight_gb300 import driver
+    specs = [driver.WeightSpec(64, 64, True), driver.WeightSpec(32, 64, False)]
+    b = bench.sharded_step_bytes(specs, num_slots=2, packed_entries=1000)
+    n0, n1 = 64 * 64, 32 * 64
+    amax = n0 * 4 + 2 * n0 // 32 * 4 + n1 * 4 + n1 // 32 * 4
+    cast = n0 * 4 + 2 * n0 // 32 + 2 * n0 + n1 * 4 + n1 // 32 + n1
+    assert b == amax + cast + 2 * 1000 * 4 + 1000 * 4 + 1000
