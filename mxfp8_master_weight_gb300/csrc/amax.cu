@@ -23,7 +23,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
-constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
+constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 #ifndef MXFP8_MIN_BLOCKS
 #define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
@@ -52,8 +52,8 @@ __device__ __forceinline__ void store_colmax(const AmaxParams& p, int64_t row0, 
 }
 
 // Whole tile inside the fragment: 16-byte loads (realigned when the fragment's
-// virtual base is not 16-byte aligned), no per-element tests.
-template <class T, bool kCol, bool kShift>
+// virtual base sits kS bytes past a 16-byte boundary), no per-element tests.
+template <class T, bool kCol, int kS>
 __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -62,13 +62,12 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const bool writer = (lane % T::G) == 0;
   const int64_t out_r = row0 * p.ld_r + (j >> 5);
-  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
-  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
+  constexpr int NB = kS ? kShiftBatch : kRowBatch;
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
   for (int rb = 0; rb < 32; rb += NB) {
     uint4 v[NB];
-    load_rows<NB>(v, src + rb * row_bytes, row_bytes, lane, shift);
+    load_rows<NB, kS>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);
@@ -76,6 +75,17 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
     }
   }
   if constexpr (kCol) store_colmax<T, kCol>(p, row0, j, colmax);
+}
+
+// A fast tile of a launch whose fragments are all aligned (kShift false) or all
+// shifted (kShift true: the fragment's own offset picks the specialisation).
+template <class T, bool kCol, bool kShift>
+__device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int64_t col0, int lane) {
+  if constexpr (kShift) {
+    with_shift<T>(p.g.shift, [&](auto s) { amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane); });
+  } else {
+    amax_tile_fast<T, kCol, 0>(p, row0, col0, lane);
+  }
 }
 
 // Tile cut by the fragment boundary or the matrix edge: per-element predicated
@@ -126,9 +136,9 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
     const bool col = kDirs == kMixed ? p.amax_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) amax_tile_fast<T, true, kShift>(p, row0, col0, lane);
+        if constexpr (kDirs != kRowOnly) amax_fast<T, true, kShift>(p, row0, col0, lane);
       } else {
-        if constexpr (kDirs != kBidir) amax_tile_fast<T, false, kShift>(p, row0, col0, lane);
+        if constexpr (kDirs != kBidir) amax_fast<T, false, kShift>(p, row0, col0, lane);
       }
     } else if (kind == kTileMasked) {
       if (col) {

@@ -25,7 +25,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
-constexpr int kShiftBatch = 4;   // the realigning path holds two chunks per row
+constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 #ifndef MXFP8_MIN_BLOCKS
 #define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
@@ -57,7 +57,7 @@ __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t
 
 // Whole tile inside the fragment: 16-byte loads (realigned for a shifted virtual
 // base), one scale byte per row, word stores when the outputs are aligned.
-template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+template <class T, bool kCol, int kS, bool kVec, int kModel>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -66,8 +66,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const uint8_t* srow = p.s_r + row0 * p.ld_sr + (j >> 5);
   const int64_t o0 = row0 * cols + j + p.out_shift;
-  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
-  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
+  constexpr int NB = kS ? kShiftBatch : kRowBatch;
   float mc[T::V];
   if constexpr (kCol) colwise_multipliers<T>(p, row0, j, mc);
 #pragma unroll 1
@@ -76,7 +75,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
     uint32_t sb[NB];
 #pragma unroll
     for (int r = 0; r < NB; ++r) sb[r] = srow[(rb + r) * p.ld_sr];
-    load_rows<NB>(v, src + rb * row_bytes, row_bytes, lane, shift);
+    load_rows<NB, kS>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float y[T::V];
@@ -89,6 +88,18 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
       store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
       if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
     }
+  }
+}
+
+// A fast tile of a launch whose fragments are all aligned or all shifted.
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+__device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int64_t col0, int lane) {
+  if constexpr (kShift) {
+    with_shift<T>(p.g.shift, [&](auto s) {
+      cast_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane);
+    });
+  } else {
+    cast_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane);
   }
 }
 
@@ -167,9 +178,9 @@ __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) cast_tile_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kRowOnly) cast_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane);
       } else {
-        if constexpr (kDirs != kBidir) cast_tile_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kBidir) cast_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane);
       }
     } else if (kind == kTileMasked) {
       if (col) {

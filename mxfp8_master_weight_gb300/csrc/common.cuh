@@ -320,33 +320,6 @@ __device__ __forceinline__ int classify_tile(const FragGeom& g, int64_t row0, in
 }
 
 // ---------------------------------------------------------------- row loads
-// Chunks of NB consecutive rows of a fast tile for this lane: chunk r holds the V
-// elements (row0 + r, col0 + V*lane ...).  `src` is the lane's element address in
-// the first row.  shift == 0: one aligned 16-byte load per row.  shift != 0 (the
-// fragment's virtual base is not 16-byte aligned): each lane loads the aligned chunk
-// that holds its first element, takes the rest from the next lane's chunk (lane 31
-// loads one extra chunk), and a funnel shift realigns the bytes.  All lanes of the
-// warp must be active.
-__device__ __forceinline__ uint32_t pick4(uint32_t q, uint32_t a, uint32_t b, uint32_t c,
-                                          uint32_t d) {
-  return q == 0 ? a : (q == 1 ? b : (q == 2 ? c : d));
-}
-
-__device__ __forceinline__ uint4 realign(const uint4& A, const uint4& B, uint32_t shift) {
-  const uint32_t q = shift >> 2, r = (shift & 3u) * 8u;
-  const uint32_t w0 = pick4(q, A.x, A.y, A.z, A.w);
-  const uint32_t w1 = pick4(q, A.y, A.z, A.w, B.x);
-  const uint32_t w2 = pick4(q, A.z, A.w, B.x, B.y);
-  const uint32_t w3 = pick4(q, A.w, B.x, B.y, B.z);
-  const uint32_t w4 = pick4(q, B.x, B.y, B.z, B.w);
-  uint4 o;
-  o.x = __funnelshift_r(w0, w1, r);
-  o.y = __funnelshift_r(w1, w2, r);
-  o.z = __funnelshift_r(w2, w3, r);
-  o.w = __funnelshift_r(w3, w4, r);
-  return o;
-}
-
 template <bool kHint>
 __device__ __forceinline__ uint4 ld_chunk(const void* p, uint64_t pol) {
   if constexpr (kHint) {
@@ -356,29 +329,102 @@ __device__ __forceinline__ uint4 ld_chunk(const void* p, uint64_t pol) {
   }
 }
 
-template <int NB, bool kHint = false>
+// The first NW words of the 16-byte aligned chunk at p (the rest read as 0), with one
+// load of 4, 8 or 16 bytes.
+template <int NW, bool kHint>
+__device__ __forceinline__ uint4 ld_head(const void* p, uint64_t pol) {
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if constexpr (NW >= 3) {
+    v = ld_chunk<kHint>(p, pol);
+  } else if constexpr (NW == 2) {
+    if constexpr (kHint) {
+      asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                   : "=r"(v.x), "=r"(v.y) : "l"(p), "l"(pol));
+    } else {
+      asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+    }
+  } else {
+    if constexpr (kHint) {
+      asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.u32 %0, [%1], %2;"
+                   : "=r"(v.x) : "l"(p), "l"(pol));
+    } else {
+      asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v.x) : "l"(p));
+    }
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4& c, int k) {
+  return k == 0 ? c.x : (k == 1 ? c.y : (k == 2 ? c.z : c.w));
+}
+
+// Chunks of NB consecutive rows of a fast tile for this lane: chunk r holds the V
+// elements (row0 + r, col0 + V*lane ...).  `src` is the lane's element address in
+// the first row.  kS is the byte offset of the fragment's virtual base from a
+// 16-byte boundary (a multiple of the element size).  kS == 0: one aligned 16-byte
+// load per row.  kS != 0: each lane loads the aligned chunk that holds its first
+// element and takes the words past it from the next lane's chunk -- only the
+// ceil(kS/4) words it needs, one shuffle each (lane 31 loads them from the chunk
+// after the tile row) -- and a half-word funnel shift finishes a 2-byte offset.
+// All lanes of the warp must be active.
+template <int NB, int kS, bool kHint = false>
 __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64_t row_bytes,
-                                          int lane, uint32_t shift, uint64_t pol = 0) {
-  if (shift == 0) {
+                                          int lane, uint64_t pol = 0) {
+  if constexpr (kS == 0) {
 #pragma unroll
     for (int r = 0; r < NB; ++r) v[r] = ld_chunk<kHint>(src + r * row_bytes, pol);
   } else {
-    const char* a = src - shift;
+    static_assert(kS > 0 && kS < 16, "shift is a byte offset inside a 16-byte chunk");
+    constexpr int Q = kS / 4;            // whole words of the own chunk to skip
+    constexpr int R = (kS % 4) * 8;      // bits to skip inside the next word (0 or 16)
+    constexpr int NW = Q + (R != 0);     // words taken from the next lane's chunk
+    const char* a = src - kS;
     uint4 extra[NB];
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       v[r] = ld_chunk<kHint>(a + r * row_bytes, pol);
-      extra[r] = lane == 31 ? ld_chunk<kHint>(a + r * row_bytes + 16, pol) : make_uint4(0u, 0u, 0u, 0u);
+      extra[r] = lane == 31 ? ld_head<NW, kHint>(a + r * row_bytes + 16, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
-      uint4 b;
-      b.x = __shfl_down_sync(kFullMask, v[r].x, 1);
-      b.y = __shfl_down_sync(kFullMask, v[r].y, 1);
-      b.z = __shfl_down_sync(kFullMask, v[r].z, 1);
-      b.w = __shfl_down_sync(kFullMask, v[r].w, 1);
-      if (lane == 31) b = extra[r];
-      v[r] = realign(v[r], b, shift);
+      uint32_t w[8] = {v[r].x, v[r].y, v[r].z, v[r].w, 0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int k = 0; k < NW; ++k) {
+        const uint32_t nx = __shfl_down_sync(kFullMask, w[k], 1);
+        w[4 + k] = lane == 31 ? word_of(extra[r], k) : nx;
+      }
+      uint32_t o[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) o[k] = R ? __funnelshift_r(w[Q + k], w[Q + k + 1], R) : w[Q + k];
+      v[r] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+// Calls f(ShiftC<S>{}) with S the compile-time copy of `shift`, a non-zero byte
+// offset from a 16-byte boundary that is a multiple of T's element size: each offset
+// gets its own specialisation of the realigning loads.
+template <int S>
+struct ShiftC {
+  static constexpr int value = S;
+};
+template <class T, class F>
+__device__ __forceinline__ void with_shift(int32_t shift, F&& f) {
+  if constexpr (T::kBytes == 4) {
+    switch (shift) {
+      case 4: f(ShiftC<4>{}); break;
+      case 8: f(ShiftC<8>{}); break;
+      default: f(ShiftC<12>{}); break;
+    }
+  } else {
+    switch (shift) {
+      case 2: f(ShiftC<2>{}); break;
+      case 4: f(ShiftC<4>{}); break;
+      case 6: f(ShiftC<6>{}); break;
+      case 8: f(ShiftC<8>{}); break;
+      case 10: f(ShiftC<10>{}); break;
+      case 12: f(ShiftC<12>{}); break;
+      default: f(ShiftC<14>{}); break;
     }
   }
 }

@@ -76,15 +76,14 @@ __device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t ro
   }
 }
 
-template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+template <class T, bool kCol, int kS, bool kVec, int kModel>
 __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t row0, int64_t col0,
                                                 int lane, RowScales& rsc, int warp) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
   const int64_t row_bytes = cols * T::kBytes;
-  const uint32_t shift = kShift ? static_cast<uint32_t>(p.g.shift) : 0u;
-  constexpr int NB = kShift ? kShiftBatch : kRowBatch;
+  constexpr int NB = kS ? kShiftBatch : kRowBatch;
   const int grp = lane / T::G;
   const bool writer = (lane % T::G) == 0;
   const int64_t blk = j >> 5;
@@ -95,7 +94,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 #pragma unroll 1
   for (int rb = 0; rb < 32; rb += NB) {
     uint4 v[NB];
-    load_rows<NB, true>(v, src + rb * row_bytes, row_bytes, lane, shift, keep);
+    load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, keep);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const uint4 a = chunk_abs<T>(v[r]);
@@ -119,7 +118,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 #pragma unroll 1
   for (int rb = 0; rb < 32; rb += NB) {
     uint4 v[NB];
-    load_rows<NB, true>(v, src + rb * row_bytes, row_bytes, lane, shift, drop);
+    load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, drop);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float y[T::V];
@@ -134,6 +133,19 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
     }
   }
   __syncwarp();
+}
+
+// A fast tile of a launch whose fragments are all aligned or all shifted.
+template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+__device__ __forceinline__ void fused_fast(const FusedParams& p, int64_t row0, int64_t col0, int lane,
+                                           RowScales& rsc, int warp) {
+  if constexpr (kShift) {
+    with_shift<T>(p.g.shift, [&](auto s) {
+      fused_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+    });
+  } else {
+    fused_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+  }
 }
 
 // Tile cut by the fragment boundary or the matrix edge.  Every block the fragment
@@ -237,9 +249,9 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) fused_tile_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+        if constexpr (kDirs != kRowOnly) fused_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       } else {
-        if constexpr (kDirs != kBidir) fused_tile_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+        if constexpr (kDirs != kBidir) fused_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       }
     } else if (kind == kTileMasked) {
       if (col) {

@@ -83,6 +83,23 @@ def test_fused_full_weights(cfg):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_fused_every_misalignment(dtype):
+    """A whole weight in a buffer that starts at every element offset inside a 16-byte
+    chunk, so each offset's specialisation of the realigning loads runs on interior
+    tiles, for both direction sets."""
+    rows, cols = 96, 1024
+    rng = np.random.default_rng(78)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(4.0) ** rng.integers(-6, 6, rows * cols).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    for shift in range(4 if dtype == "f32" else 8):
+        for colwise in (True, False):
+            got = _fused(x, rows, cols, 0, colwise, shift=shift)
+            want = oracle.full_cast(x, rows, cols, colwise)
+            assert_bitwise(got, want, f"fused {dtype} shift {shift} colwise {colwise}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("rows,cols", [(33, 65), (100, 70), (64, 4096 + 40), (97, 256), (1, 1)])
 def test_fused_ragged_full_weights(dtype, rows, cols):
     rng = np.random.default_rng(rows + 1000 * cols)
