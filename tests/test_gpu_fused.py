@@ -92,11 +92,17 @@ def test_fused_every_misalignment(dtype):
     x = wl.normal_f32(rng, rows * cols) * np.float32(4.0) ** rng.integers(-6, 6, rows * cols).astype(np.float32)
     if dtype == "bf16":
         x = wl.truncate_to_bf16_bits(x)
-    for shift in range(4 if dtype == "f32" else 8):
+    per_word = 4 if dtype == "f32" else 8
+    for shift in range(per_word):
         for colwise in (True, False):
             got = _fused(x, rows, cols, 0, colwise, shift=shift)
             want = oracle.full_cast(x, rows, cols, colwise)
             assert_bitwise(got, want, f"fused {dtype} shift {shift} colwise {colwise}")
+            # fragment-sized outputs at every byte offset inside an output word
+            out_offset = (5 * shift + 1) % per_word
+            got = _fused(x, rows, cols, 0, colwise, shift=shift, out_offset=out_offset)
+            want = _oracle_fragment(x, rows, cols, 0, colwise, out_offset=out_offset)
+            assert_bitwise(got, want, f"fused {dtype} shift {shift} out_offset {out_offset}")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

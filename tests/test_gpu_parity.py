@@ -122,6 +122,27 @@ def test_fragment_output_interface(dtype, shift):
     assert np.array_equal(got[4], full[4][start:start + length])
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("colwise", [True, False])
+def test_every_output_misalignment(dtype, colwise):
+    """Fragment-sized outputs whose virtual base sits at every byte offset inside an
+    output word (4 bytes for FP32 input, 8 for BF16), some with misaligned input
+    buffers too: interior tiles then store bytes instead of words; bytes before
+    out_offset stay untouched."""
+    rows, cols = 128, 2048
+    rng = np.random.default_rng(33)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(2.0) ** rng.integers(-12, 12, rows * cols).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    start = 3 * cols + 5
+    length = rows * cols - start - 11
+    frag = np.ascontiguousarray(x[start:start + length])
+    for out_offset in range(4 if dtype == "f32" else 8):
+        got = gpu_fragment(frag, rows, cols, start, colwise, out_offset=out_offset, shift=out_offset % 3)
+        want = oracle_fragment(frag, rows, cols, start, colwise, out_offset=out_offset)
+        assert_bitwise(got, want, f"{dtype} out_offset {out_offset}")
+
+
 def test_empty_fragment_writes_nothing():
     rows, cols = 128, 256
     ar = torch.full((rows, 8), 3.0, device="cuda")
