@@ -343,18 +343,6 @@ MXFP8_API int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments, const 
                                  mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                                  void* stream);
 
-/* Status of the library's bounded device-side waits on the current device.  The
- * one-pass kernels stream tiles through shared memory by bulk asynchronous copies and
- * wait for each copy on an mbarrier with a poll limit; a wait that gives up (a copy
- * that never lands) sets a device word and ends that warp's work instead of hanging
- * the GPU, and that launch's outputs are then incomplete.  Returns 0 when no wait has
- * given up since the previous call; otherwise clears the word and returns 6
- * (CUDA error, message in mxfp8_last_error).  Blocking: synchronises the current
- * device first.  A diagnostic of this implementation; the pages' method has no
- * counterpart.
- */
-MXFP8_API int mxfp8_async_status(void);
-
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 MXFP8_API const char* mxfp8_last_error(void);
 

@@ -32,13 +32,6 @@ def device_can_access(t: torch.Tensor) -> bool:
     return bool(_capi.load().mxfp8_device_can_access(ctypes.c_void_p(t.data_ptr()), nbytes))
 
 
-def mxfp8_async_status() -> None:
-    """Raise MXFP8Error when a bounded device-side wait of the library (the one-pass
-    kernels' waits on their bulk copies) gave up on the current device since the last
-    call; clears the condition.  Synchronises the device."""
-    _capi.check(_capi.load().mxfp8_async_status())
-
-
 def handle(t: torch.Tensor | None, name: str, allow_host: bool = False) -> Tensor:
     """mxfp8_tensor for a CUDA tensor; None / zero-element tensors give an empty handle.
     With ``allow_host``, a page-locked CPU tensor is accepted when the device can access

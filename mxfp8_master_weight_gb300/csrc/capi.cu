@@ -97,7 +97,6 @@ int check_dims(int64_t rows, int64_t cols, int64_t start, int64_t len) {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sms[kMaxDevices];
-std::atomic<int*> g_flag[kMaxDevices];  // per device: the library's timeout word
 
 int device_info(DeviceInfo* d) {
   cudaError_t e = cudaGetDevice(&d->device);
@@ -109,13 +108,6 @@ int device_info(DeviceInfo* d) {
     if (d->device < kMaxDevices) g_sms[d->device].store(sms);
   }
   d->sms = sms;
-  int* flag = d->device < kMaxDevices ? g_flag[d->device].load() : nullptr;
-  if (flag == nullptr) {
-    e = mxfp8::timeout_flag_address(&flag);
-    if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-    if (d->device < kMaxDevices) g_flag[d->device].store(flag);
-  }
-  d->timeout_flag = flag;
   return MXFP8_OK;
 }
 
@@ -260,16 +252,6 @@ int prep_cast(const mxfp8_cast_job& job, CastParams* p, int* dtype, bool* colwis
   p->vec_out = vec_out;
   *dtype = dt == MXFP8_DTYPE_F32 ? 0 : 1;
   return MXFP8_OK;
-}
-
-// True when p is device memory of some device (not host memory mapped for the device).
-bool is_device_memory(const void* p) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return a.type == cudaMemoryTypeDevice;
 }
 
 int prep_fused(const mxfp8_quantize_job& job, FusedParams* p, int* dtype, bool* colwise,
@@ -506,7 +488,6 @@ int run_fused(const mxfp8_quantize_job* jobs, int32_t njobs, void* stream) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
     for (int i = 0; i < m; ++i) {
       prep_fused(jobs[base + i], &win[i], &dt, &col, &skip);
-      if (!skip) win[i].device_in = is_device_memory(win[i].in);
       key[i] = skip ? -1 : jobs[base + i].model_dtype * 8 + dt * 4 + (win[i].g.shift != 0) * 2 +
                                (win[i].vec_out != 0);
     }
@@ -539,15 +520,6 @@ int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
 }  // namespace mxfp8
 
 extern "C" {
-
-int mxfp8_async_status(void) {
-  int flag = 0;
-  cudaError_t e = mxfp8::read_timeout_flag(&flag, true);
-  if (e != cudaSuccess) return fail(MXFP8_ERR_CUDA, "reading the wait-timeout word: %s", cudaGetErrorString(e));
-  if (flag != 0)
-    return fail(MXFP8_ERR_CUDA, "a bounded wait on an asynchronous copy gave up; outputs of that launch are incomplete");
-  return ok();
-}
 
 const char* mxfp8_last_error(void) { return g_err; }
 

@@ -68,65 +68,6 @@ __device__ __forceinline__ uint4 ld_hint16(const void* p, uint64_t pol) {
   return v;
 }
 
-// ---------------------------------------------------------------- bulk copies, mbarriers
-// Shared-memory address of a pointer into this CTA's shared memory.
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t arrivals) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(arrivals) : "memory");
-}
-
-// Makes initialised mbarriers visible to the asynchronous proxy (the bulk-copy unit).
-__device__ __forceinline__ void mbar_init_fence() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-// One arrival that also announces `bytes` of bulk-copy data to come in this phase.
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Waits for the phase of `bar` with the given parity to complete, giving up after
-// `limit` polls (each poll may suspend the thread for a short, hardware-chosen time);
-// returns false on giving up, so a copy that never lands cannot hang the kernel.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t limit) {
-  for (uint32_t i = 0; i < limit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
-}
-
-// Orders this thread's earlier generic-proxy accesses of shared memory before later
-// asynchronous-proxy (bulk-copy) writes to it.
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Bulk asynchronous copy of `bytes` (a multiple of 16) from global memory to this
-// CTA's shared memory, both addresses 16-byte aligned; completion is counted on `bar`.
-// The L2 policy marks the lines as read once.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                              uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
-      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
 // ---------------------------------------------------------------- per-element access
 template <class T>
 __device__ __forceinline__ uint32_t load_bits(const void* base, int64_t idx) {

@@ -36,11 +36,9 @@ constexpr int kMaxGroups = 8;  // row blocks per warp tile (BF16: 256 columns / 
 #endif
 constexpr int kFusedMinBlocks = MXFP8_FUSED_MIN_BLOCKS;
 
-// E8M0 bytes of the 32 rows' row blocks of a warp's tile, handed from pass 1 to pass 2
-// through shared memory (one such slice per warp).
-using RowScaleRows = uint8_t[32][kMaxGroups];
+// E8M0 bytes of the 32 rows' row blocks of each warp's tile, handed from pass 1 to pass 2.
 struct RowScales {
-  RowScaleRows b[kWarps];
+  uint8_t b[kWarps][32][kMaxGroups];
 };
 
 template <class T, bool kCol>
@@ -80,7 +78,7 @@ __device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t ro
 
 template <class T, bool kCol, int kS, bool kVec, int kModel>
 __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t row0, int64_t col0,
-                                                int lane, RowScaleRows& rs) {
+                                                int lane, RowScales& rsc, int warp) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
@@ -105,7 +103,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
       if (writer) {
         const int64_t i = row0 + rb + r;
         const uint32_t e = e8m0_from_bits<T>(m);
-        rs[rb + r][grp] = static_cast<uint8_t>(e);
+        rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
         p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
         if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, m);
       }
@@ -126,7 +124,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
       float y[T::V];
       model_values<T, kModel>(v[r], y);
       float mr[T::V];
-      const float m = scale_multiplier(rs[rb + r][grp]);
+      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const int64_t o = o0 + (rb + r) * cols;
@@ -140,13 +138,13 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 // A fast tile of a launch whose fragments are all aligned or all shifted.
 template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 __device__ __forceinline__ void fused_fast(const FusedParams& p, int64_t row0, int64_t col0, int lane,
-                                           RowScaleRows& rs) {
+                                           RowScales& rsc, int warp) {
   if constexpr (kShift) {
     with_shift<T>(p.g.shift, [&](auto s) {
-      fused_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane, rs);
+      fused_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane, rsc, warp);
     });
   } else {
-    fused_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane, rs);
+    fused_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane, rsc, warp);
   }
 }
 
@@ -154,7 +152,7 @@ __device__ __forceinline__ void fused_fast(const FusedParams& p, int64_t row0, i
 // touches is whole, so the maxima over the loaded elements are the block maxima.
 template <class T, bool kCol, bool kVec, int kModel>
 __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row0, int64_t col0,
-                                               int lane, RowScaleRows& rs) {
+                                               int lane, RowScales& rsc, int warp) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
@@ -174,7 +172,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       const uint32_t m = group_max<T>(chunk_reduce<T>(a));
       const int64_t i = row0 + rb + r;
       const uint32_t e = e8m0_from_bits<T>(m);
-      if (writer) rs[rb + r][grp] = static_cast<uint8_t>(e);
+      if (writer) rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
       if (writer && i < g.rows && b0 < g.cols &&
           row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1))) {
         p.s_r[i * p.ld_sr + (b0 >> 5)] = static_cast<uint8_t>(e);
@@ -210,7 +208,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       float y[T::V];
       model_values<T, kModel>(v[r], y);
       float mr[T::V];
-      const float m = scale_multiplier(rs[rb + r][grp]);
+      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const uint2 qr = quantize_chunk<T>(y, mr);
@@ -242,7 +240,6 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  RowScaleRows& rs = rsc.b[warp];
   const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
   const int64_t stride = int64_t(gridDim.x) * kWarps;
   for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < total; t += stride) {
@@ -252,218 +249,18 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) fused_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rs);
+        if constexpr (kDirs != kRowOnly) fused_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       } else {
-        if constexpr (kDirs != kBidir) fused_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rs);
+        if constexpr (kDirs != kBidir) fused_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       }
     } else if (kind == kTileMasked) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) fused_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane, rs);
+        if constexpr (kDirs != kRowOnly) fused_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       } else {
-        if constexpr (kDirs != kBidir) fused_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane, rs);
+        if constexpr (kDirs != kBidir) fused_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane, rsc, warp);
       }
     }
   }
-}
-
-// ---------------------------------------------------------------- staged variant
-// The same work with each fast tile streamed through shared memory: the tile's 32
-// rows arrive by bulk asynchronous copies (cp.async.bulk, one row per lane, with a
-// read-once L2 policy) that complete on the warp's mbarrier, and both passes read
-// shared memory.  HBM and L2 see every input byte once, and a warp has a whole tile
-// (16.5 KB) in flight instead of one batch of register loads.  Each warp is its own
-// producer: it requests its next fast tile as soon as a stage is free, so with
-// kStages > 1 the next tile streams in while the current one is processed.  Tiles
-// cut by the fragment or the matrix edge take the register path above.
-#ifndef MXFP8_STAGED_WARPS
-#define MXFP8_STAGED_WARPS 12
-#endif
-#ifndef MXFP8_STAGED_STAGES
-#define MXFP8_STAGED_STAGES 1
-#endif
-constexpr int kStagedWarps = MXFP8_STAGED_WARPS;
-constexpr int kStages = MXFP8_STAGED_STAGES;
-constexpr int kStageRow = 33 * 16;           // 32 chunks + the extra chunk of a realigned row
-constexpr int kStageBytes = 32 * kStageRow;  // one tile
-constexpr size_t kStagedSmem = size_t(kStagedWarps) * kStages * kStageBytes + 8u * kStagedWarps * kStages;
-constexpr uint32_t kWaitPolls = 1u << 20;    // polls before a stage wait gives up
-static_assert(kStagedSmem + sizeof(RowScaleRows) * kStagedWarps <= 227u * 1024u, "shared memory per block");
-
-// Lane's chunk of one staged row: bytes [16 * lane, +16) past the row's first element,
-// which sits kS bytes into the buffer (the copy started at the aligned address below it).
-template <class T, int kS>
-__device__ __forceinline__ uint4 stage_chunk(const uint8_t* row, int lane) {
-  const uint4 a = *reinterpret_cast<const uint4*>(row + 16 * lane);
-  if constexpr (kS == 0) {
-    return a;
-  } else {
-    constexpr int Q = kS / 4, R = (kS % 4) * 8;
-    const uint4 nb = *reinterpret_cast<const uint4*>(row + 16 * lane + 16);
-    const uint32_t w[8] = {a.x, a.y, a.z, a.w, nb.x, nb.y, nb.z, nb.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) o[k] = R ? __funnelshift_r(w[Q + k], w[Q + k + 1], R) : w[Q + k];
-    return make_uint4(o[0], o[1], o[2], o[3]);
-  }
-}
-
-template <class T, bool kCol, int kS, bool kVec, int kModel>
-__device__ __forceinline__ void fused_tile_staged(const FusedParams& p, int64_t row0, int64_t col0,
-                                                  int lane, RowScaleRows& rs, const uint8_t* st) {
-  const int64_t cols = p.g.cols;
-  const int64_t j = col0 + lane * T::V;
-  const int grp = lane / T::G;
-  const bool writer = (lane % T::G) == 0;
-  const int64_t blk = j >> 5;
-
-  // pass 1: block maxima -> scales
-  uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll 8
-  for (int r = 0; r < 32; ++r) {
-    const uint4 a = chunk_abs<T>(stage_chunk<T, kS>(st + r * kStageRow, lane));
-    if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
-    const uint32_t m = group_max<T>(chunk_reduce<T>(a));
-    if (writer) {
-      const int64_t i = row0 + r;
-      const uint32_t e = e8m0_from_bits<T>(m);
-      rs[r][grp] = static_cast<uint8_t>(e);
-      p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
-      if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, m);
-    }
-  }
-  float mc[T::V];
-  if constexpr (kCol) store_col_stats<T, kCol>(p, row0, j, colmax, mc);
-  __syncwarp();
-
-  // pass 2: cast from the same shared-memory rows
-  const int64_t o0 = row0 * cols + j + p.out_shift;
-#pragma unroll 8
-  for (int r = 0; r < 32; ++r) {
-    float y[T::V];
-    model_values<T, kModel>(stage_chunk<T, kS>(st + r * kStageRow, lane), y);
-    float mr[T::V];
-    const float m = scale_multiplier(rs[r][grp]);
-#pragma unroll
-    for (int k = 0; k < T::V; ++k) mr[k] = m;
-    const int64_t o = o0 + r * cols;
-    store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
-    if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
-  }
-  __syncwarp();
-}
-
-template <class T, bool kCol, bool kShift, bool kVec, int kModel>
-__device__ __forceinline__ void fused_staged(const FusedParams& p, int64_t row0, int64_t col0, int lane,
-                                             RowScaleRows& rs, const uint8_t* st) {
-  if constexpr (kShift) {
-    with_shift<T>(p.g.shift, [&](auto s) {
-      fused_tile_staged<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane, rs, st);
-    });
-  } else {
-    fused_tile_staged<T, kCol, 0, kVec, kModel>(p, row0, col0, lane, rs, st);
-  }
-}
-
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-__global__ void __launch_bounds__(kStagedWarps * 32, 1) k_fused_staged(
-    const __grid_constant__ JobBatch<FusedParams, N> b, int* timeout_flag) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ RowScaleRows rsc[kStagedWarps];
-  constexpr int TW = tile_width<T>();
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  RowScaleRows& rs = rsc[warp];
-  uint8_t* stages = smem + size_t(warp) * kStages * kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + size_t(kStagedWarps) * kStages * kStageBytes) + warp * kStages;
-  if (lane == 0) {
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-    mbar_init_fence();
-  }
-  __syncwarp();
-  const uint64_t read_once = l2_policy_evict_first();
-  const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
-  const int64_t stride = int64_t(gridDim.x) * kStagedWarps;
-  const int64_t first = int64_t(blockIdx.x) * kStagedWarps + warp;
-
-  // Producer cursor: requests the next fast tile of this warp's sequence into stage
-  // (issued % kStages); the consumer below meets the fast tiles in the same order.
-  int64_t tp = first;
-  uint32_t issued = 0;
-  auto issue_next = [&]() {
-    for (; tp < total; tp += stride) {
-      int64_t r0, c0;
-      const FusedParams& q = b.job[batch_tile(b, tp, TW, r0, c0)];
-      if (classify_tile<T>(q.g, r0, c0, TW) != kTileFast) continue;
-      const uint32_t shift = kShift ? static_cast<uint32_t>(q.g.shift) : 0u;
-      const uint32_t bytes = shift ? uint32_t(kStageRow) : 32u * 16u;
-      uint64_t* bar = &bars[issued % kStages];
-      if (lane == 0) mbar_arrive_expect_tx(bar, 32u * bytes);
-      __syncwarp();
-      // lane r copies row r: from the aligned chunk holding its first element
-      const char* src = static_cast<const char*>(q.in) +
-                        ((r0 + lane) * q.g.cols + c0 - q.g.start) * T::kBytes - shift;
-      bulk_copy_g2s(stages + (issued % kStages) * kStageBytes + lane * kStageRow, src, bytes, bar, read_once);
-      ++issued;
-      tp += stride;
-      return;
-    }
-  };
-#pragma unroll
-  for (int s = 0; s < kStages; ++s) issue_next();
-
-  uint32_t consumed = 0;
-  bool ok = true;
-  for (int64_t t = first; t < total; t += stride) {
-    int64_t row0, col0;
-    const FusedParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
-    const int kind = classify_tile<T>(p.g, row0, col0, TW);
-    const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
-    if (kind == kTileFast) {
-      const int s = consumed % kStages;
-      const bool landed = mbar_wait(&bars[s], (consumed / kStages) & 1u, kWaitPolls);
-      if (!__all_sync(kFullMask, landed)) {  // the whole warp leaves together
-        ok = false;
-        break;
-      }
-      const uint8_t* st = stages + s * kStageBytes;
-      if (col) {
-        if constexpr (kDirs != kRowOnly) fused_staged<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rs, st);
-      } else {
-        if constexpr (kDirs != kBidir) fused_staged<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rs, st);
-      }
-      ++consumed;
-      fence_proxy_async_smem();  // this stage's reads before the next copy into it
-      issue_next();
-    } else if (kind == kTileMasked) {
-      if (col) {
-        if constexpr (kDirs != kRowOnly) fused_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane, rs);
-      } else {
-        if constexpr (kDirs != kBidir) fused_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane, rs);
-      }
-    }
-  }
-  if (!ok) {  // a stage never completed: report, then wait (bounded) for the copies still in flight
-    if (lane == 0) atomicExch(timeout_flag, 1);
-    for (uint32_t k = consumed; k < issued; ++k) mbar_wait(&bars[k % kStages], (k / kStages) & 1u, kWaitPolls);
-  }
-}
-
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-cudaError_t launch_staged_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  static std::atomic<int> configured[kMaxDevices];
-  auto kern = k_fused_staged<T, kDirs, kShift, kVec, kModel, N>;
-  if (dev.device >= kMaxDevices || configured[dev.device].load() == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kStagedSmem));
-    if (e != cudaSuccess) return e;
-    if (dev.device < kMaxDevices) configured[dev.device].store(1);
-  }
-  JobBatch<FusedParams, N> b;
-  const int64_t total = fill_batch(b, jobs, n);
-  if (total == 0) return cudaSuccess;
-  const unsigned grid = balanced_grid(total, kStagedWarps, int64_t(dev.sms));
-  kern<<<grid, kStagedWarps * 32, kStagedSmem, stream>>>(b, dev.timeout_flag);
-  return cudaGetLastError();
 }
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
@@ -485,19 +282,6 @@ cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cuda
   return cudaGetLastError();
 }
 
-#ifndef MXFP8_FUSED_STAGED
-#define MXFP8_FUSED_STAGED 0
-#endif
-// The staged kernel when every input is device memory (bulk copies are not used on
-// host memory mapped for the device), else the register kernel.
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-cudaError_t launch_pick(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  bool staged = MXFP8_FUSED_STAGED != 0;
-  for (int i = 0; i < n; ++i) staged = staged && jobs[i].device_in != 0;
-  if (staged) return launch_staged_n<T, kDirs, kShift, kVec, kModel, N>(jobs, n, dev, stream);
-  return launch_n<T, kDirs, kShift, kVec, kModel, N>(jobs, n, dev, stream);
-}
-
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's
 // direction set; single BF16-model jobs use the one-entry job table.
 template <class T, bool kShift, bool kVec, int kModel>
@@ -505,8 +289,8 @@ cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaSt
   auto colwise = [](const FusedParams& p) { return p.out_c != nullptr; };
   if constexpr (kModel == kModelBF16) {
     if (n == 1) {
-      return colwise(jobs[0]) ? launch_pick<T, kBidir, kShift, kVec, kModel, 1>(jobs, 1, dev, stream)
-                              : launch_pick<T, kRowOnly, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+      return colwise(jobs[0]) ? launch_n<T, kBidir, kShift, kVec, kModel, 1>(jobs, 1, dev, stream)
+                              : launch_n<T, kRowOnly, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
     }
   }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
@@ -514,13 +298,13 @@ cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaSt
     cudaError_t e;
     switch (batch_dirs(jobs + k, m, colwise)) {
       case kRowOnly:
-        e = launch_pick<T, kRowOnly, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kRowOnly, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
         break;
       case kBidir:
-        e = launch_pick<T, kBidir, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kBidir, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
         break;
       default:
-        e = launch_pick<T, kMixed, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kMixed, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
         break;
     }
     if (e != cudaSuccess) return e;

@@ -65,7 +65,6 @@ struct FusedParams {
   int32_t vec_c;       // colwise amax rows may take 16-byte stores
   int32_t vec_sc;      // colwise scale rows may take V-byte stores
   int32_t vec_out;     // outputs' virtual bases are V-byte aligned
-  int32_t device_in;   // input is device memory (may be read by bulk asynchronous copies)
 };
 
 // One direction of a scale update: scale[r][c] = E8M0(amax[r][c]), r < nrows, c < ncols.
@@ -102,13 +101,7 @@ struct ReduceScaleSegment {
 struct DeviceInfo {
   int device;
   int sms;
-  int* timeout_flag;  // device word a kernel sets when a bounded wait gives up
 };
-
-// The library's device word for timed-out waits on the current device (misc.cu), and
-// a blocking read (optionally clearing it) after the device has gone idle.
-cudaError_t timeout_flag_address(int** addr);
-cudaError_t read_timeout_flag(int* value, bool clear);
 
 // Direction sets a kernel instantiation handles: only rowwise, rowwise + columnwise,
 // or a mix (each job's columnwise pointer picks, per tile, one of the two

@@ -260,21 +260,4 @@ cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, 
   return cudaGetLastError();
 }
 
-// Set (to 1) by a kernel whose bounded wait on an asynchronous copy gave up; read and
-// cleared by the host through read_timeout_flag.
-__device__ int g_timeout_flag;
-
-cudaError_t timeout_flag_address(int** addr) {
-  return cudaGetSymbolAddress(reinterpret_cast<void**>(addr), g_timeout_flag);
-}
-
-cudaError_t read_timeout_flag(int* value, bool clear) {
-  cudaError_t e = cudaDeviceSynchronize();
-  if (e != cudaSuccess) return e;
-  e = cudaMemcpyFromSymbol(value, g_timeout_flag, sizeof(int));
-  if (e != cudaSuccess || !clear || *value == 0) return e;
-  const int zero = 0;
-  return cudaMemcpyToSymbol(g_timeout_flag, &zero, sizeof(int));
-}
-
 }  // namespace mxfp8

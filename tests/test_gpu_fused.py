@@ -71,7 +71,6 @@ def test_fused_cfg4_headline(colwise):
     got = _fused(w.data, w.rows, w.cols, 0, colwise)
     want = oracle.full_cast(w.data, w.rows, w.cols, colwise)
     assert_bitwise(got, want, f"fused cfg4 colwise={colwise}")
-    api.mxfp8_async_status()
 
 
 @pytest.mark.parametrize("cfg", ["cfg1", "cfg3"])
@@ -104,7 +103,6 @@ def test_fused_every_misalignment(dtype):
             got = _fused(x, rows, cols, 0, colwise, shift=shift, out_offset=out_offset)
             want = _oracle_fragment(x, rows, cols, 0, colwise, out_offset=out_offset)
             assert_bitwise(got, want, f"fused {dtype} shift {shift} out_offset {out_offset}")
-    api.mxfp8_async_status()  # no bounded wait of the staged kernel gave up
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
