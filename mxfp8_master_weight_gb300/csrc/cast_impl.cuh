@@ -66,7 +66,10 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const uint8_t* srow = p.s_r + row0 * p.ld_sr + (j >> 5);
   const int64_t o0 = row0 * cols + j + p.out_shift;
-  constexpr int NB = kS ? kShiftBatch : kRowBatch;
+  // FP32 realigning tiles batch 8 rows (the extra words loaded by row lanes keep the
+  // registers in bounds); BF16 ones 4 rows with lane 31 loading them
+  constexpr bool kRowLanes = kS != 0 && T::kBytes == 4;
+  constexpr int NB = kS ? (kRowLanes ? kRowBatch : kShiftBatch) : kRowBatch;
   float mc[T::V];
   if constexpr (kCol) colwise_multipliers<T>(p, row0, j, mc);
 #pragma unroll 1
@@ -75,7 +78,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
     uint32_t sb[NB];
 #pragma unroll
     for (int r = 0; r < NB; ++r) sb[r] = srow[(rb + r) * p.ld_sr];
-    load_rows<NB, kS>(v, src + rb * row_bytes, row_bytes, lane);
+    load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float y[T::V];

@@ -364,10 +364,13 @@ __device__ __forceinline__ uint32_t word_of(const uint4& c, int k) {
 // 16-byte boundary (a multiple of the element size).  kS == 0: one aligned 16-byte
 // load per row.  kS != 0: each lane loads the aligned chunk that holds its first
 // element and takes the words past it from the next lane's chunk -- only the
-// ceil(kS/4) words it needs, one shuffle each (lane 31 loads them from the chunk
-// after the tile row) -- and a half-word funnel shift finishes a 2-byte offset.
+// ceil(kS/4) words it needs, one shuffle each -- and a half-word funnel shift
+// finishes a 2-byte offset.  Lane 31 takes those words from the chunk after the tile
+// row: it loads them itself for every row, or (kRowLanes) lane r loads them for row
+// r with a single load for the batch and lane 31 gets them by one more shuffle per
+// word, which holds 4 registers instead of 4 per row for larger batches.
 // All lanes of the warp must be active.
-template <int NB, int kS, bool kHint = false>
+template <int NB, int kS, bool kHint = false, bool kRowLanes = false>
 __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64_t row_bytes,
                                           int lane, uint64_t pol = 0) {
   if constexpr (kS == 0) {
@@ -379,11 +382,17 @@ __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64
     constexpr int R = (kS % 4) * 8;      // bits to skip inside the next word (0 or 16)
     constexpr int NW = Q + (R != 0);     // words taken from the next lane's chunk
     const char* a = src - kS;
-    uint4 extra[NB];
+    static_assert(NB <= 32, "one lane per row of the batch");
+    uint4 extra[kRowLanes ? 1 : NB];
+    if constexpr (kRowLanes) {  // lane r: the chunk after row r of the tile
+      extra[0] = lane < NB ? ld_head<NW, kHint>(a - lane * 16 + 32 * 16 + lane * row_bytes, pol)
+                           : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       v[r] = ld_chunk<kHint>(a + r * row_bytes, pol);
-      extra[r] = lane == 31 ? ld_head<NW, kHint>(a + r * row_bytes + 16, pol) : make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (!kRowLanes)
+        extra[r] = lane == 31 ? ld_head<NW, kHint>(a + r * row_bytes + 16, pol) : make_uint4(0u, 0u, 0u, 0u);
     }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
@@ -391,7 +400,13 @@ __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64
 #pragma unroll
       for (int k = 0; k < NW; ++k) {
         const uint32_t nx = __shfl_down_sync(kFullMask, w[k], 1);
-        w[4 + k] = lane == 31 ? word_of(extra[r], k) : nx;
+        uint32_t ex;
+        if constexpr (kRowLanes) {
+          ex = __shfl_sync(kFullMask, word_of(extra[0], k), r);
+        } else {
+          ex = word_of(extra[r], k);
+        }
+        w[4 + k] = lane == 31 ? ex : nx;
       }
       uint32_t o[4];
 #pragma unroll
