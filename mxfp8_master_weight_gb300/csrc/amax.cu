@@ -125,6 +125,7 @@ __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0,
 template <class T, int kDirs, bool kShift, int N>
 __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
+  grid_dependency_sync();
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
   const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
@@ -157,8 +158,7 @@ cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaS
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = tile_grid(total, kWarps);
-  k_partial_amax<T, kDirs, kShift, N><<<grid, kThreads, 0, stream>>>(b);
-  return cudaGetLastError();
+  return launch_kernel(k_partial_amax<T, kDirs, kShift, N>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

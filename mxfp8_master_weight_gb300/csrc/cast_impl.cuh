@@ -170,6 +170,7 @@ __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0,
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 __global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
+  grid_dependency_sync();
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
   const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
@@ -202,8 +203,7 @@ cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaS
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = tile_grid(total, kWarps);
-  k_partial_cast<T, kDirs, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
-  return cudaGetLastError();
+  return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

@@ -10,6 +10,7 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 #include "kernels.h"
@@ -36,6 +37,37 @@ struct BF16T {
 };
 template <class T>
 __host__ __device__ constexpr int tile_width() { return 32 * T::V; }
+
+// ---------------------------------------------------------------- launches
+// Programmatic dependent launch.  Every kernel starts with grid_dependency_sync():
+// it returns once the kernel before it in the stream has completed and its writes
+// are visible (at once when this grid was launched without a programmatic
+// dependency), and then lets the next kernel's blocks be scheduled on SMs that this
+// grid frees, so a launch overlaps the tail of the grid before it instead of
+// following its completion.  No global memory is touched before the wait, so the
+// kernel before may be any producer of this kernel's inputs.
+__device__ __forceinline__ void grid_dependency_sync() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch with the programmatic stream serialisation attribute (the kernel must start
+// with grid_dependency_sync()).
+template <class... KArgs, class... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------- memory ops
 // 16-byte global load that does not allocate in L1 (each byte is read once).

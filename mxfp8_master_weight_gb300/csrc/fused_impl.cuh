@@ -237,6 +237,7 @@ template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const __grid_constant__ JobBatch<FusedParams, N> b) {
   __shared__ RowScales rsc;
+  grid_dependency_sync();
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -278,8 +279,7 @@ cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cuda
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  k_fused_quantize<T, kDirs, kShift, kVec, kModel, N><<<grid, kThreads, 0, stream>>>(b);
-  return cudaGetLastError();
+  return launch_kernel(k_fused_quantize<T, kDirs, kShift, kVec, kModel, N>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

@@ -31,6 +31,7 @@ struct ScaleBatch {
 // blockIdx.y selects the segment; blocks stride over its entries.
 template <class T>
 __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constant__ ScaleBatch b) {
+  grid_dependency_sync();
   const ScaleSegment& s = b.seg[blockIdx.y];
   const int64_t n = s.nrows * s.ncols;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -68,6 +69,7 @@ struct ReduceScaleBatch {
 template <class T>
 __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
     const __grid_constant__ ReduceScaleBatch b) {
+  grid_dependency_sync();
   const ReduceScaleSegment& s = b.seg[blockIdx.y];
   const int64_t n = s.nrows * s.ncols;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -116,6 +118,7 @@ template <class T>
 __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict__ slots,
                                                          void* __restrict__ out, int64_t elems,
                                                          int nslots, int vec) {
+  grid_dependency_sync();
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (vec) {
@@ -141,6 +144,7 @@ __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict_
 }
 
 __global__ void __launch_bounds__(kThreads) k_swizzle_scales(const __grid_constant__ SwizzleParams p) {
+  grid_dependency_sync();
   const int64_t tiles_c = p.pc / 4;
   const int64_t lines = (p.pr / 128) * tiles_c * 32;
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
@@ -198,12 +202,8 @@ cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
     int64_t want = (work + kThreads - 1) / kThreads;
     const unsigned gx = unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg));
     const dim3 grid(gx, unsigned(b.nseg));
-    if (dtype == 0) {
-      k_update_scales<F32T><<<grid, kThreads, 0, stream>>>(b);
-    } else {
-      k_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(b);
-    }
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = dtype == 0 ? launch_kernel(k_update_scales<F32T>, grid, kThreads, 0, stream, b)
+                                     : launch_kernel(k_update_scales<BF16T>, grid, kThreads, 0, stream, b);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -226,12 +226,9 @@ cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg
     const int64_t want = (work + kThreads - 1) / kThreads;
     const unsigned gx = unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg));
     const dim3 grid(gx, unsigned(b.nseg));
-    if (dtype == 0) {
-      k_reduce_update_scales<F32T><<<grid, kThreads, 0, stream>>>(b);
-    } else {
-      k_reduce_update_scales<BF16T><<<grid, kThreads, 0, stream>>>(b);
-    }
-    const cudaError_t e = cudaGetLastError();
+    const cudaError_t e = dtype == 0
+                              ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
+                              : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
@@ -241,8 +238,7 @@ cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
                                   cudaStream_t stream) {
   const int64_t lines = (p.pr / 128) * (p.pc / 4) * 32;
   if (lines == 0) return cudaSuccess;
-  k_swizzle_scales<<<grid_for(lines, dev), kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_kernel(k_swizzle_scales, grid_for(lines, dev), kThreads, 0, stream, p);
 }
 
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,
@@ -252,12 +248,8 @@ cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, 
   const int vec = (slot_elems % V == 0) && (reinterpret_cast<uintptr_t>(slots) % 16 == 0) &&
                   (reinterpret_cast<uintptr_t>(out) % 16 == 0);
   const unsigned grid = grid_for(vec ? slot_elems / V : slot_elems, dev);
-  if (dtype == 0) {
-    k_max_reduce<F32T><<<grid, kThreads, 0, stream>>>(slots, out, slot_elems, num_slots, vec);
-  } else {
-    k_max_reduce<BF16T><<<grid, kThreads, 0, stream>>>(slots, out, slot_elems, num_slots, vec);
-  }
-  return cudaGetLastError();
+  if (dtype == 0) return launch_kernel(k_max_reduce<F32T>, grid, kThreads, 0, stream, slots, out, slot_elems, num_slots, vec);
+  return launch_kernel(k_max_reduce<BF16T>, grid, kThreads, 0, stream, slots, out, slot_elems, num_slots, vec);
 }
 
 }  // namespace mxfp8
