@@ -78,29 +78,41 @@ __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
   if (s.vec) {
     const char* src = static_cast<const char*>(s.slot0);
     const int64_t slot_bytes = s.slot_stride * T::kBytes;
-    for (int64_t q = tid; q < n / 4; q += stride) {
-      uint32_t m[4] = {0u, 0u, 0u, 0u};
+    const int64_t quads = n / 4;
+    constexpr int U = 2;  // quads per thread per iteration, all loaded before any store
+    for (int64_t q0 = tid; q0 < quads; q0 += U * stride) {
+      uint32_t m[U][4] = {};
       for (int k = 0; k < s.nslots; ++k) {
-        const char* p = src + k * slot_bytes + q * 4 * T::kBytes;
-        if constexpr (T::kBytes == 4) {
-          const uint4 a = *reinterpret_cast<const uint4*>(p);
-          m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], a.y & kAbs);
-          m[2] = max(m[2], a.z & kAbs); m[3] = max(m[3], a.w & kAbs);
-        } else {
-          const uint2 a = *reinterpret_cast<const uint2*>(p);
-          m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], (a.x >> 16) & kAbs);
-          m[2] = max(m[2], a.y & kAbs); m[3] = max(m[3], (a.y >> 16) & kAbs);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int64_t q = q0 + u * stride;
+          if (q >= quads) break;
+          const char* p = src + k * slot_bytes + q * 4 * T::kBytes;
+          if constexpr (T::kBytes == 4) {
+            const uint4 a = ld_stream16(p);
+            m[u][0] = max(m[u][0], a.x & kAbs); m[u][1] = max(m[u][1], a.y & kAbs);
+            m[u][2] = max(m[u][2], a.z & kAbs); m[u][3] = max(m[u][3], a.w & kAbs);
+          } else {
+            const uint2 a = *reinterpret_cast<const uint2*>(p);
+            m[u][0] = max(m[u][0], a.x & kAbs); m[u][1] = max(m[u][1], (a.x >> 16) & kAbs);
+            m[u][2] = max(m[u][2], a.y & kAbs); m[u][3] = max(m[u][3], (a.y >> 16) & kAbs);
+          }
         }
       }
-      if constexpr (T::kBytes == 4) {
-        reinterpret_cast<uint4*>(s.reduced)[q] = make_uint4(m[0], m[1], m[2], m[3]);
-      } else {
-        reinterpret_cast<uint2*>(s.reduced)[q] = make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
-      }
-      uint32_t out = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[k]) << (8 * k);
-      reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+      for (int u = 0; u < U; ++u) {
+        const int64_t q = q0 + u * stride;
+        if (q >= quads) break;
+        if constexpr (T::kBytes == 4) {
+          reinterpret_cast<uint4*>(s.reduced)[q] = make_uint4(m[u][0], m[u][1], m[u][2], m[u][3]);
+        } else {
+          reinterpret_cast<uint2*>(s.reduced)[q] = make_uint2(m[u][0] | (m[u][1] << 16), m[u][2] | (m[u][3] << 16));
+        }
+        uint32_t out = 0;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[u][k]) << (8 * k);
+        reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+      }
     }
   } else {
     for (int64_t e = tid; e < n; e += stride) {
