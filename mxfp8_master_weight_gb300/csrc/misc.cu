@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
     for (int64_t q = tid; q < n / 4; q += stride) {
       uint32_t w[4];
       if constexpr (T::kBytes == 4) {
-        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(s.amax) + 4 * q);
+        const uint4 a = ld_stream16(static_cast<const uint32_t*>(s.amax) + 4 * q);
         w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
       } else {
         const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(s.amax) + 4 * q);

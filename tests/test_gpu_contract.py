@@ -102,3 +102,39 @@ def test_special_values_follow_stated_conventions():
     assert np.isnan(got[0][0, 0]) and np.isinf(got[0][0, 1])
     assert got[2][0, 0] == 0xFF and got[2][0, 1] == 0xFF
     assert np.all(got[4] == 0x7F)
+
+
+def test_kernels_see_the_writes_of_the_kernel_before_them():
+    """Every library kernel is launched as a programmatic dependent of the kernel before
+    it in the stream and waits for it before touching memory: a torch kernel that
+    rewrites the master weight right before the amax, our own amax -> scales -> cast
+    chain, and a torch kernel that consumes the cast output right after it all see
+    each other's writes, step after step, with no synchronisation in between."""
+    rows, cols = 1024, 2048
+    rng = np.random.default_rng(9)
+    x = to_device(wl.normal_f32(rng, rows * cols))
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    ar = torch.zeros((rr, rc), device="cuda")
+    ac = torch.zeros((cr, cc), device="cuda")
+    sr = torch.empty((rr, rc), dtype=torch.uint8, device="cuda")
+    sc = torch.empty((cr, cc), dtype=torch.uint8, device="cuda")
+    qr = torch.empty(rows * cols, dtype=torch.uint8, device="cuda")
+    qc = torch.empty(rows * cols, dtype=torch.uint8, device="cuda")
+    first = None
+    seen = []
+    for step in range(6):
+        x.mul_(2.0)                                   # producer: a torch kernel
+        api.mxfp8_partial_amax(x, ar, ac, rows, cols, 0)
+        api.mxfp8_update_scales(ar, ac, sr, sc, rows, cols)
+        api.mxfp8_partial_cast(x, sr, sc, qr, qc, rows, cols, 0)
+        seen.append((sr.to(torch.int32).sum(), qr.to(torch.int64).sum()))  # consumer kernels
+        if first is None:
+            first = (ar.clone(), sr.clone(), qr.clone(), qc.clone())
+    torch.cuda.synchronize()
+    # doubling x doubles every amax and adds one to every scale byte; the data are unchanged
+    assert torch.equal(ar, first[0] * 32.0)
+    assert torch.equal(sr.to(torch.int32), first[1].to(torch.int32) + 5)
+    assert torch.equal(qr, first[2]) and torch.equal(qc, first[3])
+    sums = [(int(a), int(b)) for a, b in seen]
+    assert all(sums[k + 1][0] - sums[k][0] == rr * rc for k in range(5))
+    assert len({b for _, b in sums}) == 1
