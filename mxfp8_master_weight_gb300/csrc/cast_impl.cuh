@@ -57,7 +57,9 @@ __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t
 
 // Whole tile inside the fragment: 16-byte loads (realigned for a shifted virtual
 // base), one scale byte per row, word stores when the outputs are aligned.
-template <class T, bool kCol, int kS, bool kVec, int kModel>
+// kM: byte offset of the outputs' virtual bases past a V-byte boundary (0: word
+// stores; > 0: aligned pieces; < 0: bytes, the two outputs differ).
+template <class T, bool kCol, int kS, int kM, int kModel>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
                                                int lane) {
   const int64_t cols = p.g.cols;
@@ -88,9 +90,36 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const int64_t o = o0 + (rb + r) * cols;
-      store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
-      if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
+      store_chunk_at<T, kM>(p.out_r + o, quantize_chunk<T>(y, mr));
+      if constexpr (kCol) store_chunk_at<T, kM>(p.out_c + o, quantize_chunk<T>(y, mc));
     }
+  }
+}
+
+// Fast tile with outputs that are not V-aligned (kVec false).  The offset m of each
+// output past a V-byte boundary is the same for every row and lane of the tile; when
+// both outputs share it, it selects a specialisation with aligned piece stores: for
+// an aligned input any m, for a realigned input the m that a fragment-sized output in
+// an aligned allocation has (input offset / element size) -- other combinations store
+// bytes.
+template <class T, bool kCol, int kS, int kModel>
+__device__ __forceinline__ void cast_tile_unaligned(const CastParams& p, int64_t row0, int64_t col0,
+                                                    int lane) {
+  constexpr uint32_t V = T::V;
+  const uint32_t mr = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.out_r) + uintptr_t(p.out_shift)) & (V - 1);
+  const uint32_t mc =
+      kCol ? static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.out_c) + uintptr_t(p.out_shift)) & (V - 1) : mr;
+  if (mr != mc || mr == 0) {
+    cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane);
+  } else if constexpr (kS != 0) {
+    constexpr int M = (kS / T::kBytes) % int(V);
+    if (M != 0 && mr == uint32_t(M)) {
+      cast_tile_fast<T, kCol, kS, M, kModel>(p, row0, col0, lane);
+    } else {
+      cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane);
+    }
+  } else {
+    with_out_offset<T>(mr, [&](auto m) { cast_tile_fast<T, kCol, 0, decltype(m)::value, kModel>(p, row0, col0, lane); });
   }
 }
 
@@ -99,10 +128,18 @@ template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 __device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int64_t col0, int lane) {
   if constexpr (kShift) {
     with_shift<T>(p.g.shift, [&](auto s) {
-      cast_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane);
+      if constexpr (kVec) {
+        cast_tile_fast<T, kCol, decltype(s)::value, 0, kModel>(p, row0, col0, lane);
+      } else {
+        cast_tile_unaligned<T, kCol, decltype(s)::value, kModel>(p, row0, col0, lane);
+      }
     });
   } else {
-    cast_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane);
+    if constexpr (kVec) {
+      cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane);
+    } else {
+      cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane);
+    }
   }
 }
 
@@ -236,24 +273,18 @@ cudaError_t launch(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStr
   return cudaSuccess;
 }
 
-template <class T, int kModel>
-cudaError_t launch_variant(const CastParams* jobs, int n, bool shifted, bool vec_out,
-                           const DeviceInfo& dev, cudaStream_t stream) {
-  if (shifted) {
-    return vec_out ? launch<T, true, true, kModel>(jobs, n, dev, stream)
-                   : launch<T, true, false, kModel>(jobs, n, dev, stream);
-  }
-  return vec_out ? launch<T, false, true, kModel>(jobs, n, dev, stream)
-                 : launch<T, false, false, kModel>(jobs, n, dev, stream);
-}
-
-// All launches for one input dtype T (instantiated by that dtype's translation unit).
-template <class T>
-cudaError_t launch_for_dtype(const CastParams* jobs, int n, bool shifted, bool vec_out, int model,
+// All launches for one input dtype T and output alignment kVec (instantiated by that
+// combination's translation unit).
+template <class T, bool kVec>
+cudaError_t launch_for_dtype(const CastParams* jobs, int n, bool shifted, int model,
                              const DeviceInfo& dev, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
-  if (model == kModelF16) return launch_variant<T, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
-  return launch_variant<T, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
+  if (model == kModelF16) {
+    return shifted ? launch<T, true, kVec, kModelF16>(jobs, n, dev, stream)
+                   : launch<T, false, kVec, kModelF16>(jobs, n, dev, stream);
+  }
+  return shifted ? launch<T, true, kVec, kModelBF16>(jobs, n, dev, stream)
+                 : launch<T, false, kVec, kModelBF16>(jobs, n, dev, stream);
 }
 
 }  // namespace

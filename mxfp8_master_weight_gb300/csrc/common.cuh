@@ -301,6 +301,81 @@ __device__ __forceinline__ void store_chunk(uint8_t* dst, const uint2& q) {
   }
 }
 
+// A compile-time integer handed to the generic lambdas of the dispatch helpers.
+template <int S>
+struct ShiftC {
+  static constexpr int value = S;
+};
+
+// Bytes [off, off + 4) of a lane's V output bytes (q.x, then q.y), as the low bytes.
+template <class T, int kOff>
+__device__ __forceinline__ uint32_t chunk_bytes(const uint2& q) {
+  if constexpr (kOff == 0) {
+    return q.x;
+  } else if constexpr (kOff < 4) {
+    return T::V == 4 ? q.x >> (8 * kOff) : __funnelshift_r(q.x, q.y, 8 * kOff);
+  } else {
+    return q.y >> (8 * (kOff - 4));
+  }
+}
+
+// Stores the V bytes at dst, which sits kM bytes past a V-byte boundary (the same
+// offset for every lane and row of a tile, known at compile time), as naturally
+// aligned 1-, 2- and 4-byte pieces from byte kOff on: at most 3 stores for V = 4 and
+// 4 for V = 8 instead of V byte stores.
+template <class T, int kM, int kOff = 0>
+__device__ __forceinline__ void store_chunk_pieces(uint8_t* dst, const uint2& q) {
+  if constexpr (kOff < T::V) {
+    constexpr int kA = (kM + kOff) % 4;  // address mod 4 of this piece
+    constexpr int kS = (kA == 0 && kOff + 4 <= T::V) ? 4 : ((kA % 2 == 0 && kOff + 2 <= T::V) ? 2 : 1);
+    const uint32_t bits = chunk_bytes<T, kOff>(q);
+    if constexpr (kS == 4) {
+      *reinterpret_cast<uint32_t*>(dst + kOff) = bits;
+    } else if constexpr (kS == 2) {
+      *reinterpret_cast<uint16_t*>(dst + kOff) = static_cast<uint16_t>(bits);
+    } else {
+      dst[kOff] = static_cast<uint8_t>(bits);
+    }
+    store_chunk_pieces<T, kM, kOff + kS>(dst, q);
+  }
+}
+
+// Store of a lane's V output bytes for an output whose virtual base sits kM bytes past
+// a V-byte boundary: kM == 0 one word, 0 < kM < V naturally aligned pieces, kM < 0
+// (offset not known at compile time) single bytes.
+template <class T, int kM>
+__device__ __forceinline__ void store_chunk_at(uint8_t* dst, const uint2& q) {
+  if constexpr (kM == 0) {
+    store_chunk<T, true>(dst, q);
+  } else if constexpr (kM > 0) {
+    store_chunk_pieces<T, kM>(dst, q);
+  } else {
+    store_chunk<T, false>(dst, q);
+  }
+}
+
+// Calls f(ShiftC<M>{}) with M the compile-time copy of a non-zero output offset m < V.
+template <class T, class F>
+__device__ __forceinline__ void with_out_offset(uint32_t m, F&& f) {
+  if constexpr (T::V == 4) {
+    switch (m) {
+      case 1: f(ShiftC<1>{}); break;
+      case 2: f(ShiftC<2>{}); break;
+      default: f(ShiftC<3>{}); break;
+    }
+  } else {
+    switch (m) {
+      case 1: f(ShiftC<1>{}); break;
+      case 2: f(ShiftC<2>{}); break;
+      case 3: f(ShiftC<3>{}); break;
+      case 4: f(ShiftC<4>{}); break;
+      case 5: f(ShiftC<5>{}); break;
+      case 6: f(ShiftC<6>{}); break;
+      default: f(ShiftC<7>{}); break;
+    }
+  }
+}
+
 // ---------------------------------------------------------------- fragment geometry
 // The fragment is every element from (rs, cs) to (re, ce) in row-major order, so row
 // i holds fragment columns [row_lo(i), row_hi(i)] (none when i is outside [rs, re])
@@ -451,10 +526,6 @@ __device__ __forceinline__ void load_rows(uint4 (&v)[NB], const char* src, int64
 // Calls f(ShiftC<S>{}) with S the compile-time copy of `shift`, a non-zero byte
 // offset from a 16-byte boundary that is a multiple of T's element size: each offset
 // gets its own specialisation of the realigning loads.
-template <int S>
-struct ShiftC {
-  static constexpr int value = S;
-};
 template <class T, class F>
 __device__ __forceinline__ void with_shift(int32_t shift, F&& f) {
   if constexpr (T::kBytes == 4) {

@@ -158,11 +158,17 @@ cudaError_t launch_fused_quantize(const FusedParams* jobs, int n, int dtype, boo
                                   bool vec_out, int model, const DeviceInfo& dev,
                                   cudaStream_t stream);
 
-// Per-input-dtype halves of the two launchers above (separate translation units).
-cudaError_t launch_partial_cast_f32(const CastParams* jobs, int n, bool shifted, bool vec_out,
-                                    int model, const DeviceInfo& dev, cudaStream_t stream);
-cudaError_t launch_partial_cast_bf16(const CastParams* jobs, int n, bool shifted, bool vec_out,
-                                     int model, const DeviceInfo& dev, cudaStream_t stream);
+// Parts of the two launchers above in separate translation units: the cast per input
+// dtype and output alignment (word-aligned outputs, or not), the one-pass kernel per
+// input dtype.
+cudaError_t launch_partial_cast_f32(const CastParams* jobs, int n, bool shifted, int model,
+                                    const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast_f32_unaligned(const CastParams* jobs, int n, bool shifted, int model,
+                                              const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast_bf16(const CastParams* jobs, int n, bool shifted, int model,
+                                     const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast_bf16_unaligned(const CastParams* jobs, int n, bool shifted, int model,
+                                               const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_fused_quantize_f32(const FusedParams* jobs, int n, bool shifted, bool vec_out,
                                       int model, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_fused_quantize_bf16(const FusedParams* jobs, int n, bool shifted,

@@ -126,10 +126,11 @@ def test_fragment_output_interface(dtype, shift):
 @pytest.mark.parametrize("colwise", [True, False])
 def test_every_output_misalignment(dtype, colwise):
     """Fragment-sized outputs whose virtual base sits at every byte offset inside an
-    output word (4 bytes for FP32 input, 8 for BF16), some with misaligned input
-    buffers too: interior tiles then store bytes instead of words; bytes before
-    out_offset stay untouched."""
-    rows, cols = 128, 2048
+    output word (4 bytes for FP32 input, 8 for BF16), combined with input buffers at
+    every element offset inside a 16-byte chunk: interior tiles store aligned pieces
+    (the specialisations for an aligned input and for the input offset that matches
+    the output offset) or bytes; bytes before out_offset stay untouched."""
+    rows, cols = 128, 1024
     rng = np.random.default_rng(33)
     x = wl.normal_f32(rng, rows * cols) * np.float32(2.0) ** rng.integers(-12, 12, rows * cols).astype(np.float32)
     if dtype == "bf16":
@@ -137,10 +138,12 @@ def test_every_output_misalignment(dtype, colwise):
     start = 3 * cols + 5
     length = rows * cols - start - 11
     frag = np.ascontiguousarray(x[start:start + length])
-    for out_offset in range(4 if dtype == "f32" else 8):
-        got = gpu_fragment(frag, rows, cols, start, colwise, out_offset=out_offset, shift=out_offset % 3)
+    per_word = 4 if dtype == "f32" else 8
+    for out_offset in range(per_word):
         want = oracle_fragment(frag, rows, cols, start, colwise, out_offset=out_offset)
-        assert_bitwise(got, want, f"{dtype} out_offset {out_offset}")
+        for shift in range(per_word):
+            got = gpu_fragment(frag, rows, cols, start, colwise, out_offset=out_offset, shift=shift)
+            assert_bitwise(got, want, f"{dtype} out_offset {out_offset} input shift {shift}")
 
 
 def test_empty_fragment_writes_nothing():
