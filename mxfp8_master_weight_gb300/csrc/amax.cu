@@ -25,9 +25,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
 constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
-#ifndef MXFP8_MIN_BLOCKS
-#define MXFP8_MIN_BLOCKS 1  // resident blocks per SM the register allocation must allow
-#endif
+// Resident blocks per SM the register allocation must allow: the amax is a pure
+// streaming read, and 3 blocks (24 warps, at most 85 registers) keep more loads in flight
+// than the 2 an unconstrained allocation leaves room for.
+constexpr int kMinBlocks = 3;
 
 // Per-row work shared by both tile paths: fold |x| of one chunk into the column
 // maxima and return the maximum of the chunk's 32-element row block (all lanes of
@@ -123,7 +124,7 @@ __device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0,
 }
 
 template <class T, int kDirs, bool kShift, int N>
-__global__ void __launch_bounds__(kThreads, MXFP8_MIN_BLOCKS) k_partial_amax(
+__global__ void __launch_bounds__(kThreads, kMinBlocks) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
