@@ -10,6 +10,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import hashlib
 import os
+import re
 import shutil
 import subprocess
 
@@ -39,13 +40,24 @@ def _sources():
     return files
 
 
+_COMMENT = re.compile(r"//[^\n]*|/\*.*?\*/", re.S)
+
+
+def code_text(text: str) -> str:
+    """A source file's code with comments dropped and whitespace runs collapsed (the
+    sources hold no comment markers inside string literals)."""
+    return " ".join(_COMMENT.sub(" ", text).split())
+
+
 def source_digest() -> str:
-    """SHA-256 over every source file of the library (names and contents)."""
+    """SHA-256 over the code of every source file of the library (names and contents,
+    comments and layout excluded: editing a comment changes neither the kernels nor
+    the digest that build stamps and recorded profiles refer to)."""
     h = hashlib.sha256()
     for f in _sources():
         h.update(os.path.basename(f).encode())
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f, encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
     return h.hexdigest()
 
 

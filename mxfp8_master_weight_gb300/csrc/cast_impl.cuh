@@ -1,8 +1,9 @@
 // Partial cast kernel templates: master values of a contiguous fragment -> model
 // dtype (BF16, or FP16; nearest-even) -> E4M3 (nearest-even, saturating at 448),
 // scaled by the E8M0 block scales, written in place into the rowwise and
-// (optionally) columnwise outputs.  cast_f32.cu and cast_bf16.cu instantiate them
-// for FP32 and BF16 master values.
+// (optionally) columnwise outputs.  cast_f32.cu / cast_bf16.cu instantiate them for
+// FP32 and BF16 master values with word-aligned outputs, cast_*_unaligned.cu for
+// outputs that are not.
 //
 // Follows "Support row-only MXFP8 distributed master-weight casts" (sections
 // "Changes" and the flow diagram): rounding goes through the model dtype, the
@@ -12,8 +13,9 @@
 //
 // Work unit and tile classes as in the amax kernel: one warp per 32 x (32*V)
 // tile, one 16-byte input chunk per lane per row; a row's V output bytes per
-// direction leave as one 4- (FP32) or 8-byte (BF16) store, so a warp writes 128
-// or 256 contiguous bytes per row and direction.  The columnwise multipliers of a
+// direction leave as one 4- (FP32) or 8-byte (BF16) store when the output is
+// word-aligned (naturally aligned pieces otherwise), so a warp writes 128 or 256
+// contiguous bytes per row and direction.  The columnwise multipliers of a
 // lane's V columns are loaded once per tile; the rowwise multiplier once per row.
 #pragma once
 

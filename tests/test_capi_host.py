@@ -197,3 +197,13 @@ def test_swizzle_size_and_validation(lib):
     assert sw(ctypes.byref(T(P, F32, 130, 6)), ctypes.byref(T(P + 8192, U8, 2048)), 130, 6, 0, None) == 3
     assert sw(ctypes.byref(s), ctypes.byref(E()), 130, 6, 0, None) == 4
     assert sw(ctypes.byref(T(P, U8, 129, 6)), ctypes.byref(T(P + 8192, U8, 2048)), 130, 6, 0, None) == 2
+
+
+def test_code_digest_ignores_comments_only():
+    from mxfp8_master_weight_gb300 import build
+    a = "int f(int x) {  // doubles x\n  return 2 * x; /* fast */ }\n"
+    b = "/* a header */\nint f(int x) {\n  return 2 * x;\n}  // changed comment\n"
+    c = "int f(int x) { return 3 * x; }"
+    assert build.code_text(a) == build.code_text(b)
+    assert build.code_text(a) != build.code_text(c)
+    assert len(build.source_digest()) == 64
