@@ -37,7 +37,7 @@ def torch_dtype(x: np.ndarray):
 
 def gpu_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bool, *,
                  out_offset: int | None = None, out_size: int | None = None, shift: int = 0,
-                 pad: int = 0, amax_fill: float = 0.0, sentinel: int = 0xA5):
+                 pad: int = 0, amax_fill: float = 0.0, sentinel: int = 0xA5, model: str = "bf16"):
     """amax -> scales -> cast of one fragment on the GPU.  Returns host arrays
     (amax_r, amax_c, scale_r, scale_c, q_r, q_c); columnwise items None when absent."""
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
@@ -55,7 +55,7 @@ def gpu_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bo
         out_size = rows * cols if out_offset == start else frag.size + out_offset
     qr = torch.full((out_size,), sentinel, dtype=torch.uint8, device="cuda")
     qc = torch.full((out_size,), sentinel, dtype=torch.uint8, device="cuda") if colwise else None
-    api.mxfp8_partial_cast(x, sr, sc, qr, qc, rows, cols, start, out_offset)
+    api.mxfp8_partial_cast(x, sr, sc, qr, qc, rows, cols, start, out_offset, model_dtype=model)
     torch.cuda.synchronize()
     h = lambda t: None if t is None else to_host(t)
     return h(ar), h(ac), h(sr), h(sc), h(qr), h(qc)
@@ -63,7 +63,7 @@ def gpu_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bo
 
 def oracle_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bool, *,
                     out_offset: int | None = None, out_size: int | None = None, pad: int = 0,
-                    amax_fill: float = 0.0, sentinel: int = 0xA5):
+                    amax_fill: float = 0.0, sentinel: int = 0xA5, model: str = "bf16"):
     """The same step sequence on the CPU oracle."""
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
     npdt = frag.dtype
@@ -85,7 +85,7 @@ def oracle_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise:
         out_size = rows * cols if out_offset == start else frag.size + out_offset
     qr = np.full(out_size, sentinel, np.uint8)
     qc = np.full(out_size, sentinel, np.uint8) if colwise else None
-    oracle.partial_cast(frag, rows, cols, start, sr, sc, qr, qc, out_offset)
+    oracle.partial_cast(frag, rows, cols, start, sr, sc, qr, qc, out_offset, model=model)
     return ar, ac, sr, sc, qr, qc
 
 

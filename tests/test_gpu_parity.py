@@ -146,6 +146,26 @@ def test_every_output_misalignment(dtype, colwise):
             assert_bitwise(got, want, f"{dtype} out_offset {out_offset} input shift {shift}")
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_output_misalignment_f16_model(dtype):
+    """The aligned-piece stores of fragment-sized outputs with FP16 as the model dtype,
+    for an aligned input buffer and for the input offset that matches each output offset."""
+    rows, cols = 64, 1024
+    rng = np.random.default_rng(34)
+    x = wl.normal_f32(rng, rows * cols) * np.float32(2.0) ** rng.integers(-20, 8, rows * cols).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    start = cols + 3
+    frag = np.ascontiguousarray(x[start:rows * cols - 5])
+    per_word = 4 if dtype == "f32" else 8
+    for out_offset in range(per_word):
+        want = oracle_fragment(frag, rows, cols, start, True, out_offset=out_offset, model="f16")
+        # input virtual base aligned (shift = start mod per_word), or offset like the output
+        for shift in sorted({start % per_word, out_offset}):
+            got = gpu_fragment(frag, rows, cols, start, True, out_offset=out_offset, shift=shift, model="f16")
+            assert_bitwise(got, want, f"{dtype} f16 model out_offset {out_offset} shift {shift}")
+
+
 def test_empty_fragment_writes_nothing():
     rows, cols = 128, 256
     ar = torch.full((rows, 8), 3.0, device="cuda")
