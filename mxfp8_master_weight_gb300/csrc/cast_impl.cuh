@@ -29,7 +29,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
 constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
-constexpr int kMinBlocks = 1;  // resident blocks per SM the register allocation must allow
+// Resident blocks per SM the register allocation must allow: 2 for BF16 input, whose
+// batched kernels would otherwise take 168 registers and run one block per SM.
+template <class T>
+constexpr int min_blocks() { return T::kBytes == 2 ? 2 : 1; }
 
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
@@ -205,7 +208,7 @@ __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0,
 }
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) k_partial_cast(
+__global__ void __launch_bounds__(kThreads, min_blocks<T>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
