@@ -221,6 +221,83 @@ def run_reference(args):
     }))
 
 
+def graph_us_per_call(call, stream, elems: int, rounds: int = 7, replays: int = 20) -> float:
+    """Median over `rounds` of the µs per call of a CUDA graph holding G calls (G = 50 for
+    fragments of at most 4M elements, else 10), replayed `replays` times per round."""
+    import torch
+
+    g_calls = 50 if elems <= 4 * 2 ** 20 else 10
+    side = torch.cuda.Stream(stream.device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            call.call(side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(g_calls):
+            call.call(side)
+    graph.replay()
+    torch.cuda.synchronize()
+    per_round = []
+    for _ in range(rounds):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per_round.append(a.elapsed_time(b) * 1e3 / (replays * g_calls))
+    return statistics.median(per_round)
+
+
+def measure_configs(x_headline, dev) -> dict:
+    """amax and cast µs per call on the other workloads (configs 1-3 and the headline weight
+    row-only), the pages' timing method: graphs of repeated calls, 7 rounds, median.
+    Configs 1-3 fit in L2 (126 MB), so their figures are L2-warm, not HBM measurements."""
+    import torch
+
+    from mxfp8_master_weight_gb300 import api
+    from mxfp8_master_weight_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream(dev)
+    w1, w2, w3 = wl.cfg1_tiny(), wl.cfg2_bf16_outliers(), wl.cfg3_square()
+    cases = [  # name, weight shape, flat device data, fragment start/length, colwise, memory
+        ("cfg1 160x96 FP32 full bidirectional", w1, 0, w1.numel, True, "L2-warm"),
+        ("cfg2 1024x1024 BF16 [17, +262144) bidirectional", w2, 17, w2.numel // 4, True, "L2-warm"),
+        ("cfg2 1024x1024 BF16 [17, +262144) row-only", w2, 17, w2.numel // 4, False, "L2-warm"),
+        ("cfg3 4096x4096 FP32 full bidirectional", w3, 0, w3.numel, True, "L2-warm"),
+        ("cfg3 4096x4096 FP32 [17, +n/4) bidirectional", w3, 17, w3.numel // 4, True, "L2-warm"),
+        ("cfg4 16384x6144 FP32 full row-only", None, 0, ROWS * COLS, False, "HBM"),
+    ]
+    out = {}
+    for name, w, start, length, colwise, mem in cases:
+        if w is None:
+            rows, cols, flat = ROWS, COLS, x_headline
+        else:
+            rows, cols = w.rows, w.cols
+            if w.data.dtype == np.uint16:
+                flat = torch.from_numpy(w.data.view(np.int16)).to(dev).view(torch.bfloat16)
+            else:
+                flat = torch.from_numpy(w.data).to(dev)
+        frag = flat[start:start + length]
+        (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+        ar = torch.zeros((rr, rc), dtype=frag.dtype, device=dev)
+        ac = torch.zeros((cr, cc), dtype=frag.dtype, device=dev) if colwise else None
+        sr = torch.empty((rr, rc), dtype=torch.uint8, device=dev)
+        scl = torch.empty((cr, cc), dtype=torch.uint8, device=dev) if colwise else None
+        qr = torch.empty(rows * cols, dtype=torch.uint8, device=dev)
+        qc = torch.empty(rows * cols, dtype=torch.uint8, device=dev) if colwise else None
+        amax = api.prepare_partial_amax(frag, ar, ac, rows, cols, start)
+        amax.call(stream)
+        api.mxfp8_update_scales(ar, ac, sr, scl, rows, cols)
+        cast = api.prepare_partial_cast(frag, sr, scl, qr, qc, rows, cols, start)
+        out[name] = {"amax_us": round(graph_us_per_call(amax, stream, length), 3),
+                     "cast_us": round(graph_us_per_call(cast, stream, length), 3), "memory": mem}
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -317,7 +394,18 @@ def run_ours(args):
     b_us = g0.elapsed_time(g1) * 1e3 / b_steps
     b_bytes = sharded_step_bytes(bspecs, bsc.num_shards, bsc.layout.total)
     bsc_launches = bsc.launches_per_step()
+    # per-phase split of the sharded step (events around the phases of a few steps)
+    phase_us = [[], [], []]
+    for _ in range(10):
+        pe = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        bsc.step(bshards, events=pe)
+        torch.cuda.synchronize()
+        for k, (a_, b_) in enumerate(((0, 1), (1, 3), (3, 4))):
+            phase_us[k].append(pe[a_].elapsed_time(pe[b_]) * 1e3)
+    b_phases = {nm: round(statistics.median(v), 2)
+                for nm, v in zip(("amax", "reduce_scales", "cast"), phase_us)}
     del bshards, bsc, batch
+    configs = measure_configs(x, dev)
 
     # end to end through the public API with host buffers: the pipelined host-staged
     # quantiser (chunks of whole 32-row bands; copy in, one-pass quantise, copy out on
@@ -406,7 +494,7 @@ def run_ours(args):
             "workload": "7 FP32 weights (8192x8192; 4096x4096 / 2048x8192, 3 row-only, 4 "
                         "bidirectional; 167.8M elements), 4 emulated shards in own buffers",
             "launches_per_step": bsc_launches,
-            "us_per_step": round(b_us, 2), "algorithmic_bytes": b_bytes,
+            "us_per_step": round(b_us, 2), "phases_us": b_phases, "algorithmic_bytes": b_bytes,
             "gbs": round(b_bytes / (b_us * 1e-6) / 1e9, 1),
             "frac_of_" + peak_kind + "_peak": round(b_bytes / (b_us * 1e-6) / 1e9 / peak, 4)},
         "e2e": {"value": round(e2e_bytes / e2e_t / 1e9, 1), "unit": "GB/s",
@@ -415,6 +503,10 @@ def run_ours(args):
                 "path": f"HostQuantizer: {len(hq.chunks)} chunks of {hq.chunk_rows} rows, "
                         "3 streams, one-pass kernel per chunk",
                 "copy_gbs": round((h2d + d2h) * e2e_steps / e2e_t / 1e9, 1)},
+        "other_configs": {
+            "method": "CUDA graph of 50 calls (fragments <= 4M elements) else 10, 20 replays per "
+                      "round, 7 rounds, median us per call; outputs checked bitwise in the tests",
+            "cases": configs},
         "gpu_launches": sc.launches_per_step() * args.steps,
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,

@@ -91,9 +91,11 @@ __device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int
 
 // Tile cut by the fragment boundary or the matrix edge: per-element predicated
 // loads, issued a batch of rows at a time; only blocks that meet the fragment are
-// written.
+// written.  Inlined into the kernel, so the fragment geometry is read straight from
+// the kernel's parameters (behind a call, every store through an output pointer made
+// the compiler reload it, which doubled the time of small, all-masked fragments).
 template <class T, bool kCol>
-__device__ __noinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0, int64_t col0,
+__device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0, int64_t col0,
                                               int lane) {
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;

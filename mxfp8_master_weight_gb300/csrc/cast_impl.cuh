@@ -30,9 +30,12 @@ constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fas
 constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 // Resident blocks per SM the register allocation must allow: 2 for BF16 input, whose
-// batched kernels would otherwise take 168 registers and run one block per SM.
-template <class T>
-constexpr int min_blocks() { return T::kBytes == 2 ? 2 : 1; }
+// batched kernels would otherwise take 168 registers and run one block per SM; 3 for
+// the single-fragment FP32 kernels (they fit without spills, and the inlined masked
+// path would otherwise leave room for only 2); the batched FP32 kernels would spill
+// under that cap and keep their allocation.
+template <class T, int N>
+constexpr int min_blocks() { return T::kBytes == 2 ? 2 : (N == 1 ? 3 : 1); }
 
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
@@ -149,9 +152,10 @@ __device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int
 // Tile cut by the fragment boundary or the matrix edge: loads a batch of rows at a
 // time (16-byte loads for chunks wholly inside the fragment, predicated per-element
 // loads otherwise), one scale byte per row and block, and stores only the
-// fragment's elements (a word per whole chunk when the output is aligned).
+// fragment's elements (a word per whole chunk when the output is aligned).  Inlined
+// into the kernel, as in the amax kernel.
 template <class T, bool kCol, bool kVec, int kModel>
-__device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0, int64_t col0,
+__device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t row0, int64_t col0,
                                               int lane) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
   const FragGeom& g = p.g;
@@ -208,7 +212,7 @@ __device__ __noinline__ void cast_tile_masked(const CastParams& p, int64_t row0,
 }
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-__global__ void __launch_bounds__(kThreads, min_blocks<T>()) k_partial_cast(
+__global__ void __launch_bounds__(kThreads, min_blocks<T, N>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
