@@ -26,6 +26,9 @@ import torch
 
 from . import api
 
+# NVTX range names of the step phases (the reduction range holds the fused scale update)
+_PHASE_NAMES = ("mxfp8.partial_amax", "mxfp8.max_reduce", "mxfp8.update_scales", "mxfp8.partial_cast")
+
 _ALIGN = 16
 
 
@@ -244,7 +247,10 @@ class ShardedCast:
             if events is not None:
                 events[0].record(torch_stream)
             for k, calls in enumerate(phases):
-                for c in calls:
-                    c.call(raw)
+                if calls:  # NVTX range per phase, for timeline profilers
+                    torch.cuda.nvtx.range_push(_PHASE_NAMES[k])
+                    for c in calls:
+                        c.call(raw)
+                    torch.cuda.nvtx.range_pop()
                 if events is not None:
                     events[k + 1].record(torch_stream)
