@@ -216,6 +216,16 @@ __device__ __forceinline__ uint32_t e4m3x2_rn_sat(float lo, float hi) {
   return r;
 }
 
+// Two FP32 products in one packed multiply (mul.rn.f32x2), each rounded to nearest as a
+// scalar multiply is; with a power-of-two multiplier the products are exact.
+__device__ __forceinline__ void mul2_rn(float a0, float a1, float b0, float b1, float& p0, float& p1) {
+  uint64_t x, y, z;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b0), "f"(b1));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(z) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(p0), "=f"(p1) : "l"(z));
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
@@ -275,11 +285,12 @@ __device__ __forceinline__ void model_values(const uint4& c, float (&y)[T::V]) {
 template <class T>
 __device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
   uint2 q;
-  q.x = e4m3x2_rn_sat(y[0] * mult[0], y[1] * mult[1]) |
-        (e4m3x2_rn_sat(y[2] * mult[2], y[3] * mult[3]) << 16);
+  float p[T::V];
+#pragma unroll
+  for (int k = 0; k < T::V; k += 2) mul2_rn(y[k], y[k + 1], mult[k], mult[k + 1], p[k], p[k + 1]);
+  q.x = e4m3x2_rn_sat(p[0], p[1]) | (e4m3x2_rn_sat(p[2], p[3]) << 16);
   if constexpr (T::V == 8) {
-    q.y = e4m3x2_rn_sat(y[4] * mult[4], y[5] * mult[5]) |
-          (e4m3x2_rn_sat(y[6] * mult[6], y[7] * mult[7]) << 16);
+    q.y = e4m3x2_rn_sat(p[4], p[5]) | (e4m3x2_rn_sat(p[6], p[7]) << 16);
   } else {
     q.y = 0;
   }
