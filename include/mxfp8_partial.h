@@ -25,6 +25,9 @@
  *   allocates, frees or keeps a pointer after the call returns.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream).  A return of 0 means "validated and launched".
+ *   Kernels are launched as programmatic dependents of the kernel before them in
+ *   the stream: they may be scheduled while that kernel's last blocks run, but
+ *   read and write nothing until it has completed, so stream order holds.
  * - Tensors are dense and row-major: a 2-D tensor's row stride is shape[1].
  * - An EMPTY handle (data == NULL, or any shape entry == 0, or a NULL handle
  *   pointer) means "this direction is absent" (section "Changes": omission uses
