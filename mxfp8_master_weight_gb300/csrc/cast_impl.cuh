@@ -31,11 +31,10 @@ constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 // Resident blocks per SM the register allocation must allow: 2 for BF16 input, whose
 // batched kernels would otherwise take 168 registers and run one block per SM; 3 for
-// the single-fragment FP32 kernels (they fit without spills, and the inlined masked
-// path would otherwise leave room for only 2); the batched FP32 kernels would spill
-// under that cap and keep their allocation.
+// FP32 (the single-fragment kernels fit without spills; the batched ones spill a few
+// dozen bytes to L1 and still run faster than at 2 blocks).
 template <class T, int N>
-constexpr int min_blocks() { return T::kBytes == 2 ? 2 : (N == 1 ? 3 : 1); }
+constexpr int min_blocks() { return T::kBytes == 2 ? 2 : 3; }
 
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
