@@ -29,12 +29,12 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
 constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
-// Resident blocks per SM the register allocation must allow: 2 for BF16 input, whose
-// batched kernels would otherwise take 168 registers and run one block per SM; 3 for
-// FP32 (the single-fragment kernels fit without spills; the batched ones spill a few
-// dozen bytes to L1 and still run faster than at 2 blocks).
-template <class T, int N>
-constexpr int min_blocks() { return T::kBytes == 2 ? 2 : 3; }
+// Resident blocks per SM the register allocation must allow (an unconstrained allocation
+// leaves room for 1-2): 3, where some variants then spill a few dozen bytes to L1 and
+// still run faster (FP32 config-5 cast phase -4 %, BF16 16384x6144 cast -4 %); 2 for the
+// BF16 kernels with unaligned outputs, whose piece stores spill more.
+template <class T, int N, bool kVec>
+constexpr int min_blocks() { return (T::kBytes == 2 && !kVec) ? 2 : 3; }
 
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
@@ -211,7 +211,7 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
 }
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-__global__ void __launch_bounds__(kThreads, min_blocks<T, N>()) k_partial_cast(
+__global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
