@@ -245,6 +245,16 @@ def test_max_reduce(oracle_mod):
                           wl.truncate_to_bf16_bits(s).view(np.uint16).max(axis=0))
 
 
+def test_max_reduce_nan_propagates(oracle_mod):
+    """A NaN in any slot makes the reduced entry NaN (so its E8M0 byte is 0xFF), in
+    whichever slot it sits and whatever the other slots hold."""
+    s = np.array([[np.nan, 1.0, 3.0, 0.0], [2.0, np.nan, 1.0, 0.5], [1.0, 5.0, np.nan, 0.25]],
+                 np.float32)
+    r = oracle_mod.max_reduce(s)
+    assert np.isnan(r[:3]).all() and r[3] == 0.5
+    assert (oracle_mod.e8m0_from_amax(r[:3].astype(np.float64)) == 0xFF).all()
+
+
 # ------------------------------------------------------------------ cast
 
 def _cast_brute(x_bf16_vals, scale_bytes):
