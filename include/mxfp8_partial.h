@@ -21,8 +21,9 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  * - Every pointer inside an mxfp8_tensor is a DEVICE pointer (global memory of
- *   the current CUDA device).  The caller owns all memory; the library never
- *   allocates, frees or keeps a pointer after the call returns.
+ *   the current CUDA device), or page-locked host memory that the device can
+ *   address directly (see mxfp8_device_can_access).  The caller owns all memory;
+ *   the library never allocates, frees or keeps a pointer after the call returns.
  * - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *   legacy default stream).  A return of 0 means "validated and launched".
  *   Kernels are launched as programmatic dependents of the kernel before them in
@@ -170,8 +171,9 @@ MXFP8_API int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* 
  * bidirectional batches).  Each job means exactly what the single-fragment call with
  * the same arguments means; the jobs are validated first (a failure launches nothing
  * and names the job), then run as few kernels as possible: jobs that share the input
- * dtype, the direction set and the alignment class go into one launch (at most 16 jobs
- * each), with the tiles of all jobs scheduled together.  Jobs may run concurrently:
+ * dtype, the model dtype and the alignment class go into one launch (at most 16 jobs
+ * each; row-only and bidirectional jobs together, each tile taking its job's
+ * specialisation), with the tiles of all jobs scheduled together.  Jobs may run concurrently:
  * jobs whose written entries overlap (two fragments of one weight writing the SAME
  * amax buffer, whose boundary blocks both jobs overwrite) race -- give each fragment
  * its own amax buffer, as a packed per-rank slot does.  Fragments of one weight write
