@@ -12,10 +12,16 @@ partial cast (three kernels).
 Prints ONE JSON line (rank 0).  `value` is whole-job HBM throughput in GB/s of
 algorithmic bytes (every kernel's compulsory reads and writes) with the input
 resident in device memory; `kernels` gives each kernel's CUDA-event time per
-call, GB/s and fraction of the measured HBM peak; `e2e` repeats the step with
-the input copied from pinned host memory and the outputs copied back inside the
-timed region.  `--impl reference` times the CPU oracle on a bounded sample of
-the same workload (the reference arm of this benchmark).
+call, GB/s and fraction of the measured HBM peak; `roofline` the dominant
+kernel against that peak (with the ncu DRAM traffic recorded for the current
+kernel code under profiles/); `e2e` repeats the step with the input copied from
+pinned host memory and the outputs copied back inside the timed region.  Outside
+the timed steps: `fused_whole_blocks` (the one-pass kernel on the same weight),
+`sharded_batch` (the multi-fragment driver on the config-5 batch in four
+emulated shards) and `other_configs` (configs 1-3 and the weight row-only, CUDA
+graphs of repeated calls, median of 7 rounds).  `--impl reference` times the CPU
+oracle on a bounded sample of the same workload (the reference arm of this
+benchmark).
 N > 1 (torchrun): every rank runs its own replica of the workload on its GPU.
 """
 from __future__ import annotations
