@@ -181,6 +181,26 @@ def barrier(world: int):
         dist.barrier()
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine type)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":", 1)[0].strip().lower() == "model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.split(":", 1)[0].strip().lower() in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
 def cpu_sample_run(data: np.ndarray, row0: int, rows: int):
     """Time the CPU oracle (as it stands, one thread) on rows [row0, row0+rows) of the
     workload (whole 32-row bands, so every block is complete): amax -> scales -> cast.
@@ -192,6 +212,48 @@ def cpu_sample_run(data: np.ndarray, row0: int, rows: int):
     dt = time.perf_counter() - t0
     b = algorithmic_bytes(rows * COLS)
     return dt, b["amax"] + b["scales"] + b["cast"]
+
+
+def _band_worker(args):
+    """Worker process: the unchanged oracle on rows [row0, row0 + rows) of the sample
+    file (memory-mapped); returns its seconds and algorithmic bytes."""
+    path, row0, rows, cols = args
+    import oracle
+    oracle.build()
+    data = np.load(path, mmap_mode="r")
+    x = np.ascontiguousarray(data[row0 * cols:(row0 + rows) * cols])
+    t0 = time.perf_counter()
+    oracle.full_cast(x, rows, cols, True)
+    dt = time.perf_counter() - t0
+    b = algorithmic_bytes(rows * cols)
+    return dt, b["amax"] + b["scales"] + b["cast"]
+
+
+def cpu_all_cores_run(data: np.ndarray, rows: int, procs: int):
+    """The oracle as it stands, run on every host core at once: the sample's 32-row bands
+    are split over `procs` worker processes (started with spawn, so they are safe after
+    CUDA use), each running the single-threaded oracle on its bands.  Returns (wall
+    seconds of the parallel run, algorithmic bytes, processes used)."""
+    import multiprocessing as mp
+    import tempfile
+
+    bands = rows // 32
+    procs = max(1, min(procs, bands))
+    per = [bands // procs + (1 if k < bands % procs else 0) for k in range(procs)]
+    with tempfile.TemporaryDirectory() as tmp:
+        path = os.path.join(tmp, "sample.npy")
+        np.save(path, np.ascontiguousarray(data[:rows * COLS]))
+        tasks, row0 = [], 0
+        for nb in per:
+            tasks.append((path, row0, nb * 32, COLS))
+            row0 += nb * 32
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(procs) as pool:
+            pool.map(_band_worker, [(path, 0, 32, COLS)] * procs)  # start and build first
+            t0 = time.perf_counter()
+            res = pool.map(_band_worker, tasks)
+            wall = time.perf_counter() - t0
+    return wall, sum(b for _, b in res), procs
 
 
 def run_reference(args):
@@ -471,7 +533,15 @@ def run_ours(args):
         dt, b = cpu_sample_run(w.data, 0, cpu_rows)
         cpu = {"value": b / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"first {cpu_rows} rows ({cpu_rows * COLS} elements) of the workload: "
-                         f"amax, scales, cast; {dt:.1f} s single-threaded"}
+                         f"amax, scales, cast; {dt:.1f} s single-threaded",
+               "cpu_model": cpu_model()}
+        try:
+            wall, pb, used = cpu_all_cores_run(w.data, cpu_rows, os.cpu_count() or 1)
+            cpu["all_cores"] = {"value": pb / wall / 1e9, "unit": "GB/s", "cores": used,
+                                "sample": f"the same rows in 32-row bands over {used} processes "
+                                          f"running the single-threaded oracle; {wall:.2f} s wall"}
+        except Exception as exc:  # the single-core figure stands on its own
+            cpu["all_cores"] = {"unavailable": f"{type(exc).__name__}: {exc}"[:200]}
 
     value = total_bytes / t_max / 1e9
     line = {

@@ -4,6 +4,7 @@ run as two gloo ranks on the CPU."""
 import os
 import socket
 
+import numpy as np
 import pytest
 import torch.multiprocessing as mp
 
@@ -72,3 +73,15 @@ def test_sharded_step_bytes():
     amax = n0 * 4 + 2 * n0 // 32 * 4 + n1 * 4 + n1 // 32 * 4
     cast = n0 * 4 + 2 * n0 // 32 + 2 * n0 + n1 * 4 + n1 // 32 + n1
     assert b == amax + cast + 2 * 1000 * 4 + 1000 * 4 + 1000
+
+
+def test_cpu_all_cores_run_matches_single_core_bytes():
+    """The all-cores oracle baseline splits whole 32-row bands over worker processes and
+    accounts for exactly the bytes of the single-threaded run of the same rows."""
+    rng = np.random.default_rng(0)
+    rows = 96
+    data = (rng.standard_normal(rows * bench.COLS) * 0.02).astype(np.float32)
+    wall, b, used = bench.cpu_all_cores_run(data, rows, 2)
+    _, b1 = bench.cpu_sample_run(data, 0, rows)
+    assert used == 2 and b == b1 and wall > 0
+    assert isinstance(bench.cpu_model(), str)
