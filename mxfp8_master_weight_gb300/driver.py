@@ -179,8 +179,9 @@ class ShardedCast:
 
     def launches_per_step(self) -> int:
         """Library kernel launches of one step: the batched amax and cast take one launch
-        per (direction set, alignment class) group of at most 16 fragments, the
-        reduction one, the batched scale update one per 32 block grids."""
+        per (dtype, alignment class) group of at most 16 fragments (row-only and
+        bidirectional fragments share launches), the reduction one, the batched scale
+        update (when not fused with the reduction) one per 32 block grids."""
         return self._launches if hasattr(self, "_launches") else -1
 
     def _check_shards(self, shards) -> None:

@@ -43,6 +43,9 @@ def test_cfg5_sharded_mixed_batch(scale):
     sc, shards = _run(batch)
     sc.step(shards)
     _check_against_full(batch, sc)
+    amax_calls, reduce_calls, scale_calls, cast_calls = sc._prepared(shards)
+    assert len(reduce_calls) == 1 and not scale_calls  # exactly one packed reduction per step
+    assert len(amax_calls) == 1 and len(cast_calls) == 1  # one batched call per phase
 
 
 def test_consecutive_updates_keep_pointers_and_match():
