@@ -52,6 +52,27 @@ MUTATIONS = {
         "(rr % 32) * 16 + (rr / 32) * 4 + cc", "(rr / 32) * 16 + (rr % 32) * 4 + cc"),
     "fp16 overflow threshold off by one unit": (
         "if (r > 65504.0) r = INFINITY;", "if (r >= 65504.0) r = INFINITY;"),
+    "fp16 ties away from zero": (
+        "    double r = nearbyint(a / quantum) * quantum;\n    if (r > 65504.0)",
+        "    double r = round(a / quantum) * quantum;\n    if (r > 65504.0)"),
+    "fp16 subnormal threshold off by one": (
+        "if (p < -14) p = -14;", "if (p < -15) p = -15;"),
+    "e4m3 subnormal spacing off by one": (
+        "int p = (a < ldexp(1.0, -6)) ? -6 : floor_log2(a);",
+        "int p = (a < ldexp(1.0, -7)) ? -7 : floor_log2(a);"),
+    "e4m3 decode exponent bias off by one": (
+        "else v = ldexp(1.0 + m / 8.0, e - 7);", "else v = ldexp(1.0 + m / 8.0, e - 8);"),
+    "infinite amax not mapped to the NaN scale": (
+        "if (isnan(amax) || isinf(amax)) return 0xFF;", "if (isnan(amax)) return 0xFF;"),
+    "NaN scale byte not special-cased in the cast": (
+        "if (s == 0xFF) return 0x7F;", "if (s == 0xFF) return 0x00;"),
+    "out_offset ignored by the cast": (
+        "int64_t o = out_offset + (k - start);", "int64_t o = (k - start);"),
+    "columnwise data scaled by the column's row-block scale index": (
+        "scale_c[(i / 32) * ld_sc + j]);", "scale_c[(i / 32) * ld_sc + j / 32 * 32]);"),
+    "amax column index shifted by one": (
+        "        int64_t i = k / cols, j = k % cols;\n        double a = fabs(",
+        "        int64_t i = k / cols, j = (k + 1) % cols;\n        double a = fabs("),
 }
 
 
