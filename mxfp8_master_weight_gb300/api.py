@@ -32,6 +32,21 @@ def device_can_access(t: torch.Tensor) -> bool:
     return bool(_capi.load().mxfp8_device_can_access(ctypes.c_void_p(t.data_ptr()), nbytes))
 
 
+def mxfp8_device_can_access(t: torch.Tensor) -> bool:
+    """The C entry of the same name for a tensor's storage (see device_can_access)."""
+    return device_can_access(t)
+
+
+def mxfp8_last_error() -> str:
+    """Message of the calling thread's most recent non-zero status ("" if none)."""
+    return _capi.load().mxfp8_last_error().decode(errors="replace")
+
+
+def mxfp8_version() -> int:
+    """Library version as major*10000 + minor*100 + patch."""
+    return int(_capi.load().mxfp8_version())
+
+
 def handle(t: torch.Tensor | None, name: str, allow_host: bool = False) -> Tensor:
     """mxfp8_tensor for a CUDA tensor; None / zero-element tensors give an empty handle.
     With ``allow_host``, a page-locked CPU tensor is accepted when the device can access

@@ -207,3 +207,11 @@ def test_code_digest_ignores_comments_only():
     assert build.code_text(a) == build.code_text(b)
     assert build.code_text(a) != build.code_text(c)
     assert len(build.source_digest()) == 64
+
+
+def test_python_binding_has_every_entry_point():
+    """The binding exposes a function of the same name for every C entry point."""
+    from mxfp8_master_weight_gb300 import api
+    missing = [n for n in _declared_symbols() if not callable(getattr(api, n, None))]
+    assert not missing, missing
+    assert api.mxfp8_version() >= 100 and isinstance(api.mxfp8_last_error(), str)
