@@ -215,3 +215,40 @@ def test_python_binding_has_every_entry_point():
     missing = [n for n in _declared_symbols() if not callable(getattr(api, n, None))]
     assert not missing, missing
     assert api.mxfp8_version() >= 100 and isinstance(api.mxfp8_last_error(), str)
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "mxfp8_partial.h"
+
+int main(void) {
+  float dummy[64];
+  mxfp8_tensor in = {dummy, MXFP8_DTYPE_F32, 1, {64, 0}};
+  mxfp8_tensor ar = {dummy, MXFP8_DTYPE_F32, 2, {2, 1}};
+  /* rows <= 0 is rejected during validation, before any device work */
+  int rc = mxfp8_partial_amax(&in, &ar, NULL, -1, 32, 0, NULL);
+  printf("version=%d status=%d error=%s\n", mxfp8_version(), rc, mxfp8_last_error());
+  return rc == MXFP8_ERR_INVALID && strlen(mxfp8_last_error()) > 0 ? 0 : 1;
+}
+"""
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """A plain C11 client compiles against include/mxfp8_partial.h, links the library,
+    and gets a validation status and message back without a GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(_capi.LIB_PATH)
+    subprocess.run([cc, "-std=c11", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    str(src), "-o", str(exe), "-L", libdir, "-l:" + os.path.basename(_capi.LIB_PATH),
+                    "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "status=1" in out.stdout and "rows and cols must be positive" in out.stdout
