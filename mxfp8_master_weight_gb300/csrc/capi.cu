@@ -596,7 +596,7 @@ int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor*
     if (int rc = prep_scales(jobs[k], segs, &nseg, &jdt)) return njobs > 1 ? job_fail(rc, k) : rc;
     if (jdt != (dt == MXFP8_DTYPE_F32 ? 0 : 1)) return job_fail(fail(MXFP8_ERR_DTYPE, "amax dtype differs from the slots"), k);
     for (int q = 0; q < nseg; ++q) {
-      int64_t b;
+      int64_t b = 0;
       if (!inside(segs[q], &b)) return job_fail(fail(MXFP8_ERR_INVALID, "amax view is not inside `reduced`"), k);
     }
   }
@@ -609,8 +609,8 @@ int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor*
     if (k < njobs) {
       prep_scales(jobs[k], segs, &nseg, &jdt);
       for (int q = 0; q < nseg; ++q) {
-        int64_t b;
-        inside(segs[q], &b);
+        int64_t b = 0;
+        inside(segs[q], &b);  // validated above: the view lies inside `reduced`
         ReduceScaleSegment& r = batch[n++];
         r = ReduceScaleSegment{};
         r.slot0 = static_cast<const char*>(slots->data) + b * eb;
