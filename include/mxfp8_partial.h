@@ -69,6 +69,8 @@ typedef struct {
   int64_t shape[2]; /* shape[1] ignored when ndim == 1                     */
 } mxfp8_tensor;
 
+/* Size limits of every entry point taking rows x cols: 1 <= cols <= 2^37 and
+ * rows * cols <= 2^40 elements; outside them the call returns MXFP8_ERR_INVALID. */
 enum {
   MXFP8_OK = 0,
   MXFP8_ERR_INVALID = 1,
@@ -98,7 +100,7 @@ enum {
  * (overwritten, not max-accumulated); every other entry keeps its value, so a
  * caller that reduces across fragments zeroes its buffers first.  An empty
  * fragment (len 0) writes nothing and returns 0.  NaN members make the entry NaN.
- * Errors: 1 if start_offset < 0, rows/cols <= 0, start_offset + len > rows*cols,
+ * Errors: 1 if start_offset < 0, rows/cols out of the size limits, start_offset + len > rows*cols,
  * or a pointer is not element-aligned; 2 on a too-small amax shape;
  * 3 if an amax dtype differs from the input dtype or the input is not F32/BF16;
  * 4 if amax_rowwise is empty (and len > 0).

@@ -85,9 +85,21 @@ int check_grid(const mxfp8_tensor* t, const char* name, int64_t r, int64_t c, in
   return MXFP8_OK;
 }
 
-int check_dims(int64_t rows, int64_t cols, int64_t start, int64_t len) {
+// Weight size limits: byte offsets of every element stay far inside int64 and a band's
+// warp-tile count, ceil(cols / tile width), fits the 32-bit count the kernels keep.
+// Both are far above what one device can hold.
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+constexpr int64_t kMaxCols = int64_t(1) << 37;
+
+int check_size(int64_t rows, int64_t cols) {
   if (rows <= 0 || cols <= 0) return fail(MXFP8_ERR_INVALID, "rows and cols must be positive");
-  if (rows > INT64_MAX / cols) return fail(MXFP8_ERR_INVALID, "rows*cols overflows int64");
+  if (cols > kMaxCols) return fail(MXFP8_ERR_INVALID, "cols exceeds 2^37");
+  if (rows > kMaxElems / cols) return fail(MXFP8_ERR_INVALID, "rows*cols exceeds 2^40 elements");
+  return MXFP8_OK;
+}
+
+int check_dims(int64_t rows, int64_t cols, int64_t start, int64_t len) {
+  if (int rc = check_size(rows, cols)) return rc;
   if (start < 0) return fail(MXFP8_ERR_INVALID, "start_offset must be non-negative");
   if (len < 0 || start > rows * cols - len)
     return fail(MXFP8_ERR_INVALID, "fragment [%lld, %lld) exceeds rows*cols = %lld", (long long)start,
@@ -306,8 +318,7 @@ int prep_fused(const mxfp8_quantize_job& job, FusedParams* p, int* dtype, bool* 
 
 int prep_scales(const mxfp8_scale_job& job, ScaleSegment* segs, int* nseg, int* dtype) {
   const int64_t rows = job.rows, cols = job.cols;
-  if (rows <= 0 || cols <= 0) return fail(MXFP8_ERR_INVALID, "rows and cols must be positive");
-  if (rows > INT64_MAX / cols) return fail(MXFP8_ERR_INVALID, "rows*cols overflows int64");
+  if (int rc = check_size(rows, cols)) return rc;
   if (is_empty(&job.amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
   if (is_empty(&job.scale_inv_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_inv_rowwise is required");
   const int32_t dt = job.amax_rowwise.dtype;

@@ -87,6 +87,11 @@ def test_amax_validation(lib):
     ar = T(P, F32, 64, 2)
     ac = T(P, F32, 2, 64)
     assert amax(lib, inp, ar, ac, 0, 64, 0) == 1                 # rows must be positive
+    assert amax(lib, inp, ar, ac, 1, 2 ** 37 + 1, 0) == 1        # one row past the column limit
+    assert b"2^37" in lib.mxfp8_last_error()
+    assert amax(lib, inp, ar, ac, 2 ** 21, 2 ** 19 + 32, 0) == 1  # past 2^40 elements
+    assert b"2^40" in lib.mxfp8_last_error()
+    assert amax(lib, inp, ar, ac, 2 ** 62, 2 ** 3, 0) == 1       # rows*cols would overflow int64
     assert amax(lib, inp, ar, ac, 64, 64, -1) == 1               # negative start
     assert amax(lib, inp, ar, ac, 64, 64, 64 * 64 - 99) == 1     # fragment past the end
     assert b"exceeds" in lib.mxfp8_last_error()
@@ -143,6 +148,7 @@ def test_scales_and_reduce_validation(lib):
     sr = T(P, U8, 64, 2)
     sc = T(P, U8, 2, 64)
     up = lib.mxfp8_update_scales
+    assert up(ctypes.byref(ar), ctypes.byref(ac), ctypes.byref(sr), ctypes.byref(sc), 2 ** 40, 2, None) == 1
     assert up(ctypes.byref(ar), ctypes.byref(ac), ctypes.byref(sr), ctypes.byref(E()), 64, 64, None) == 4
     assert up(ctypes.byref(E()), ctypes.byref(ac), ctypes.byref(sr), ctypes.byref(sc), 64, 64, None) == 4
     assert up(ctypes.byref(ar), ctypes.byref(ac), ctypes.byref(T(P, U8, 64, 1)), ctypes.byref(sc), 64, 64, None) == 2
