@@ -23,7 +23,8 @@ def lib():
 def _declared_symbols():
     names = set()
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
-        text = open(h).read()
+        with open(h) as f:
+            text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
         names.update(re.findall(r"^\s*(?:MXFP8_API\s+)?(?:const\s+)?\w+\s*\*?\s*(mxfp8_\w+)\s*\(",
                                 text, flags=re.M))
