@@ -76,7 +76,8 @@ def test_scale_update_patterns(dtype):
     ad = to_device(a).view(a.shape)
     s = torch.zeros(a.shape, dtype=torch.uint8, device="cuda")
     api.mxfp8_update_scales(ad, None, s, None, rows, cols)
-    want = oracle.e8m0_from_amax(np.abs(af.astype(np.float64)))
+    with np.errstate(invalid="ignore"):  # the patterns include signalling NaNs
+        want = oracle.e8m0_from_amax(np.abs(af.astype(np.float64)))
     assert np.array_equal(to_host(s), want)
 
 
