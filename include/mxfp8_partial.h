@@ -99,7 +99,9 @@ enum {
  * Only entries of blocks that contain at least one fragment element are written
  * (overwritten, not max-accumulated); every other entry keeps its value, so a
  * caller that reduces across fragments zeroes its buffers first.  An empty
- * fragment (len 0) writes nothing and returns 0.  NaN members make the entry NaN.
+ * fragment (len 0) writes nothing and returns 0.  NaN members make the entry NaN,
+ * stored as the canonical quiet NaN (F32 0x7FC00000, BF16 0x7FC0) whatever their
+ * NaN patterns.
  * Errors: 1 if start_offset < 0, rows/cols out of the size limits, start_offset + len > rows*cols,
  * or a pointer is not element-aligned; 2 on a too-small amax shape;
  * 3 if an amax dtype differs from the input dtype or the input is not F32/BF16;
@@ -116,7 +118,8 @@ MXFP8_API int mxfp8_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_r
  *
  * slots  [in]  2-D [S][E] F32 or BF16: S packed amax buffers of E entries each.
  * out    [out] E entries (any shape with numel == E), same dtype.
- * out[k] = max over s of |slots[s][k]|; NaN propagates.  S == 1 copies |.|.
+ * out[k] = max over s of |slots[s][k]|; NaN propagates as the canonical quiet NaN
+ * (F32 0x7FC00000, BF16 0x7FC0).  S == 1 copies |.|.
  * out may not overlap slots.  Errors: 2 numel mismatch, 3 dtype, 4 empty out.
  */
 MXFP8_API int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* stream);
@@ -326,7 +329,8 @@ MXFP8_API int mxfp8_device_can_access(const void* ptr, int64_t bytes);
  *
  * fragments[f]      [in]  fragment f of the rows x cols weight (F32 or BF16, one dtype
  *                         for all; empty fragments are skipped), starting at flat
- *                         element start_offsets[f].  Fragments must not overlap.
+ *                         element start_offsets[f].  Fragments must not overlap
+ *                         (status 1 when two non-empty fragments do).
  * scale_inv_rowwise [out] REQUIRED U8 [>= rows][>= ceil(cols/32)].
  * scale_inv_colwise [out] U8 [>= ceil(rows/32)][>= cols]; required iff output_colwise.
  * output_rowwise    [out] REQUIRED U8, full size (rows*cols), written where the
@@ -338,8 +342,10 @@ MXFP8_API int mxfp8_device_can_access(const void* ptr, int64_t bytes);
  * Limits: 1..64 fragments and (nfrags + 1) amax slots of rows*ceil(cols/32) (+
  * ceil(rows/32)*cols when columnwise) entries, each rounded up to 256 bytes, within
  * the 64 MiB; a larger request fails with status 2 and a message giving the bytes
- * needed.  The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  Every call uses
+ * needed.  Every argument is checked before anything is launched: a non-zero status
+ * leaves every caller buffer untouched.  The first call on a device looks up the
+ * array's device address (with that device current); make that first call before any
+ * stream capture.  Every call uses
  * the same array and leaves its contents behind (slots are cleared at the start of
  * each call); calls that overlap on the GPU -- on different streams or from
  * different threads -- race on it.

@@ -22,7 +22,8 @@ EXPORTED = ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales"
             "mxfp8_partial_cast_batched", "mxfp8_quantize_whole_blocks",
             "mxfp8_quantize_whole_blocks_batched", "mxfp8_swizzle_scales",
             "mxfp8_swizzled_scales_size", "mxfp8_device_can_access",
-            "mxfp8_amax_max_reduce_update_scales", "mxfp8_last_error", "mxfp8_version")
+            "mxfp8_amax_max_reduce_update_scales", "mxfp8_sharded_update_noalloc",
+            "mxfp8_last_error", "mxfp8_version")
 
 
 class Tensor(ctypes.Structure):

@@ -44,11 +44,12 @@ template <class T, bool kCol>
 __device__ __forceinline__ void store_colmax(const AmaxParams& p, int64_t row0, int64_t j,
                                              const uint4& colmax) {
   const int64_t base = (row0 >> 5) * p.ld_c + j;
+  const uint4 out = canonical_nan_chunk<T>(colmax);
   if (p.vec_c) {
-    *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = colmax;
+    *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = out;
   } else {
 #pragma unroll
-    for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(colmax, k));
+    for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(out, k));
   }
 }
 
@@ -72,7 +73,7 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);
-      if (writer) store_bits<T>(p.amax_r, out_r + (rb + r) * p.ld_r, m);
+      if (writer) store_bits<T>(p.amax_r, out_r + (rb + r) * p.ld_r, canonical_nan<T>(m));
     }
   }
   if constexpr (kCol) store_colmax<T, kCol>(p, row0, j, colmax);
@@ -111,7 +112,7 @@ __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t ro
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);
       const int64_t i = row0 + rb + r;
       if (writer && i < g.rows && b0 < g.cols && row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1)))
-        store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), m);
+        store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), canonical_nan<T>(m));
     }
   }
   if constexpr (kCol) {
@@ -120,7 +121,7 @@ __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t ro
     for (int k = 0; k < T::V; ++k) {
       const int64_t col = j + k;
       if (col < g.cols && column_meets(g, col, row0, r_end))
-        store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, chunk_get<T>(colmax, k));
+        store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, canonical_nan<T>(chunk_get<T>(colmax, k)));
     }
   }
 }

@@ -528,6 +528,16 @@ const mxfp8_tensor& or_empty(const mxfp8_tensor* t) { return t ? *t : kEmpty; }
 
 namespace mxfp8 {
 int report_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
+int validate_cast_jobs(const mxfp8_cast_job* jobs, int njobs) {
+  CastParams p;
+  int dt;
+  bool col, skip;
+  for (int k = 0; k < njobs; ++k) {
+    if (int rc = prep_cast(jobs[k], &p, &dt, &col, &skip)) return njobs > 1 ? job_fail(rc, k) : rc;
+  }
+  return MXFP8_OK;
+}
 }  // namespace mxfp8
 
 extern "C" {

@@ -177,6 +177,37 @@ __device__ __forceinline__ uint32_t chunk_reduce(const uint4& c) {
   }
 }
 
+// A NaN amax is stored as the canonical quiet NaN (FP32 0x7FC00000, BF16 0x7FC0),
+// whatever NaN pattern the block's members carried: the bit-pattern maxima above keep
+// the largest member pattern, so each stored amax passes through these first.
+// One element (a BF16 value in the low 16 bits):
+template <class T>
+__device__ __forceinline__ uint32_t canonical_nan(uint32_t m) {
+  if constexpr (T::kBytes == 4) {
+    return m > 0x7f800000u ? 0x7fc00000u : m;
+  } else {
+    return m > 0x7f80u ? 0x7fc0u : m;
+  }
+}
+
+// Every element of a chunk of |x| bit patterns.
+template <class T>
+__device__ __forceinline__ uint4 canonical_nan_chunk(uint4 c) {
+  if constexpr (T::kBytes == 4) {
+    c.x = canonical_nan<T>(c.x); c.y = canonical_nan<T>(c.y);
+    c.z = canonical_nan<T>(c.z); c.w = canonical_nan<T>(c.w);
+  } else {
+    // per 16-bit half: 0xffff where the half is a NaN, then select the canonical pattern
+    uint32_t* w[4] = {&c.x, &c.y, &c.z, &c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t nan = __vcmpgtu2(*w[k], 0x7f807f80u);
+      *w[k] = (*w[k] & ~nan) | (0x7fc07fc0u & nan);
+    }
+  }
+  return c;
+}
+
 // Max over the G lanes that hold one 32-element row block (aligned lane groups).
 template <class T>
 __device__ __forceinline__ uint32_t group_max(uint32_t m) {

@@ -53,11 +53,12 @@ __device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t ro
   }
   if (p.amax_c != nullptr) {
     const int64_t base = band * p.ld_c + j;
+    const uint4 out = canonical_nan_chunk<T>(colmax);
     if (p.vec_c) {
-      *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = colmax;
+      *reinterpret_cast<uint4*>(static_cast<char*>(p.amax_c) + base * T::kBytes) = out;
     } else {
 #pragma unroll
-      for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(colmax, k));
+      for (int k = 0; k < T::V; ++k) store_bits<T>(p.amax_c, base + k, chunk_get<T>(out, k));
     }
   }
   uint8_t* dst = p.s_c + band * p.ld_sc + j;
@@ -105,7 +106,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
         const uint32_t e = e8m0_from_bits<T>(m);
         rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
         p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
-        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, m);
+        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, canonical_nan<T>(m));
       }
     }
   }
@@ -176,7 +177,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       if (writer && i < g.rows && b0 < g.cols &&
           row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1))) {
         p.s_r[i * p.ld_sr + (b0 >> 5)] = static_cast<uint8_t>(e);
-        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), m);
+        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + (b0 >> 5), canonical_nan<T>(m));
       }
     }
   }
@@ -191,7 +192,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       mc[k] = scale_multiplier(e);
       if (col < g.cols && column_meets(g, col, row0, r_end)) {
         p.s_c[(row0 >> 5) * p.ld_sc + col] = static_cast<uint8_t>(e);
-        if (p.amax_c != nullptr) store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, m);
+        if (p.amax_c != nullptr) store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, canonical_nan<T>(m));
       }
     }
   }

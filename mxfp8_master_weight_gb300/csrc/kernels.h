@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "mxfp8_partial.h"
+
 namespace mxfp8 {
 
 // Geometry of one fragment [start, end) of a rows x cols row-major weight, and
@@ -194,6 +196,10 @@ cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, 
 // Record `msg` as the calling thread's last error (returned by mxfp8_last_error) and
 // return `code`.  For entry points defined outside capi.cu.
 int report_error(int code, const char* msg);
+
+// Validate cast jobs exactly as mxfp8_partial_cast_batched does, without launching
+// anything (status and last-error message as that entry point would give them).
+int validate_cast_jobs(const mxfp8_cast_job* jobs, int njobs);
 
 // Tile width (columns per warp tile) for a dtype.
 inline int tile_width_for(int dtype) { return dtype == 0 ? 128 : 256; }

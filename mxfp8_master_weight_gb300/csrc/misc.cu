@@ -6,7 +6,8 @@
 // scale convention e = floor(log2 amax) - 8 clamped to [-127, 127].
 //
 // Packed MAX reduction: the page's single packed-amax MAX all-reduce, with the
-// ranks emulated as S slots of one device buffer: out[k] = max_s |slot_s[k]|.
+// ranks emulated as S slots of one device buffer: out[k] = max_s |slot_s[k]|; a NaN
+// result is stored as the canonical quiet NaN.
 // GEMM scale layout: the E8M0 grid (or its transpose) padded to 128 x 4 and cut into
 // 128x4 tiles of 512 bytes in row-major tile order; inside a tile element (r, c) sits
 // at (r % 32) * 16 + (r / 32) * 4 + c -- the layout block-scaled tensor-core GEMMs
@@ -103,6 +104,8 @@ __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
       for (int u = 0; u < U; ++u) {
         const int64_t q = q0 + u * stride;
         if (q >= quads) break;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) m[u][k] = canonical_nan<T>(m[u][k]);
         if constexpr (T::kBytes == 4) {
           reinterpret_cast<uint4*>(s.reduced)[q] = make_uint4(m[u][0], m[u][1], m[u][2], m[u][3]);
         } else {
@@ -120,6 +123,7 @@ __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
       const int64_t idx = r * s.ld_a + c;
       uint32_t m = 0;
       for (int k = 0; k < s.nslots; ++k) m = max(m, load_bits<T>(s.slot0, k * s.slot_stride + idx) & kAbs);
+      m = canonical_nan<T>(m);
       store_bits<T>(s.reduced, idx, m);
       s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(m));
     }
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict_
       uint4 m = make_uint4(0u, 0u, 0u, 0u);
       for (int s = 0; s < nslots; ++s)
         m = chunk_max<T>(m, chunk_abs<T>(ld_stream16(base + s * slot_bytes + q * 16)));
-      reinterpret_cast<uint4*>(out)[q] = m;
+      reinterpret_cast<uint4*>(out)[q] = canonical_nan_chunk<T>(m);
     }
   } else {
     for (int64_t e = tid; e < elems; e += stride) {
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(kThreads) k_max_reduce(const void* __restrict_
         const uint32_t a = load_bits<T>(slots, s * elems + e) & (T::kBytes == 4 ? 0x7fffffffu : 0x7fffu);
         m = max(m, a);
       }
-      store_bits<T>(out, e, m);
+      store_bits<T>(out, e, canonical_nan<T>(m));
     }
   }
 }

@@ -50,6 +50,10 @@ bool empty(const mxfp8_tensor* t) {
   return t->shape[0] == 0 || t->shape[1] == 0;
 }
 
+int64_t numel_of(const mxfp8_tensor* t) {
+  return t->ndim == 1 ? t->shape[0] : t->shape[0] * t->shape[1];
+}
+
 mxfp8_tensor view(void* base, int32_t dtype, int64_t r, int64_t c) {
   mxfp8_tensor t;
   t.data = base;
@@ -79,6 +83,8 @@ extern "C" int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments,
                                             mxfp8_tensor* output_rowwise,
                                             mxfp8_tensor* output_colwise, int64_t rows,
                                             int64_t cols, void* stream) {
+  // Everything is checked on the host before the first launch: a non-zero status
+  // leaves every caller buffer as it was.
   if (nfrags < 1 || nfrags > kMaxFragments || fragments == nullptr || start_offsets == nullptr)
     return mxfp8::report_error(MXFP8_ERR_INVALID, "need 1 to 64 fragments and their start offsets");
   if (rows <= 0 || cols <= 0 || rows > (int64_t(1) << 40) / cols)
@@ -93,6 +99,47 @@ extern "C" int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments,
     dtype = fragments[f].dtype;
   }
   if (dtype < 0) return MXFP8_OK;  // every fragment empty: nothing to do
+
+  // every fragment's cast, validated as mxfp8_partial_cast_batched would (this covers
+  // the fragments' extents, the scale grids and the outputs)
+  const mxfp8_tensor none = none_tensor();
+  mxfp8_cast_job cast_jobs[kMaxFragments];
+  for (int f = 0; f < nfrags; ++f) {
+    mxfp8_cast_job& j = cast_jobs[f];
+    j.input = fragments[f];
+    j.scale_inv_rowwise = scale_inv_rowwise ? *scale_inv_rowwise : none;
+    j.scale_inv_colwise = scale_inv_colwise ? *scale_inv_colwise : none;
+    j.output_rowwise = output_rowwise ? *output_rowwise : none;
+    j.output_colwise = output_colwise ? *output_colwise : none;
+    j.rows = rows;
+    j.cols = cols;
+    j.start_offset = start_offsets[f];
+    j.out_offset = start_offsets[f];
+    j.model_dtype = MXFP8_MODEL_BF16;
+  }
+  if (int rc = mxfp8::validate_cast_jobs(cast_jobs, nfrags)) return rc;
+
+  // fragments may not overlap: two casts would race on the same output bytes
+  int order[kMaxFragments];
+  int live = 0;
+  for (int f = 0; f < nfrags; ++f) {
+    if (empty(&fragments[f])) continue;
+    int k = live++;
+    while (k > 0 && start_offsets[order[k - 1]] > start_offsets[f]) {
+      order[k] = order[k - 1];
+      --k;
+    }
+    order[k] = f;
+  }
+  for (int k = 0; k + 1 < live; ++k) {
+    const int a = order[k], b = order[k + 1];
+    if (start_offsets[a] + numel_of(&fragments[a]) > start_offsets[b]) {
+      char msg[160];
+      std::snprintf(msg, sizeof msg, "fragments %d and %d overlap", a, b);
+      return mxfp8::report_error(MXFP8_ERR_INVALID, msg);
+    }
+  }
+
   const bool colwise = !empty(output_colwise);
   const int64_t eb = dtype == MXFP8_DTYPE_F32 ? 4 : 2;
   const int64_t nbr = (cols + 31) / 32, nbc = (rows + 31) / 32;
@@ -142,20 +189,5 @@ extern "C" int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments,
     return rc;
 
   // 4. every fragment's cast into the full-size outputs
-  const mxfp8_tensor none = none_tensor();
-  mxfp8_cast_job cast_jobs[kMaxFragments];
-  for (int f = 0; f < nfrags; ++f) {
-    mxfp8_cast_job& j = cast_jobs[f];
-    j.input = fragments[f];
-    j.scale_inv_rowwise = scale_inv_rowwise ? *scale_inv_rowwise : none;
-    j.scale_inv_colwise = scale_inv_colwise ? *scale_inv_colwise : none;
-    j.output_rowwise = output_rowwise ? *output_rowwise : none;
-    j.output_colwise = output_colwise ? *output_colwise : none;
-    j.rows = rows;
-    j.cols = cols;
-    j.start_offset = start_offsets[f];
-    j.out_offset = start_offsets[f];
-    j.model_dtype = MXFP8_MODEL_BF16;
-  }
   return mxfp8_partial_cast_batched(cast_jobs, nfrags, stream);
 }

@@ -29,9 +29,11 @@
  * amax 0 -> e = -127; stored as the biased E8M0 byte e + 127; the data byte is
  * E4M3 (bias 7, max 448, no infinities) of y * 2^-e, y = master value rounded
  * to BF16 (nearest, ties to even), with round-to-nearest-even and saturation
- * to +-448.  Non-finite handling (not a parity target of any workload): a NaN
- * or infinite amax gives scale byte 0xFF; a scale byte 0xFF casts every element
- * of its block to 0x7F; a NaN value casts to 0x7F; an infinite value saturates.
+ * to +-448.  Non-finite handling (not a parity target of any workload): a block
+ * with a NaN member has a NaN amax, stored as the canonical quiet NaN whatever
+ * the members' NaN payloads; a NaN or infinite amax gives scale byte 0xFF; a
+ * scale byte 0xFF casts every element of its block to 0x7F; a NaN value casts to
+ * 0x7F; an infinite value saturates.
  *
  * dtype codes: 0 = FP32 (float), 1 = BF16 (uint16_t bit patterns).
  */
@@ -59,15 +61,20 @@ static double load_value(const void *buf, int dtype, int64_t k) {
     }
 }
 
-/* Store a double that is exactly representable in the dtype (amax values are). */
+/* Store a double that is exactly representable in the dtype (amax values are).
+ * A NaN amax is stored as the canonical quiet NaN: FP32 bits 0x7FC00000, BF16
+ * bits 0x7FC0 (the pages print no NaN rule; one fixed pattern is the plainest). */
 static void store_value(void *buf, int dtype, int64_t k, double v) {
-    float f = (float)v;
-    if (isnan(v)) f = NAN;
-    if (dtype == ORACLE_F32) {
-        ((float *)buf)[k] = f;
+    uint32_t bits;
+    if (isnan(v)) {
+        bits = 0x7FC00000u;
     } else {
-        uint32_t bits;
+        float f = (float)v;
         memcpy(&bits, &f, sizeof bits);
+    }
+    if (dtype == ORACLE_F32) {
+        memcpy((char *)buf + 4 * k, &bits, sizeof bits);
+    } else {
         ((uint16_t *)buf)[k] = (uint16_t)(bits >> 16);
     }
 }

@@ -37,17 +37,20 @@ def torch_dtype(x: np.ndarray):
 
 def gpu_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bool, *,
                  out_offset: int | None = None, out_size: int | None = None, shift: int = 0,
-                 pad: int = 0, amax_fill: float = 0.0, sentinel: int = 0xA5, model: str = "bf16"):
+                 pad: int = 0, pad_s: int | None = None, amax_fill: float = 0.0,
+                 sentinel: int = 0xA5, model: str = "bf16"):
     """amax -> scales -> cast of one fragment on the GPU.  Returns host arrays
-    (amax_r, amax_c, scale_r, scale_c, q_r, q_c); columnwise items None when absent."""
+    (amax_r, amax_c, scale_r, scale_c, q_r, q_c); columnwise items None when absent.
+    `pad` extra columns pad the amax grids, `pad_s` (default `pad`) the scale grids."""
+    pad_s = pad if pad_s is None else pad_s
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
     dt = torch_dtype(frag)
     x = to_device(frag, shift)
     ar = torch.full((rr, rc + pad), amax_fill, dtype=dt, device="cuda")
     ac = torch.full((cr, cc + pad), amax_fill, dtype=dt, device="cuda") if colwise else None
     api.mxfp8_partial_amax(x, ar, ac, rows, cols, start)
-    sr = torch.full((rr, rc + pad), 0xEE, dtype=torch.uint8, device="cuda")
-    sc = torch.full((cr, cc + pad), 0xEE, dtype=torch.uint8, device="cuda") if colwise else None
+    sr = torch.full((rr, rc + pad_s), 0xEE, dtype=torch.uint8, device="cuda")
+    sc = torch.full((cr, cc + pad_s), 0xEE, dtype=torch.uint8, device="cuda") if colwise else None
     api.mxfp8_update_scales(ar, ac, sr, sc, rows, cols)
     if out_offset is None:
         out_offset = start
@@ -63,8 +66,10 @@ def gpu_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bo
 
 def oracle_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise: bool, *,
                     out_offset: int | None = None, out_size: int | None = None, pad: int = 0,
-                    amax_fill: float = 0.0, sentinel: int = 0xA5, model: str = "bf16"):
+                    pad_s: int | None = None, amax_fill: float = 0.0, sentinel: int = 0xA5,
+                    model: str = "bf16"):
     """The same step sequence on the CPU oracle."""
+    pad_s = pad if pad_s is None else pad_s
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
     npdt = frag.dtype
     fill = np.array([amax_fill], np.float32)
@@ -73,11 +78,11 @@ def oracle_fragment(frag: np.ndarray, rows: int, cols: int, start: int, colwise:
     ar = np.full((rr, rc + pad), fill[0], npdt)
     ac = np.full((cr, cc + pad), fill[0], npdt) if colwise else None
     oracle.partial_amax(frag, rows, cols, start, ar, ac)
-    sr = np.full((rr, rc + pad), 0xEE, np.uint8)
+    sr = np.full((rr, rc + pad_s), 0xEE, np.uint8)
     oracle.update_scales(ar, rr, rc, sr)
     sc = None
     if colwise:
-        sc = np.full((cr, cc + pad), 0xEE, np.uint8)
+        sc = np.full((cr, cc + pad_s), 0xEE, np.uint8)
         oracle.update_scales(ac, cr, cc, sc)
     if out_offset is None:
         out_offset = start

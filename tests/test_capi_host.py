@@ -259,3 +259,38 @@ def test_header_compiles_as_c_and_links(lib, tmp_path):
     out = subprocess.run([str(exe)], capture_output=True, text=True)
     assert out.returncode == 0, out.stdout + out.stderr
     assert "status=1" in out.stdout and "rows and cols must be positive" in out.stdout
+
+
+def test_noalloc_refuses_bad_arguments_before_any_device_work(lib):
+    """The allocation-free sharded update checks every argument on the host before it
+    touches a device: overlapping fragments, a missing or too small output, columnwise
+    output without columnwise scales -- all refused here, on a host without a GPU (a
+    call that got as far as the device would fail with status 6 instead)."""
+    fn = lib.mxfp8_sharded_update_noalloc
+    TP = ctypes.POINTER(_capi.Tensor)
+    fn.argtypes = [TP, ctypes.POINTER(ctypes.c_int64), ctypes.c_int32, TP, TP, TP, TP,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    rows, cols = 64, 64
+    sr, sc = T(P, U8, 64, 2), T(P, U8, 2, 64)
+    q = T(P, U8, 64 * 64)
+
+    def call(frags, starts, sr_, sc_, qr_, qc_):
+        arr = (_capi.Tensor * len(frags))(*frags)
+        st = (ctypes.c_int64 * len(starts))(*starts)
+        return fn(arr, st, len(frags), *[ctypes.byref(t) for t in (sr_, sc_, qr_, qc_)],
+                  rows, cols, None)
+
+    two = [T(P, F32, 2048), T(P + 8192, F32, 2048)]
+    assert call([T(P, F32, 2048), T(P + 8192, F32, 2049)], [0, 2047], sr, sc, q, q) == 1
+    assert b"overlap" in lib.mxfp8_last_error()
+    assert call([T(P, F32, 100), E(), T(P + 8192, F32, 10)], [200, 0, 250], sr, sc, q, q) == 1
+    assert b"fragments 0 and 2 overlap" in lib.mxfp8_last_error()
+    assert call(two, [0, 2048], sr, sc, E(), q) == 4                 # rowwise output required
+    assert call(two, [0, 2048], sr, E(), q, q) == 4                  # colwise output needs scales
+    assert b"scale_inv_colwise" in lib.mxfp8_last_error()
+    assert call(two, [0, 2048], E(), sc, q, q) == 4                  # rowwise scales required
+    assert call(two, [0, 2048], sr, sc, T(P, U8, 100), q) == 2       # output too small
+    assert call(two, [0, 3000], sr, sc, q, q) == 1                   # fragment past the end
+    assert call([T(P, F32, 2048), T(P + 8192, BF16, 2048)], [0, 2048], sr, sc, q, q) == 3
+    assert call([E(), E()], [0, 0], sr, sc, q, q) == 0              # nothing to do

@@ -8,7 +8,7 @@ import torch
 from mxfp8_master_weight_gb300 import _capi, api
 from mxfp8_master_weight_gb300 import workloads as wl
 
-from flows import gpu_fragment, to_device, to_host
+from flows import assert_bitwise, gpu_fragment, oracle_fragment, to_device, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -93,6 +93,10 @@ def test_library_is_the_in_tree_build():
     assert lib.mxfp8_version() >= 100
 
 
+# NaN patterns a block may hold: signalling, quiet, with payload, negative
+NAN_F32_PATTERNS = (0x7F800001, 0x7FBFFFFF, 0x7FC00000, 0x7FFFFFFF, 0xFFC00000, 0xFF800001)
+
+
 def test_special_values_follow_stated_conventions():
     """NaN / Inf in a block: amax NaN or Inf -> scale 0xFF -> block bytes 0x7F."""
     x = np.zeros(64, np.float32)
@@ -102,6 +106,40 @@ def test_special_values_follow_stated_conventions():
     assert np.isnan(got[0][0, 0]) and np.isinf(got[0][0, 1])
     assert got[2][0, 0] == 0xFF and got[2][0, 1] == 0xFF
     assert np.all(got[4] == 0x7F)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_nan_amax_bits_match_the_oracle(dtype):
+    """Every NaN pattern in a block gives the same amax bits as the oracle (the canonical
+    quiet NaN), in both directions, through the split and the one-pass paths."""
+    rows, cols = 64, 256
+    rng = np.random.default_rng(31)
+    x = wl.normal_f32(rng, rows * cols)
+    bits = x.view(np.uint32)
+    for k, pat in enumerate(NAN_F32_PATTERNS):  # one NaN per row block, spread over rows
+        bits[(7 * k) * cols + 32 * k + 3] = pat
+    if dtype == "bf16":
+        hb = (bits >> 16).astype(np.uint16)
+        for k, pat in enumerate(NAN_F32_PATTERNS):
+            i = (7 * k) * cols + 32 * k + 3
+            hb[i] = (pat >> 16) | (0 if (pat >> 16) & 0x7F else 0x40)  # stays a NaN
+        x = hb
+    got = gpu_fragment(x, rows, cols, 0, True)
+    want = oracle_fragment(x, rows, cols, 0, True)
+    assert_bitwise(got, want, f"{dtype} NaN patterns")
+    # the one-pass path writes the same amaxes
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    dt = torch.float32 if dtype == "f32" else torch.bfloat16
+    xd = to_device(x)
+    ar = torch.zeros((rr, rc), dtype=dt, device="cuda")
+    ac = torch.zeros((cr, cc), dtype=dt, device="cuda")
+    sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
+    sc = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda")
+    qr = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    qc = torch.zeros(rows * cols, dtype=torch.uint8, device="cuda")
+    api.mxfp8_quantize_whole_blocks(xd, ar, ac, sr, sc, qr, qc, rows, cols, 0)
+    torch.cuda.synchronize()
+    assert_bitwise([to_host(t) for t in (ar, ac, sr, sc, qr, qc)], want, f"{dtype} one-pass")
 
 
 def test_kernels_see_the_writes_of_the_kernel_before_them():

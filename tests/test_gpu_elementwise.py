@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from mxfp8_master_weight_gb300 import api
+from mxfp8_master_weight_gb300 import workloads as wl
 
 from flows import assert_bitwise, to_device, to_host
 
@@ -93,6 +94,35 @@ def test_max_reduce(dtype, nslots, elems):
     out = torch.empty(elems, dtype=d.dtype, device="cuda")
     api.mxfp8_amax_max_reduce(d, out)
     assert np.array_equal(to_host(out), oracle.max_reduce(x))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_max_reduce_nan_bits_match_the_oracle(dtype):
+    """NaN patterns of every kind in the slots reduce to the oracle's bits (the canonical
+    quiet NaN), through the plain reduction and the reduction fused with the scales."""
+    pats = (0x7F800001, 0x7FBFFFFF, 0x7FC00000, 0x7FFFFFFF, 0xFFC00000, 0xFF800001)
+    rng = np.random.default_rng(12)
+    x = wl.normal_f32(rng, (3, 256))
+    for k, p in enumerate(pats):
+        x.view(np.uint32)[k % 3, 8 * k + 1] = p
+    if dtype == "bf16":
+        hb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        for k, p in enumerate(pats):
+            hb[k % 3, 8 * k + 1] = (p >> 16) | (0 if (p >> 16) & 0x7F else 0x40)
+        x = hb
+    want = oracle.max_reduce(x)
+    d = to_device(x).view(3, 256)
+    out = torch.empty(256, dtype=d.dtype, device="cuda")
+    api.mxfp8_amax_max_reduce(d, out)
+    assert np.array_equal(to_host(out), want)
+    # fused with the scale update: the reduced buffer viewed as an 8x32 amax grid
+    red = torch.empty(256, dtype=d.dtype, device="cuda")
+    sr = torch.empty((8, 32), dtype=torch.uint8, device="cuda")
+    api.mxfp8_amax_max_reduce_update_scales(d, red, [(red.view(8, 32), None, sr, None, 8, 1024)])
+    torch.cuda.synchronize()
+    assert np.array_equal(to_host(red), want)
+    wf = want.astype(np.float32) if dtype == "f32" else wl.bf16_bits_to_f32(want)
+    assert np.array_equal(sr.cpu().numpy().reshape(-1), oracle.e8m0_from_amax(wf.astype(np.float64)))
 
 
 def test_max_reduce_nan_propagates():

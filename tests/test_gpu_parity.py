@@ -105,6 +105,27 @@ def test_ragged_shapes_random_fragments(dtype, rows, cols):
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("pad,pad_s", [(3, 0), (0, 5), (2, 7), (8, 1)])
+def test_amax_and_scale_grids_padded_differently(dtype, pad, pad_s):
+    """The amax grids and the scale grids carry different row strides: every scale entry
+    still comes from its own amax entry, and padding columns keep their sentinels."""
+    rows, cols = 96, 160
+    rng = np.random.default_rng(pad * 13 + pad_s)
+    n = rows * cols
+    x = wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-3, 3, n).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    for start, length in ((0, n), (17, n // 3), (5 * cols + 40, 2 * cols + 3)):
+        frag = np.ascontiguousarray(x[start:start + length])
+        for colwise in (True, False):
+            got = gpu_fragment(frag, rows, cols, start, colwise, pad=pad, pad_s=pad_s,
+                               amax_fill=0.5)
+            want = oracle_fragment(frag, rows, cols, start, colwise, pad=pad, pad_s=pad_s,
+                                   amax_fill=0.5)
+            assert_bitwise(got, want, f"{dtype} pad={pad} pad_s={pad_s} [{start},+{length})")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("shift", [0, 1, 2, 3, 5])
 def test_fragment_output_interface(dtype, shift):
     """out_offset = 0: the output holds only the fragment (fragment-output interface)."""

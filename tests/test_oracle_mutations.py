@@ -70,6 +70,11 @@ MUTATIONS = {
         "int64_t o = out_offset + (k - start);", "int64_t o = (k - start);"),
     "columnwise data scaled by the column's row-block scale index": (
         "scale_c[(i / 32) * ld_sc + j]);", "scale_c[(i / 32) * ld_sc + j / 32 * 32]);"),
+    "NaN amax stored as the all-ones pattern": (
+        "        bits = 0x7FC00000u;", "        bits = 0x7FFFFFFFu;"),
+    "scale update with the leading dimensions swapped": (
+        "scale[r * ld_s + c] = oracle_e8m0_from_amax(load_value(amax, dtype, r * ld_a + c));",
+        "scale[r * ld_a + c] = oracle_e8m0_from_amax(load_value(amax, dtype, r * ld_s + c));"),
     "amax column index shifted by one": (
         "        int64_t i = k / cols, j = k % cols;\n        double a = fabs(",
         "        int64_t i = k / cols, j = (k + 1) % cols;\n        double a = fabs("),

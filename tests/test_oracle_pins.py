@@ -460,3 +460,47 @@ def test_swizzle_matches_reshape_formulation(oracle_mod):
         tiles = P.reshape(pr // 128, 128, pc // 4, 4).transpose(0, 2, 1, 3)  # (tr, tc, 128, 4)
         want = tiles.reshape(pr // 128, pc // 4, 4, 32, 4).transpose(0, 1, 3, 2, 4).ravel()
         assert np.array_equal(oracle_mod.swizzle_scales(np.ascontiguousarray(S), nr, nc, tr), want)
+
+
+# ------------------------------------------------------------------ leading dimensions, NaN bits
+
+def test_update_scales_with_different_leading_dimensions(oracle_mod):
+    """Amax grid and scale grid padded by different amounts: entry (r, c) of the scale
+    grid comes from entry (r, c) of the amax grid, whatever either row stride is, and
+    the padding columns keep their sentinel.  (Both grids carry spare rows so that a
+    mistake with the strides still reads and writes inside the buffers.)"""
+    rng = np.random.default_rng(21)
+    nr, nc = 5, 6
+    for ld_a, ld_s in ((9, 13), (13, 9)):
+        amax = np.abs(wl.normal_f32(rng, (nr + 6, ld_a))) * np.float32(4.0)
+        scale = np.full((nr + 6, ld_s), 0xA5, np.uint8)
+        oracle_mod.update_scales(amax, nr, nc, scale)
+        want = oracle_mod.e8m0_from_amax(amax[:nr, :nc].astype(np.float64))
+        assert np.array_equal(scale[:nr, :nc], want), (ld_a, ld_s)
+        assert (scale[:nr, nc:] == 0xA5).all() and (scale[nr:] == 0xA5).all()
+
+
+NAN_F32_PATTERNS = (0x7F800001, 0x7FBFFFFF, 0x7FC00000, 0x7FFFFFFF, 0xFFC00000, 0xFF800001)
+
+
+def test_nan_amax_is_the_canonical_quiet_nan(oracle_mod):
+    """Whatever NaN pattern (signalling, quiet, negative, with payload) a block holds,
+    its amax -- from the partial amax and from the MAX reduction -- is stored as
+    0x7FC00000 (FP32) / 0x7FC0 (BF16), the stated convention."""
+    for pat in NAN_F32_PATTERNS:
+        x = np.zeros(64, np.float32)
+        x[5] = np.float32(3.0)
+        x.view(np.uint32)[7] = pat
+        ar = np.zeros((1, 2), np.float32)
+        oracle_mod.partial_amax(x, 1, 64, 0, ar, None)
+        assert ar.view(np.uint32)[0, 0] == 0x7FC00000 and ar[0, 1] == 0.0, hex(pat)
+        xb = (x.view(np.uint32) >> 16).astype(np.uint16)
+        xb[7] = pat >> 16 if (pat >> 16) & 0x7F else (pat >> 16) | 0x40  # keep it a NaN
+        arb = np.zeros((1, 2), np.uint16)
+        oracle_mod.partial_amax(xb, 1, 64, 0, arb, None)
+        assert arb[0, 0] == 0x7FC0, hex(pat)
+        slots = np.zeros((3, 4), np.float32)
+        slots.view(np.uint32)[1, 2] = pat
+        slots[2, 2] = 7.0
+        red = oracle_mod.max_reduce(slots)
+        assert red.view(np.uint32)[2] == 0x7FC00000 and red[0] == 0.0, hex(pat)

@@ -4,9 +4,11 @@ Some callers cannot allocate device memory when they need a master-weight update
 memory-pool allocator doing its own maintenance, a framework that reserved all device
 memory up front, code where cudaMalloc would synchronise the device).  For them the
 library runs the update with its own fixed 64 MiB device array as working memory.
-These checks compare that entry point with the ordinary entry points on two calls in a
-row (the second call must clear what the first one left in the shared array), and check
-that an oversized request is refused.  The file is collected last on purpose.
+These checks compare that entry point with the ordinary entry points and with the CPU
+oracle's whole-weight cast on two calls in a row (the second call must clear what the
+first one left in the shared array), check that an oversized request is refused, and
+that a call refused by validation writes nothing.  The file is collected last on
+purpose.
 """
 import ctypes
 
@@ -14,6 +16,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from mxfp8_master_weight_gb300 import _capi, api
 from mxfp8_master_weight_gb300 import workloads as wl
 
@@ -83,6 +86,17 @@ def test_no_alloc_matches_entry_points_twice(dtype, rows, cols, colwise, cuts):
         torch.cuda.synchronize()
         for g, w in zip(got, want):
             assert (g is None and w is None) or torch.equal(g, w), f"call {call}"
+        # and against the oracle's cast of the whole weight (the union of the fragments)
+        host = full.cpu()
+        hx = (host.view(torch.int16).numpy().view(np.uint16) if dtype == torch.bfloat16
+              else host.numpy())
+        o = oracle.full_cast(hx, rows, cols, colwise)
+        names = ("scale_rowwise", "scale_colwise", "data_rowwise", "data_colwise")
+        for name, g, w in zip(names, got, (o[2], o[3], o[4], o[5])):
+            if w is None:
+                assert g is None
+                continue
+            assert np.array_equal(g.cpu().numpy(), w), f"call {call} {name} differs from the oracle"
 
 
 def test_no_alloc_refuses_requests_beyond_its_array():
@@ -92,8 +106,30 @@ def test_no_alloc_refuses_requests_beyond_its_array():
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
     sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
     sc = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda")
-    q = torch.zeros(16, dtype=torch.uint8, device="cuda")
+    q = torch.zeros(64, dtype=torch.uint8, device="cuda")  # room for both tiny fragments
     with pytest.raises(_capi.MXFP8Error) as e:
         api.mxfp8_sharded_update_noalloc([x[:32], x[32:]], [0, 32], sr, sc, q, q, rows, cols)
     assert e.value.status == 2 and "static scratch" in str(e.value)
     assert lib.mxfp8_last_error().startswith(b"needs")
+
+
+def test_no_alloc_refused_call_writes_nothing():
+    """A call that fails validation (here: a columnwise output without columnwise
+    scales, and overlapping fragments) returns its status before anything is launched:
+    the caller's scale grids and outputs keep their sentinel bytes."""
+    rows, cols = 256, 512
+    x = torch.randn(rows * cols, device="cuda") * 0.02
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    sr = torch.full((rr, rc), 0x5A, dtype=torch.uint8, device="cuda")
+    qr = torch.full((rows * cols,), 0xA5, dtype=torch.uint8, device="cuda")
+    qc = torch.full((rows * cols,), 0xA5, dtype=torch.uint8, device="cuda")
+    frags, starts = [x[:40000], x[40000:]], [0, 40000]
+    with pytest.raises(_capi.MXFP8Error) as e:
+        api.mxfp8_sharded_update_noalloc(frags, starts, sr, None, qr, qc, rows, cols)
+    assert e.value.status == 4
+    with pytest.raises(_capi.MXFP8Error) as e:
+        api.mxfp8_sharded_update_noalloc([x[:40000], x[39999:]], [0, 39999], sr, None, qr, None,
+                                         rows, cols)
+    assert e.value.status == 1
+    torch.cuda.synchronize()
+    assert bool((sr == 0x5A).all()) and bool((qr == 0xA5).all()) and bool((qc == 0xA5).all())
