@@ -236,6 +236,30 @@ MXFP8_API int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxf
                                         const mxfp8_scale_job* jobs, int32_t njobs,
                                         void* stream);
 
+/*
+ * The same reduction when each slot holds amaxes only where its rank's fragments are.
+ * A rank's partial amax writes exactly the entries of the blocks its fragments touch;
+ * every other entry of its slot is never written.  Rather than zeroing those entries
+ * before every step and reading them back in the reduction, the caller names, per slot,
+ * the packed entries it holds, and the reduction reads only those (the emulated MAX
+ * all-reduce of section "Changes" then moves only the bytes the ranks produced).
+ *
+ * slot_ranges [in] nranges triples (slot, begin, end): slot `slot` (< S <= 64) holds
+ *                  valid amaxes for packed entries [begin, end) (0 <= begin <= end <= P).
+ *                  Entries of a slot outside all of its ranges count as zero and are
+ *                  not read (their contents are irrelevant); an entry no slot holds
+ *                  reduces to +0.  Ranges of one slot may touch or overlap.
+ * nranges == 0 (slot_ranges may be NULL): every slot holds every entry, exactly as
+ * mxfp8_amax_max_reduce_update_scales.
+ * Other arguments, results and errors as mxfp8_amax_max_reduce_update_scales; 1 also
+ * for a malformed range or more than 64 slots with ranges.
+ */
+MXFP8_API int mxfp8_amax_max_reduce_update_scales_ranged(const mxfp8_tensor* slots,
+                                               mxfp8_tensor* reduced,
+                                               const mxfp8_scale_job* jobs, int32_t njobs,
+                                               const int64_t* slot_ranges, int32_t nranges,
+                                               void* stream);
+
 MXFP8_API int mxfp8_partial_cast_batched(const mxfp8_cast_job* jobs, int32_t njobs, void* stream);
 
 /*

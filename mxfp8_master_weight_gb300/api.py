@@ -203,6 +203,23 @@ def mxfp8_amax_max_reduce_update_scales(slots, reduced, jobs, stream=None) -> No
           ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs), _stream(stream, reduced))
 
 
+def _ranges_array(slot_ranges):
+    flat = [int(v) for r in slot_ranges for v in r]
+    return (ctypes.c_int64 * max(1, len(flat)))(*flat), len(flat) // 3
+
+
+def mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, jobs, slot_ranges,
+                                               stream=None) -> None:
+    """As mxfp8_amax_max_reduce_update_scales, reading slot s only on the packed entries
+    its ranges name: ``slot_ranges`` is a sequence of (slot, begin, end) triples."""
+    arr, keep = _scale_jobs(jobs)
+    rng, nr = _ranges_array(slot_ranges)
+    hs = [handle(slots, "slots"), handle(reduced, "reduced")]
+    _call("mxfp8_amax_max_reduce_update_scales_ranged", _device_of(slots, reduced),
+          ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs), rng, nr,
+          _stream(stream, reduced))
+
+
 def mxfp8_partial_cast_batched(jobs, stream=None) -> None:
     """``jobs``: sequence of (input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
     output_colwise, rows, cols, start_offset[, out_offset])."""
@@ -379,6 +396,16 @@ def prepare_amax_max_reduce_update_scales(slots, reduced, jobs) -> Prepared:
     pr = Prepared("mxfp8_amax_max_reduce_update_scales", hs, (), keep + [slots, reduced])
     pr.args = (ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs))
     pr.handles = hs + [arr]
+    return pr
+
+
+def prepare_amax_max_reduce_update_scales_ranged(slots, reduced, jobs, slot_ranges) -> Prepared:
+    arr, keep = _scale_jobs(jobs)
+    rng, nr = _ranges_array(slot_ranges)
+    hs = [handle(slots, "slots"), handle(reduced, "reduced")]
+    pr = Prepared("mxfp8_amax_max_reduce_update_scales_ranged", hs, (), keep + [slots, reduced])
+    pr.args = (ctypes.byref(hs[0]), ctypes.byref(hs[1]), arr, len(jobs), rng, nr)
+    pr.handles = hs + [arr, rng]
     return pr
 
 

@@ -61,6 +61,26 @@ def source_digest() -> str:
     return h.hexdigest()
 
 
+# Translation units that hold host code only (argument validation, dispatch, the
+# allocation-free entry point's set-up): edits there leave every kernel unchanged.
+HOST_ONLY_UNITS = ("capi.cu", "noalloc.cu")
+
+
+def kernel_digest() -> str:
+    """SHA-256 over the code of the device-side sources only (every csrc file except the
+    host-only units, comments excluded): the key of recorded per-kernel counters, which
+    a host-side edit does not invalidate."""
+    h = hashlib.sha256()
+    for f in _sources():
+        name = os.path.basename(f)
+        if name in HOST_ONLY_UNITS or not f.startswith(CSRC):
+            continue
+        h.update(name.encode())
+        with open(f, encoding="utf-8") as fh:
+            h.update(code_text(fh.read()).encode())
+    return h.hexdigest()
+
+
 def cflags(extra=()):
     return ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2,-fvisibility=hidden",
                    f"-I{INCLUDE}", f"-I{CSRC}", *extra]

@@ -22,8 +22,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned fast path
-constexpr int kShiftBatch = 4;   // rows per batch on the realigning path (extra words per row)
+constexpr int kRowBatch = 8;     // rows per batch of 16-byte loads, aligned and realigning
 constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loads
 // Resident blocks per SM the register allocation must allow: the amax is a pure
 // streaming read, and 3 blocks (24 warps, at most 85 registers) keep more loads in flight
@@ -64,12 +63,15 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   const int64_t row_bytes = cols * T::kBytes;
   const bool writer = (lane % T::G) == 0;
   const int64_t out_r = row0 * p.ld_r + (j >> 5);
-  constexpr int NB = kS ? kShiftBatch : kRowBatch;
+  // the realigning path batches 8 rows too: lane r loads the words after row r of the
+  // tile (one load for the batch) and lane 31 takes them by shuffle
+  constexpr bool kRowLanes = kS != 0;
+  constexpr int NB = kRowBatch;
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
   for (int rb = 0; rb < 32; rb += NB) {
     uint4 v[NB];
-    load_rows<NB, kS>(v, src + rb * row_bytes, row_bytes, lane);
+    load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);

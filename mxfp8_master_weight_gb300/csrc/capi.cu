@@ -1,10 +1,12 @@
 // C ABI of the partial MXFP8 cast (declared in include/mxfp8_partial.h):
 // argument validation, fragment geometry and kernel dispatch.  No entry point
 // allocates memory or synchronises; all work is enqueued on the caller's stream.
+#include <algorithm>
 #include <atomic>
 #include <cstdarg>
 #include <cstdint>
 #include <cstdio>
+#include <vector>
 
 #include <cuda_runtime.h>
 
@@ -583,9 +585,10 @@ int mxfp8_amax_max_reduce(const mxfp8_tensor* slots, mxfp8_tensor* out, void* st
                      "max reduce launch");
 }
 
-int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor* reduced,
-                                        const mxfp8_scale_job* jobs, int32_t njobs,
-                                        void* stream) {
+int mxfp8_amax_max_reduce_update_scales_ranged(const mxfp8_tensor* slots, mxfp8_tensor* reduced,
+                                               const mxfp8_scale_job* jobs, int32_t njobs,
+                                               const int64_t* slot_ranges, int32_t nranges,
+                                               void* stream) {
   if (is_empty(reduced)) return fail(MXFP8_ERR_MISSING, "reduced is required");
   if (int rc = check_tensor(reduced, "reduced")) return rc;
   if (is_empty(slots)) return fail(MXFP8_ERR_MISSING, "slots is required");
@@ -599,6 +602,16 @@ int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor*
   if (numel(reduced) != P)
     return fail(MXFP8_ERR_SHAPE, "reduced numel %lld != slot size %lld", (long long)numel(reduced), (long long)P);
   if (S > 1024) return fail(MXFP8_ERR_INVALID, "too many slots");
+  const bool ranged = nranges > 0;
+  if (nranges < 0 || (ranged && slot_ranges == nullptr))
+    return fail(MXFP8_ERR_INVALID, "bad slot range array");
+  if (ranged && S > 64) return fail(MXFP8_ERR_INVALID, "slot ranges need at most 64 slots");
+  for (int32_t q = 0; q < nranges; ++q) {
+    const int64_t sl = slot_ranges[3 * q], lo = slot_ranges[3 * q + 1], hi = slot_ranges[3 * q + 2];
+    if (sl < 0 || sl >= S || lo < 0 || lo > hi || hi > P)
+      return fail(MXFP8_ERR_INVALID, "slot range %d: (%lld, %lld, %lld) is not a slot and an entry range "
+                  "inside [0, %lld)", int(q), (long long)sl, (long long)lo, (long long)hi, (long long)P);
+  }
   const int64_t eb = elem_bytes(dt);
   const uintptr_t s0 = reinterpret_cast<uintptr_t>(slots->data), r0 = reinterpret_cast<uintptr_t>(reduced->data);
   if (r0 < s0 + uintptr_t(S * P * eb) && s0 < r0 + uintptr_t(P * eb))
@@ -624,38 +637,69 @@ int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor*
   if (njobs == 0) return ok();
   DeviceInfo dev;
   if (int rc = device_info(&dev)) return rc;
-  ReduceScaleSegment batch[64];
-  int n = 0;
-  for (int k = 0; k <= njobs; ++k) {
-    if (k < njobs) {
-      prep_scales(jobs[k], segs, &nseg, &jdt);
-      for (int q = 0; q < nseg; ++q) {
-        int64_t b = 0;
-        inside(segs[q], &b);  // validated above: the view lies inside `reduced`
-        ReduceScaleSegment& r = batch[n++];
-        r = ReduceScaleSegment{};
-        r.slot0 = static_cast<const char*>(slots->data) + b * eb;
-        r.slot_stride = P;
-        r.nslots = int32_t(S);
-        r.reduced = const_cast<void*>(segs[q].amax);
-        r.scale = segs[q].scale;
-        r.nrows = segs[q].nrows;
-        r.ncols = segs[q].ncols;
-        r.ld_a = segs[q].ld_a;
-        r.ld_s = segs[q].ld_s;
-        r.vec = segs[q].vec && (P % 4 == 0) &&
-                (reinterpret_cast<uintptr_t>(r.slot0) % uintptr_t(4 * eb) == 0);
+  // Every grid is cut into runs of entries with one set of contributing slots: the
+  // breakpoints are the grid's ends and every slot range end inside it.
+  std::vector<ReduceScaleSegment> runs;
+  std::vector<int64_t> cuts;
+  for (int k = 0; k < njobs; ++k) {
+    prep_scales(jobs[k], segs, &nseg, &jdt);
+    for (int q = 0; q < nseg; ++q) {
+      int64_t b = 0;
+      inside(segs[q], &b);  // validated above: the view lies inside `reduced`
+      const ScaleSegment& g = segs[q];
+      const int64_t span = (g.nrows - 1) * g.ld_a + g.ncols;  // linear entries of the view
+      ReduceScaleSegment r{};
+      r.slot0 = static_cast<const char*>(slots->data) + b * eb;
+      r.slot_stride = P;
+      r.nslots = int32_t(S);
+      r.reduced = const_cast<void*>(g.amax);
+      r.scale = g.scale;
+      r.nrows = g.nrows;
+      r.ncols = g.ncols;
+      r.ld_a = g.ld_a;
+      r.ld_s = g.ld_s;
+      cuts.assign({0, span});
+      for (int32_t i = 0; i < nranges; ++i) {
+        for (int e = 1; e <= 2; ++e) {
+          const int64_t c = slot_ranges[3 * i + e] - b;
+          if (c > 0 && c < span) cuts.push_back(c);
+        }
+      }
+      std::sort(cuts.begin(), cuts.end());
+      cuts.erase(std::unique(cuts.begin(), cuts.end()), cuts.end());
+      for (size_t i = 0; i + 1 < cuts.size(); ++i) {
+        r.e0 = cuts[i];
+        r.e1 = cuts[i + 1];
+        r.all_slots = ranged ? 0 : 1;
+        r.slots = 0;
+        for (int32_t j = 0; j < nranges; ++j)
+          if (slot_ranges[3 * j + 1] - b <= r.e0 && slot_ranges[3 * j + 2] - b >= r.e1)
+            r.slots |= uint64_t(1) << slot_ranges[3 * j];
+        if (!runs.empty() && runs.back().reduced == r.reduced && runs.back().e1 == r.e0 &&
+            runs.back().slots == r.slots && runs.back().all_slots == r.all_slots) {
+          runs.back().e1 = r.e1;  // same contributors: extend the previous run
+        } else {
+          runs.push_back(r);
+        }
       }
     }
-    if (n > 0 && (n > 62 || k == njobs)) {
-      if (int rc = cuda_status(mxfp8::launch_reduce_update_scales(batch, n, dt == MXFP8_DTYPE_F32 ? 0 : 1,
-                                                                  dev, static_cast<cudaStream_t>(stream)),
-                               "reduce and update scales launch"))
-        return rc;
-      n = 0;
-    }
   }
-  return ok();
+  for (ReduceScaleSegment& r : runs) {
+    r.vec = r.ld_a == r.ncols && r.ld_s == r.ncols && r.e0 % 4 == 0 && r.e1 % 4 == 0 &&
+            (P % 4 == 0) && (reinterpret_cast<uintptr_t>(r.slot0) % uintptr_t(4 * eb) == 0) &&
+            (reinterpret_cast<uintptr_t>(r.reduced) % uintptr_t(4 * eb) == 0) &&
+            (reinterpret_cast<uintptr_t>(r.scale) % 4 == 0);
+  }
+  return cuda_status(mxfp8::launch_reduce_update_scales(runs.data(), int(runs.size()),
+                                                        dt == MXFP8_DTYPE_F32 ? 0 : 1, dev,
+                                                        static_cast<cudaStream_t>(stream)),
+                     "reduce and update scales launch");
+}
+
+int mxfp8_amax_max_reduce_update_scales(const mxfp8_tensor* slots, mxfp8_tensor* reduced,
+                                        const mxfp8_scale_job* jobs, int32_t njobs,
+                                        void* stream) {
+  return mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, jobs, njobs, nullptr, 0, stream);
 }
 
 int mxfp8_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,

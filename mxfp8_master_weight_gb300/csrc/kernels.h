@@ -88,16 +88,23 @@ struct SwizzleParams {
   int32_t vec;          // out is 16-byte aligned
 };
 
-// Fused MAX reduction + scale update of one block grid that is a view into the packed
-// reduced buffer: reduced[r][c] = max_s |slot_s[r][c]|, scale[r][c] = E8M0(reduced).
+// Fused MAX reduction + scale update of a run of entries of one block grid that is a
+// view into the packed reduced buffer: for linear entries e = r * ld_a + c in [e0, e1)
+// (padding columns c >= ncols skipped), reduced[r][c] = max over the contributing slots
+// of |slot_s[r][c]| (+0 when none contributes) and scale[r][c] = E8M0(reduced).  The
+// contributing slots are slots 0 .. nslots-1 (all_slots) or the set bits of `slots`.
 struct ReduceScaleSegment {
   const void* slot0;     // the grid's first entry inside slot 0 of the packed slots
   int64_t slot_stride;   // entries between consecutive slots
+  uint64_t slots;        // contributing slots when !all_slots (bit s = slot s)
   int32_t nslots;
-  int32_t vec;           // dense grid, 4 | entries, 16-byte (F32) / 8-byte (BF16) aligned
+  int32_t all_slots;
+  int32_t vec;           // dense grid, 4 | e0 and e1, 16-byte (F32) / 8-byte (BF16) aligned:
+                         // one work item = 4 entries; otherwise one item = one entry
   void* reduced;         // the grid's view inside the reduced buffer [nrows][ld_a]
   uint8_t* scale;        // [nrows][ld_s]
   int64_t nrows, ncols, ld_a, ld_s;
+  int64_t e0, e1;
 };
 
 struct DeviceInfo {

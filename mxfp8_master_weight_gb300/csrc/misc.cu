@@ -61,72 +61,121 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
   }
 }
 
-// Fused packed MAX reduction + scale update (blockIdx.y selects the grid).
+// Fused packed MAX reduction + scale update over runs of grid entries.  The work items
+// of every segment of a launch form one index space (prefix sums in the parameters), over
+// which the grid strides, so large and small grids share the SMs evenly; each thread
+// loads the contributing slots of two items before it stores either.
+constexpr int kMaxReduceSegments = 64;
+
 struct ReduceScaleBatch {
   int32_t nseg;
-  ReduceScaleSegment seg[kMaxSegments];
+  int64_t prefix[kMaxReduceSegments + 1];  // items before segment k
+  ReduceScaleSegment seg[kMaxReduceSegments];
 };
+
+// Maximum of |.| over the contributing slots of entry idx (4 consecutive entries when
+// kQuad) of a segment, as raw bit patterns; NaN canonicalised.
+template <class T, bool kQuad>
+__device__ __forceinline__ void reduce_entries(const ReduceScaleSegment& s, int64_t idx, uint32_t (&m)[4]) {
+  constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
+  m[0] = m[1] = m[2] = m[3] = 0u;
+  const char* base = static_cast<const char*>(s.slot0) + idx * T::kBytes;
+  const int64_t slot_bytes = s.slot_stride * T::kBytes;
+  uint64_t mask = s.slots;
+  for (int k = 0;; ++k) {
+    int slot;
+    if (s.all_slots) {
+      if (k >= s.nslots) break;
+      slot = k;
+    } else {
+      if (mask == 0) break;
+      slot = __ffsll(static_cast<long long>(mask)) - 1;
+      mask &= mask - 1;
+    }
+    const char* p = base + slot * slot_bytes;
+    if constexpr (kQuad) {
+      if constexpr (T::kBytes == 4) {
+        const uint4 a = ld_stream16(p);
+        m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], a.y & kAbs);
+        m[2] = max(m[2], a.z & kAbs); m[3] = max(m[3], a.w & kAbs);
+      } else {
+        const uint2 a = *reinterpret_cast<const uint2*>(p);
+        m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], (a.x >> 16) & kAbs);
+        m[2] = max(m[2], a.y & kAbs); m[3] = max(m[3], (a.y >> 16) & kAbs);
+      }
+    } else {
+      m[0] = max(m[0], load_bits<T>(p, 0) & kAbs);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < 4; ++k) m[k] = canonical_nan<T>(m[k]);
+}
+
+// One work item: its segment, the linear entry it starts at, and the reduced values.
+struct ReduceItem {
+  int seg;
+  int64_t e;
+  bool live;
+  uint32_t m[4];
+};
+
+template <class T>
+__device__ __forceinline__ void load_item(const ReduceScaleBatch& b, int64_t t, ReduceItem& it) {
+  int lo = 0, hi = b.nseg;  // prefix[lo] <= t < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (b.prefix[mid] <= t) lo = mid; else hi = mid;
+  }
+  const ReduceScaleSegment& s = b.seg[lo];
+  const int64_t k = t - b.prefix[lo];
+  it.seg = lo;
+  if (s.vec) {
+    it.e = s.e0 + 4 * k;
+    it.live = true;
+    reduce_entries<T, true>(s, it.e, it.m);
+  } else {
+    it.e = s.e0 + k;
+    it.live = (it.e % s.ld_a) < s.ncols;  // padding columns of a padded grid: nothing to do
+    if (it.live) reduce_entries<T, false>(s, it.e, it.m);
+  }
+}
+
+template <class T>
+__device__ __forceinline__ void store_item(const ReduceScaleBatch& b, const ReduceItem& it) {
+  if (!it.live) return;
+  const ReduceScaleSegment& s = b.seg[it.seg];
+  if (s.vec) {
+    if constexpr (T::kBytes == 4) {
+      *reinterpret_cast<uint4*>(static_cast<uint32_t*>(s.reduced) + it.e) =
+          make_uint4(it.m[0], it.m[1], it.m[2], it.m[3]);
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(s.reduced) + it.e) =
+          make_uint2(it.m[0] | (it.m[1] << 16), it.m[2] | (it.m[3] << 16));
+    }
+    uint32_t out = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(it.m[k]) << (8 * k);
+    *reinterpret_cast<uint32_t*>(s.scale + it.e) = out;  // dense: ld_s == ld_a == ncols
+  } else {
+    const int64_t r = it.e / s.ld_a, c = it.e % s.ld_a;
+    store_bits<T>(s.reduced, it.e, it.m[0]);
+    s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(it.m[0]));
+  }
+}
 
 template <class T>
 __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
     const __grid_constant__ ReduceScaleBatch b) {
   grid_dependency_sync();
-  const ReduceScaleSegment& s = b.seg[blockIdx.y];
-  const int64_t n = s.nrows * s.ncols;
+  const int64_t total = b.prefix[b.nseg];
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
-  constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
-  if (s.vec) {
-    const char* src = static_cast<const char*>(s.slot0);
-    const int64_t slot_bytes = s.slot_stride * T::kBytes;
-    const int64_t quads = n / 4;
-    constexpr int U = 2;  // quads per thread per iteration, all loaded before any store
-    for (int64_t q0 = tid; q0 < quads; q0 += U * stride) {
-      uint32_t m[U][4] = {};
-      for (int k = 0; k < s.nslots; ++k) {
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int64_t q = q0 + u * stride;
-          if (q >= quads) break;
-          const char* p = src + k * slot_bytes + q * 4 * T::kBytes;
-          if constexpr (T::kBytes == 4) {
-            const uint4 a = ld_stream16(p);
-            m[u][0] = max(m[u][0], a.x & kAbs); m[u][1] = max(m[u][1], a.y & kAbs);
-            m[u][2] = max(m[u][2], a.z & kAbs); m[u][3] = max(m[u][3], a.w & kAbs);
-          } else {
-            const uint2 a = *reinterpret_cast<const uint2*>(p);
-            m[u][0] = max(m[u][0], a.x & kAbs); m[u][1] = max(m[u][1], (a.x >> 16) & kAbs);
-            m[u][2] = max(m[u][2], a.y & kAbs); m[u][3] = max(m[u][3], (a.y >> 16) & kAbs);
-          }
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int64_t q = q0 + u * stride;
-        if (q >= quads) break;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) m[u][k] = canonical_nan<T>(m[u][k]);
-        if constexpr (T::kBytes == 4) {
-          reinterpret_cast<uint4*>(s.reduced)[q] = make_uint4(m[u][0], m[u][1], m[u][2], m[u][3]);
-        } else {
-          reinterpret_cast<uint2*>(s.reduced)[q] = make_uint2(m[u][0] | (m[u][1] << 16), m[u][2] | (m[u][3] << 16));
-        }
-        uint32_t out = 0;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[u][k]) << (8 * k);
-        reinterpret_cast<uint32_t*>(s.scale)[q] = out;
-      }
-    }
-  } else {
-    for (int64_t e = tid; e < n; e += stride) {
-      const int64_t r = e / s.ncols, c = e % s.ncols;
-      const int64_t idx = r * s.ld_a + c;
-      uint32_t m = 0;
-      for (int k = 0; k < s.nslots; ++k) m = max(m, load_bits<T>(s.slot0, k * s.slot_stride + idx) & kAbs);
-      m = canonical_nan<T>(m);
-      store_bits<T>(s.reduced, idx, m);
-      s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(m));
-    }
+  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += 2 * stride) {
+    ReduceItem a, c;
+    load_item<T>(b, t, a);
+    const bool two = t + stride < total;
+    if (two) load_item<T>(b, t + stride, c);
+    store_item<T>(b, a);
+    if (two) store_item<T>(b, c);
   }
 }
 
@@ -227,21 +276,18 @@ cudaError_t launch_update_scales(const ScaleSegment* segs, int nseg, int dtype,
 
 cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg, int dtype,
                                        const DeviceInfo& dev, cudaStream_t stream) {
-  for (int k0 = 0; k0 < nseg; k0 += kMaxSegments) {
+  for (int k0 = 0; k0 < nseg; k0 += kMaxReduceSegments) {
     ReduceScaleBatch b;
-    b.nseg = nseg - k0 < kMaxSegments ? nseg - k0 : kMaxSegments;
-    int64_t work = 0;
+    b.nseg = nseg - k0 < kMaxReduceSegments ? nseg - k0 : kMaxReduceSegments;
+    b.prefix[0] = 0;
     for (int k = 0; k < b.nseg; ++k) {
       b.seg[k] = segs[k0 + k];
-      const int64_t n = b.seg[k].nrows * b.seg[k].ncols;
-      const int64_t items = b.seg[k].vec ? n / 4 : n;
-      work = items > work ? items : work;
+      const int64_t n = b.seg[k].e1 - b.seg[k].e0;
+      b.prefix[k + 1] = b.prefix[k] + (b.seg[k].vec ? n / 4 : n);
     }
-    if (work == 0) continue;
-    const int64_t per_seg = (int64_t(dev.sms) * 8 + b.nseg - 1) / b.nseg;
-    const int64_t want = (work + kThreads - 1) / kThreads;
-    const unsigned gx = unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg));
-    const dim3 grid(gx, unsigned(b.nseg));
+    const int64_t total = b.prefix[b.nseg];
+    if (total == 0) continue;
+    const unsigned grid = grid_for((total + 1) / 2, dev);
     const cudaError_t e = dtype == 0
                               ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
                               : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);

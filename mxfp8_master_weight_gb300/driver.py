@@ -8,15 +8,17 @@ present directions are updated, and every rank casts its fragments in place.
 
 Here the ranks are emulated on one GPU: shard s is its own device buffer (as a
 rank's master shard would be) and has its own slot of the packed amax buffer;
-the cross-rank MAX all-reduce is one ``mxfp8_amax_max_reduce`` over the slots.
+the cross-rank MAX all-reduce is one reduction over the slots, fused with the
+scale update.  A slot is read only on the entries its shard's amax writes (the
+ranged reduction), so slots are never zeroed between steps.
 All arithmetic runs in the CUDA library; this module only plans fragments and
 packed offsets (host logic) and issues the calls.
 
 Packed layout: weights in batch order; for each weight its rowwise block grid
 [rows][ceil(cols/32)], then -- only when it has a columnwise direction -- its
-columnwise grid [ceil(rows/32)][cols].  Each entry starts on a multiple of 16
+columnwise grid [ceil(rows/32)][cols].  Each grid starts on a multiple of 16
 elements (64 bytes for FP32) so that every view keeps 16-byte vector access;
-the padding entries stay zero and reduce to zero.
+the padding entries between grids belong to no grid and are never reduced.
 """
 from __future__ import annotations
 
@@ -78,6 +80,58 @@ def plan_fragments(specs, bounds):
     return plan
 
 
+def fragment_block_ranges(spec: WeightSpec, start: int, length: int):
+    """Entries of the block grids that the fragment [start, start+length) of a weight
+    touches, as ranges of linear grid indices: (rowwise ranges over r*ceil(cols/32)+b,
+    columnwise ranges over c*cols+j -- empty for a row-only weight).  These are exactly
+    the entries the partial amax of that fragment writes.
+
+    Rowwise: the fragment is contiguous in row-major order, so its 1x32 blocks are one
+    run of the rowwise grid.  Columnwise: every 32-row band strictly between the first
+    and last band is whole; in an end band the touched columns are the union of the
+    fragment's row spans inside the band (which may leave a gap when the band holds
+    only two partial rows of the fragment).
+    """
+    if length <= 0:
+        return [], []
+    rows, cols = spec.rows, spec.cols
+    nbr = (cols + 31) // 32
+    end = start + length
+    r0, cs = divmod(start, cols)
+    r1, ce = divmod(end - 1, cols)
+    row = [(r0 * nbr + cs // 32, r1 * nbr + ce // 32 + 1)]
+    col = []
+    if spec.colwise:
+        c0, c1 = r0 // 32, r1 // 32
+        for c in range(c0, c1 + 1):
+            if c0 < c < c1:
+                spans = [(0, cols - 1)]
+            else:
+                a, b = max(r0, 32 * c), min(r1, 32 * c + 31)
+                spans = []
+                for i in ((a, b) if b > a else (a,)):  # middle rows of a band are whole
+                    spans.append((cs if i == r0 else 0, ce if i == r1 else cols - 1))
+                if b - a >= 2:
+                    spans = [(0, cols - 1)]
+            for lo, hi in sorted(spans):
+                lo_e, hi_e = c * cols + lo, c * cols + hi + 1
+                if col and col[-1][1] >= lo_e:
+                    col[-1] = (col[-1][0], max(col[-1][1], hi_e))
+                else:
+                    col.append((lo_e, hi_e))
+    return row, col
+
+
+def _merge(ranges):
+    out = []
+    for lo, hi in sorted(ranges):
+        if out and out[-1][1] >= lo:
+            out[-1] = (out[-1][0], max(out[-1][1], hi))
+        else:
+            out.append((lo, hi))
+    return out
+
+
 class PackedLayout:
     """Element offsets of every present block grid inside the packed amax buffer."""
 
@@ -96,6 +150,22 @@ class PackedLayout:
                 self.colwise.append(None)
         self.total = off
 
+    def slot_ranges(self, plan):
+        """(slot, begin, end) packed-entry ranges that each slot's fragments write: the
+        only entries of a slot the reduction needs to read."""
+        out = []
+        for s, cuts in enumerate(plan):
+            rs = []
+            for c in cuts:
+                row, col = fragment_block_ranges(self.specs[c.weight], c.start, c.length)
+                ro = self.rowwise[c.weight][0]
+                rs += [(ro + a, ro + b) for a, b in row]
+                if self.colwise[c.weight] is not None:
+                    co = self.colwise[c.weight][0]
+                    rs += [(co + a, co + b) for a, b in col]
+            out += [(s, a, b) for a, b in _merge(rs)]
+        return out
+
     def views(self, buf: torch.Tensor, w: int):
         """(rowwise view, columnwise view or None) of weight w inside a 1-D packed buffer."""
         o, shp = self.rowwise[w]
@@ -107,7 +177,7 @@ class PackedLayout:
         return vr, vc
 
 
-def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs, fused_reduce=False) -> int:
+def _count_launches(amax_jobs, cast_jobs, n_reduce_runs, specs, fused_reduce=False) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
     entries launch once per group of at most 16 jobs sharing dtype and alignment class
     (fragment virtual base on a 16-byte boundary; for the cast also the outputs'
@@ -128,8 +198,33 @@ def _count_launches(amax_jobs, cast_jobs, n_scale_jobs, specs, fused_reduce=Fals
         vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
         ckeys.append((frag.dtype, vbase(frag, start) % 16 != 0, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
-    reduce_and_scales = (n_grids + 31) // 32 if fused_reduce else 1 + (n_grids + 31) // 32
+    if fused_reduce:  # one launch per 64 runs of grid entries with one set of slots
+        reduce_and_scales = (n_reduce_runs + 63) // 64
+    else:             # the reduction, then one scale launch per 32 grids
+        reduce_and_scales = 1 + (n_grids + 31) // 32
     return groups(akeys, 16) + reduce_and_scales + groups(ckeys, 16)
+
+
+def reduce_runs(layout: PackedLayout, ranges) -> int:
+    """Runs the fused reduction splits the block grids into: each grid is cut at every
+    slot range end inside it, and neighbouring pieces read by the same slots are joined
+    (without ranges, one run per grid)."""
+    runs = 0
+    grids = [g for w in range(len(layout.specs)) for g in (layout.rowwise[w], layout.colwise[w])
+             if g is not None]
+    for off, (nr, nc) in grids:
+        span = nr * nc
+        if not ranges:
+            runs += 1
+            continue
+        cuts = sorted({0, span} | {e - off for _, a, b in ranges for e in (a, b) if 0 < e - off < span})
+        prev = None
+        for lo, hi in zip(cuts[:-1], cuts[1:]):
+            mask = frozenset(s for s, a, b in ranges if a - off <= lo and b - off >= hi)
+            if mask != prev:
+                runs += 1
+            prev = mask
+    return runs
 
 
 def _round_up(x: int, a: int) -> int:
@@ -145,7 +240,8 @@ class ShardedCast:
     always, columnwise only for bidirectional weights).
     """
 
-    def __init__(self, specs, bounds, device, dtype=torch.float32, fuse_reduce_scales=True):
+    def __init__(self, specs, bounds, device, dtype=torch.float32, fuse_reduce_scales=True,
+                 ranged=True):
         self.specs = [s if isinstance(s, WeightSpec) else WeightSpec(*s) for s in specs]
         self.bounds = list(bounds)
         self.plan = plan_fragments(self.specs, self.bounds)
@@ -157,9 +253,14 @@ class ShardedCast:
         S = len(self.bounds) - 1
         self.slots = torch.zeros((S, self.layout.total), dtype=dtype, device=device)
         self.reduced = torch.zeros(self.layout.total, dtype=dtype, device=device)
-        # a slot needs zeroing before each step unless its shard holds every weight whole
-        # (then every block entry of the slot is overwritten by the amax kernels)
-        self._zero_slot = [not (len(cuts) == len(self.specs) and
+        # With the ranged reduction (fused path) each slot is read only on the entries its
+        # fragments' amax writes every step, so no slot is ever zeroed.  The plain
+        # reduction reads whole slots: a slot then needs zeroing before each step unless
+        # its shard holds every weight whole (every entry of it is overwritten).
+        self.ranged = bool(ranged and fuse_reduce_scales and len(self.bounds) - 1 <= 64)
+        self.ranges = self.layout.slot_ranges(self.plan) if self.ranged else None
+        self._zero_slot = [not self.ranged and
+                           not (len(cuts) == len(self.specs) and
                                 all(c.start == 0 and c.length == self.specs[c.weight].numel
                                     for c in cuts))
                            for cuts in self.plan]
@@ -216,10 +317,14 @@ class ShardedCast:
         # one batched call per phase: every fragment of every shard (each shard writes
         # its own slot, so no two jobs write the same amax entry), one reduction, every
         # weight's scales, every fragment's cast
-        self._launches = _count_launches(amax_jobs, cast_jobs, len(scale_jobs), self.specs,
-                                         self.fuse_reduce_scales)
+        self._launches = _count_launches(amax_jobs, cast_jobs, reduce_runs(self.layout, self.ranges),
+                                         self.specs, self.fuse_reduce_scales)
         amax = [api.prepare_partial_amax_batched(amax_jobs)]
-        if self.fuse_reduce_scales:
+        if self.ranged:
+            reduce = [api.prepare_amax_max_reduce_update_scales_ranged(self.slots, self.reduced,
+                                                                       scale_jobs, self.ranges)]
+            scales = []
+        elif self.fuse_reduce_scales:
             reduce = [api.prepare_amax_max_reduce_update_scales(self.slots, self.reduced, scale_jobs)]
             scales = []
         else:

@@ -131,3 +131,134 @@ class ZeroCopyQuantizer:
                                             host_qr.reshape(-1),
                                             None if host_qc is None else host_qc.reshape(-1),
                                             self.rows, self.cols, 0, allow_host=True)
+
+
+class HostPartialFlow:
+    """The four-step partial flow on a host-resident master weight, pipelined with the copies.
+
+    Partial amax -> packed MAX reduction fused with the scale update -> partial cast, as a
+    rank of the distributed writeback runs it ("Support row-only MXFP8 distributed
+    master-weight casts", flow diagram), for a weight whose master copy lives in pinned
+    host memory.  The weight is cut into chunks of whole 32-row bands, each a fragment of
+    the weight: chunk k's block maxima are taken as soon as its copy has landed (while
+    chunk k+1 is still being copied in), every chunk writing its own blocks of the one
+    amax slot; after the last chunk the slot is reduced and the scales are derived; then
+    chunk k is cast into a staging buffer while chunk k-1's E4M3 bytes are copied out.
+    The device input is double-buffered across calls, so one call's copy-in overlaps the
+    previous call's copy-out.  All arithmetic runs in the library's kernels; this class
+    only orders copies and launches on three streams.
+    """
+
+    def __init__(self, rows: int, cols: int, colwise: bool = True, dtype=torch.float32,
+                 device="cuda", chunk_rows: int = 1024, depth: int = 3):
+        if rows <= 0 or cols <= 0:
+            raise ValueError("rows and cols must be positive")
+        self.rows, self.cols, self.colwise, self.dtype = rows, cols, colwise, dtype
+        self.device = torch.device(device)
+        self.chunk_rows = max(32, min((chunk_rows + 31) // 32 * 32, (rows + 31) // 32 * 32))
+        self.depth = max(1, depth)
+        n = rows * cols
+        cn = self.chunk_rows * cols
+        (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+        with torch.cuda.device(self.device):
+            self.dev_x = [torch.empty(n, dtype=dtype, device=self.device) for _ in range(2)]
+            entries = rr * rc + (cr * cc if colwise else 0)
+            self.slot = torch.zeros((1, entries), dtype=dtype, device=self.device)
+            self.reduced = torch.zeros(entries, dtype=dtype, device=self.device)
+            self.amax_r = self.slot[0, :rr * rc].view(rr, rc)
+            self.amax_c = self.slot[0, rr * rc:].view(cr, cc) if colwise else None
+            red_r = self.reduced[:rr * rc].view(rr, rc)
+            red_c = self.reduced[rr * rc:].view(cr, cc) if colwise else None
+            self.scale_r = torch.empty((rr, rc), dtype=torch.uint8, device=self.device)
+            self.scale_c = torch.empty((cr, cc), dtype=torch.uint8, device=self.device) if colwise else None
+            self.dev_qr = [torch.empty(cn, dtype=torch.uint8, device=self.device) for _ in range(self.depth)]
+            self.dev_qc = ([torch.empty(cn, dtype=torch.uint8, device=self.device) for _ in range(self.depth)]
+                           if colwise else None)
+            self.h2d, self.comp, self.d2h = (torch.cuda.Stream(self.device) for _ in range(3))
+            self.in_ready = [torch.cuda.Event() for _ in self.chunks]
+            self.x_free = [torch.cuda.Event() for _ in range(2)]
+            self.comp_done = [torch.cuda.Event() for _ in range(self.depth)]
+            self.d2h_done = [torch.cuda.Event() for _ in range(self.depth)]
+            self.scales_out = torch.cuda.Event()
+        # one marshalled library call per chunk and phase, for each device input buffer
+        self._amax = [[api.prepare_partial_amax(self.dev_x[b][r0 * cols:r1 * cols], self.amax_r,
+                                                self.amax_c, rows, cols, r0 * cols)
+                       for r0, r1 in self.chunks] for b in range(2)]
+        self._reduce = api.prepare_amax_max_reduce_update_scales(
+            self.slot, self.reduced, [(red_r, red_c, self.scale_r, self.scale_c, rows, cols)])
+        self._cast = [[api.prepare_partial_cast(
+            self.dev_x[b][r0 * cols:r1 * cols], self.scale_r, self.scale_c,
+            self.dev_qr[k % self.depth][:(r1 - r0) * cols],
+            self.dev_qc[k % self.depth][:(r1 - r0) * cols] if colwise else None,
+            rows, cols, r0 * cols, 0) for k, (r0, r1) in enumerate(self.chunks)] for b in range(2)]
+        self._calls = 0
+
+    @property
+    def chunks(self):
+        return [(r0, min(self.rows, r0 + self.chunk_rows))
+                for r0 in range(0, self.rows, self.chunk_rows)]
+
+    def launches_per_run(self) -> int:
+        """Library kernel launches of one call: an amax and a cast per chunk, one reduction."""
+        return 2 * len(self.chunks) + 1
+
+    def run(self, host_x: torch.Tensor, host_qr: torch.Tensor, host_qc: torch.Tensor | None,
+            host_sr: torch.Tensor, host_sc: torch.Tensor | None) -> None:
+        """Quantise ``host_x`` (pinned, rows*cols elements) into the pinned host outputs.
+
+        Asynchronous with respect to the host, like HostQuantizer.run: the caller's
+        current stream waits for the last copy out."""
+        rows, cols = self.rows, self.cols
+        for t, name in ((host_x, "host_x"), (host_qr, "host_qr"), (host_qc, "host_qc"),
+                        (host_sr, "host_sr"), (host_sc, "host_sc")):
+            if t is not None and (t.is_cuda or not t.is_pinned()):
+                raise ValueError(f"{name} must be pinned host memory")
+        if host_x.numel() != rows * cols or host_qr.numel() != rows * cols:
+            raise ValueError("host_x and host_qr must hold rows*cols elements")
+        if self.colwise != (host_qc is not None) or self.colwise != (host_sc is not None):
+            raise ValueError("host_qc and host_sc are required exactly when the weight is bidirectional")
+        if host_x.dtype != self.dtype:
+            raise ValueError("host_x has the wrong dtype")
+        x, qr = host_x.reshape(-1), host_qr.reshape(-1)
+        qc = host_qc.reshape(-1) if host_qc is not None else None
+        b = self._calls % 2
+        self._calls += 1
+        caller = torch.cuda.current_stream(self.device)
+        for s in (self.h2d, self.comp, self.d2h):
+            s.wait_stream(caller)
+        dx = self.dev_x[b]
+        raw_comp = api._stream(self.comp, None)
+        # copy in, chunk by chunk (the buffer is free once the casts of two calls ago ran)
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.x_free[b])
+            for k, (r0, r1) in enumerate(self.chunks):
+                dx[r0 * cols:r1 * cols].copy_(x[r0 * cols:r1 * cols], non_blocking=True)
+                self.in_ready[k].record(self.h2d)
+        with torch.cuda.stream(self.comp):
+            # partial amax of each chunk as soon as it has landed
+            for k in range(len(self.chunks)):
+                self.comp.wait_event(self.in_ready[k])
+                self._amax[b][k].call(raw_comp)
+            # the previous call's scales must have left before they are rewritten
+            self.comp.wait_event(self.scales_out)
+            self._reduce.call(raw_comp)
+            for k, (r0, r1) in enumerate(self.chunks):
+                s = k % self.depth
+                self.comp.wait_event(self.d2h_done[s])  # staging buffer s has been copied out
+                self._cast[b][k].call(raw_comp)
+                self.comp_done[s].record(self.comp)
+            self.x_free[b].record(self.comp)
+        with torch.cuda.stream(self.d2h):
+            for k, (r0, r1) in enumerate(self.chunks):
+                s = k % self.depth
+                self.d2h.wait_event(self.comp_done[s])
+                n = (r1 - r0) * cols
+                qr[r0 * cols:r1 * cols].copy_(self.dev_qr[s][:n], non_blocking=True)
+                if qc is not None:
+                    qc[r0 * cols:r1 * cols].copy_(self.dev_qc[s][:n], non_blocking=True)
+                self.d2h_done[s].record(self.d2h)
+            host_sr.copy_(self.scale_r, non_blocking=True)
+            if host_sc is not None:
+                host_sc.copy_(self.scale_c, non_blocking=True)
+            self.scales_out.record(self.d2h)
+        caller.wait_stream(self.d2h)

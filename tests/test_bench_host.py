@@ -73,6 +73,17 @@ def test_sharded_step_bytes():
     amax = n0 * 4 + 2 * n0 // 32 * 4 + n1 * 4 + n1 // 32 * 4
     cast = n0 * 4 + 2 * n0 // 32 + 2 * n0 + n1 * 4 + n1 // 32 + n1
     assert b == amax + cast + 2 * 1000 * 4 + 1000 * 4 + 1000
+    ph = bench.sharded_phase_bytes(specs, num_slots=2, packed_entries=1000)
+    assert ph == {"amax": amax, "reduce_scales": 2 * 1000 * 4 + 1000 * 4 + 1000, "cast": cast}
+    assert sum(ph.values()) == b
+
+
+def test_stats_and_kernel_digest():
+    s = bench.stats([3.0, 1.0, 2.0, 10.0])
+    assert s["median"] == 2.5 and s["mean"] == 4.0 and s["n"] == 4
+    from mxfp8_master_weight_gb300 import build
+    d = build.kernel_digest()
+    assert len(d) == 64 and d != build.source_digest()
 
 
 def test_cpu_all_cores_run_matches_single_core_bytes():

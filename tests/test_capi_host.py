@@ -294,3 +294,25 @@ def test_noalloc_refuses_bad_arguments_before_any_device_work(lib):
     assert call(two, [0, 3000], sr, sc, q, q) == 1                   # fragment past the end
     assert call([T(P, F32, 2048), T(P + 8192, BF16, 2048)], [0, 2048], sr, sc, q, q) == 3
     assert call([E(), E()], [0, 0], sr, sc, q, q) == 0              # nothing to do
+
+
+def test_ranged_reduction_validation(lib):
+    fn = lib.mxfp8_amax_max_reduce_update_scales_ranged
+    slots = T(P, F32, 4, 100)
+    red = T(P + 4096, F32, 100)
+    job = _capi.ScaleJob(T(P + 4096, F32, 2, 50), E(), T(P + 8192, U8, 2, 50), E(), 2, 1600)
+
+    def call(triples, slots_=slots):
+        flat = [v for t in triples for v in t]
+        arr = (ctypes.c_int64 * max(1, len(flat)))(*flat)
+        return fn(ctypes.byref(slots_), ctypes.byref(red), ctypes.byref(job), 1, arr,
+                  len(triples), None)
+
+    assert call([(4, 0, 10)]) == 1              # no slot 4
+    assert call([(0, 20, 10)]) == 1             # begin > end
+    assert call([(0, 0, 101)]) == 1             # past the slot
+    assert call([(-1, 0, 1)]) == 1
+    assert b"slot range" in lib.mxfp8_last_error()
+    assert call([(0, 0, 10)], T(P, F32, 65, 100)) == 1  # ranges need at most 64 slots
+    assert b"64" in lib.mxfp8_last_error()
+    assert fn(ctypes.byref(slots), ctypes.byref(red), ctypes.byref(job), 1, None, 1, None) == 1

@@ -3,7 +3,7 @@ force membership, and the packed amax layout."""
 import numpy as np
 import pytest
 
-from mxfp8_master_weight_gb300 import driver
+from mxfp8_master_weight_gb300 import api, driver
 from mxfp8_master_weight_gb300 import workloads as wl
 
 
@@ -80,3 +80,74 @@ def test_packed_layout():
     buf = torch.arange(lay.total, dtype=torch.float32)
     vr, vc = lay.views(buf, 1)
     assert vc is None and vr.shape == (40, 3) and vr.is_contiguous()
+
+
+def _written_entries(rows, cols, colwise, start, length):
+    """Linear grid indices the oracle's partial amax writes for a fragment: grids filled
+    with a NaN sentinel, every written entry holds a finite maximum afterwards."""
+    import oracle
+    rng = np.random.default_rng(start * 31 + length)
+    frag = (rng.standard_normal(length) * 0.02).astype(np.float32)
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    ar = np.full((rr, rc), np.nan, np.float32)
+    ac = np.full((cr, cc), np.nan, np.float32) if colwise else None
+    oracle.partial_amax(frag, rows, cols, start, ar, ac)
+    row = set(np.flatnonzero(~np.isnan(ar.reshape(-1))).tolist())
+    col = set(np.flatnonzero(~np.isnan(ac.reshape(-1))).tolist()) if colwise else set()
+    return row, col
+
+
+def _expand(ranges):
+    return {e for a, b in ranges for e in range(a, b)}
+
+
+@pytest.mark.parametrize("rows,cols", [(70, 50), (64, 96), (33, 65), (96, 7)])
+def test_fragment_block_ranges_are_the_written_entries(oracle_mod, rows, cols):
+    """The ranges the driver gives the ranged reduction are exactly the entries the
+    partial amax writes, for fragments of every shape: inside a row, across two rows of
+    one band (the gap case), across bands, whole weights."""
+    n = rows * cols
+    rng = np.random.default_rng(rows * cols)
+    cases = [(0, n), (0, 1), (n - 1, 1), (cols - 3, 5), (cols * 31 + 7, 2 * cols - 10),
+             (cols * 30 + 40 % cols, cols + 3), (5, cols * 40)]
+    cases += [(int(s), int(rng.integers(1, n - s + 1))) for s in rng.integers(0, n, 40)]
+    for start, length in cases:
+        if start + length > n or length <= 0:
+            continue
+        for colwise in (True, False):
+            spec = driver.WeightSpec(rows, cols, colwise)
+            row, col = driver.fragment_block_ranges(spec, start, length)
+            w_row, w_col = _written_entries(rows, cols, colwise, start, length)
+            assert _expand(row) == w_row, (rows, cols, start, length)
+            assert _expand(col) == w_col, (rows, cols, start, length, colwise)
+            assert all(a < b for a, b in row + col)
+
+
+def test_slot_ranges_cover_each_grid_and_count_runs():
+    """Every entry of every grid is held by at least one slot; entries of blocks cut by a
+    shard boundary by exactly two; the run count matches a brute-force cut."""
+    specs = [driver.WeightSpec(96, 64, True), driver.WeightSpec(64, 96, False),
+             driver.WeightSpec(32, 128, True)]
+    total = sum(s.numel for s in specs)
+    bounds = [0, 1000, 1000, 96 * 64 + 17, total]
+    plan = driver.plan_fragments(specs, bounds)
+    layout = driver.PackedLayout(specs)
+    ranges = layout.slot_ranges(plan)
+    holders = {}
+    for s, a, b in ranges:
+        for e in range(a, b):
+            holders.setdefault(e, set()).add(s)
+    grids = [g for w in range(3) for g in (layout.rowwise[w], layout.colwise[w]) if g is not None]
+    for off, (nr, nc) in grids:
+        for e in range(off, off + nr * nc):
+            assert 1 <= len(holders.get(e, ())) <= 2
+    # brute-force runs: consecutive grid entries with the same holder set
+    want = 0
+    for off, (nr, nc) in grids:
+        prev = None
+        for e in range(off, off + nr * nc):
+            h = frozenset(holders[e])
+            want += h != prev
+            prev = h
+    assert driver.reduce_runs(layout, ranges) == want
+    assert driver.reduce_runs(layout, None) == len(grids)

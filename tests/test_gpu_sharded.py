@@ -134,3 +134,72 @@ def test_fused_reduce_scales_entry_with_padded_views():
     with pytest.raises(_capi.MXFP8Error) as e:
         api.mxfp8_amax_max_reduce_update_scales(slots, reduced, [(outside, None, sr, None, rows, cols)])
     assert e.value.status == 1
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ranged_reduction_never_reads_untouched_slot_entries(dtype):
+    """The driver's slots are never zeroed: the ranged reduction reads a slot only where
+    its shard's amax wrote.  Slots pre-filled with garbage (NaN, huge values) that the
+    amax leaves in place must not reach the reduced amax, the scales or the data --
+    over two consecutive steps."""
+    batch = wl.cfg5_sharded_batch(seed=4, scale=8)
+    if dtype == torch.bfloat16:
+        flat = wl.truncate_to_bf16_bits(batch.flat)
+        weights = [wl.Weight(w.rows, w.cols, wl.BF16, flat[o:o + w.numel], w.colwise)
+                   for w, o in zip(batch.weights, batch.offsets)]
+        batch = wl.ShardedBatch(weights, batch.offsets, batch.bounds, flat)
+    sc, shards = _run(batch, dtype)
+    assert sc.ranged and not any(sc._zero_slot)
+    for fill in (float("nan"), 3.0e38 if dtype == torch.float32 else 1.0e38):
+        sc.slots.fill_(fill)
+        sc.reduced.fill_(-1.0)
+        sc.step(shards)
+        _check_against_full(batch, sc)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_ranged_entry_matches_whole_slot_reduction(dtype):
+    """Random slot ranges over a packed buffer with padded views: the ranged reduction
+    equals the whole-slot reduction of slots zeroed outside their ranges (entries no slot
+    holds reduce to +0), both bit for bit against the oracle."""
+    from mxfp8_master_weight_gb300 import api
+    rng = np.random.default_rng(11)
+    S, rows, cols = 5, 96, 200
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    P = rr * 9 + 64 + cr * 203
+    garbage = np.abs(wl.normal_f32(rng, (S, P))) * np.float32(1e3)
+    ranges = []
+    for s in range(S):
+        for _ in range(3):
+            a = int(rng.integers(0, P))
+            b = int(min(P, a + rng.integers(0, P // 3)))
+            ranges.append((s, a, b))
+    ranges.append((2, 0, 8))  # touching ranges of one slot
+    ranges.append((2, 8, 40))
+    held = np.zeros((S, P), bool)
+    for s, a, b in ranges:
+        held[s, a:b] = True
+    zeroed = np.where(held, garbage, np.float32(0.0)).astype(np.float32)
+    if dtype == torch.bfloat16:
+        garbage, zeroed = wl.truncate_to_bf16_bits(garbage), wl.truncate_to_bf16_bits(zeroed)
+    want = oracle.max_reduce(zeroed)
+    slots = to_device(garbage).view(S, P)
+    reduced = torch.full((P,), 7.0, dtype=dtype, device="cuda")
+    vr = reduced[:rr * 9].view(rr, 9)
+    vc = reduced[rr * 9 + 64:].view(cr, 203)
+    sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
+    scl = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda")
+    api.mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, [(vr, vc, sr, scl, rows, cols)], ranges)
+    torch.cuda.synchronize()
+    got = to_host(reduced)
+    wf = want if dtype == torch.float32 else wl.bf16_bits_to_f32(want)
+    for o, ld, nr, nc, st in ((0, 9, rr, rc, sr), (rr * 9 + 64, 203, cr, cc, scl)):
+        g = got[o:o + nr * ld].reshape(nr, ld)[:, :nc]
+        w_ = want[o:o + nr * ld].reshape(nr, ld)[:, :nc]
+        assert np.array_equal(g.view(np.uint16 if dtype == torch.bfloat16 else np.uint32),
+                              w_.view(np.uint16 if dtype == torch.bfloat16 else np.uint32))
+        wf_ = wf[o:o + nr * ld].reshape(nr, ld)[:, :nc]
+        assert np.array_equal(to_host(st), oracle.e8m0_from_amax(wf_.astype(np.float64)))
+    with pytest.raises(Exception):
+        api.mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, [(vr, vc, sr, scl, rows, cols)],
+                                                       [(S, 0, 4)])  # no such slot
