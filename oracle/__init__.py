@@ -63,6 +63,25 @@ def _load():
             lib.oracle_e4m3_decode.restype = dbl
             lib.oracle_quantize.argtypes = [dbl, ctypes.c_uint8]
             lib.oracle_quantize.restype = ctypes.c_uint8
+            flt = ctypes.c_float
+            lib.oracle_e2m1_encode_array.argtypes = [vp, vp, i64]
+            lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_decode.restype = dbl
+            lib.oracle_nvfp4_tensor_scale.argtypes = [flt]
+            lib.oracle_nvfp4_tensor_scale.restype = flt
+            lib.oracle_nvfp4_block_scale.argtypes = [flt, flt]
+            lib.oracle_nvfp4_block_scale.restype = ctypes.c_uint8
+            lib.oracle_nvfp4_block_scale_array.argtypes = [vp, flt, vp, i64]
+            lib.oracle_nvfp4_multiplier.argtypes = [ctypes.c_uint8, flt]
+            lib.oracle_nvfp4_multiplier.restype = flt
+            lib.oracle_nvfp4_quantize.argtypes = [flt, flt]
+            lib.oracle_nvfp4_quantize.restype = ctypes.c_uint8
+            lib.oracle_nvfp4_partial_amax.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, vp, i64,
+                                                      vp, i64, vp]
+            lib.oracle_nvfp4_partial_amax.restype = ctypes.c_int
+            lib.oracle_nvfp4_update_scales.argtypes = [vp, i64, i64, i64, flt, vp, i64]
+            lib.oracle_nvfp4_partial_cast.argtypes = [vp, ctypes.c_int, i64, i64, i64, i64, vp, i64,
+                                                      vp, i64, flt, vp, vp, i64]
             _lib = lib
     return _lib
 
@@ -229,3 +248,110 @@ def full_cast(x: np.ndarray, rows: int, cols: int, colwise: bool = True, model: 
     q_c = np.zeros(rows * cols, np.uint8) if colwise else None
     partial_cast(x, rows, cols, 0, scale_r, scale_c, q_r, q_c, 0, model=model)
     return amax_r, amax_c, scale_r, scale_c, q_r, q_c
+
+
+# ---------------------------------------------------------------- NVFP4 (stated convention)
+# E2M1 data in 1x16 / 16x1 blocks with E4M3 block scales and one FP32 tensor scale
+# S = 2688 / G (G = tensor amax); see the NVFP4 section of mxfp8_oracle.c.
+
+def e2m1_encode(v: np.ndarray) -> np.ndarray:
+    """E2M1 codes (0..15) of float64 values: nearest, ties to the even code, saturate to 6."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, np.uint8)
+    _load().oracle_e2m1_encode_array(_ptr(v), _ptr(out), v.size)
+    return out
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.oracle_e2m1_decode(int(b)) for b in c.reshape(-1)]).reshape(c.shape)
+
+
+def nvfp4_tensor_scale(g: float) -> float:
+    return float(_load().oracle_nvfp4_tensor_scale(float(g)))
+
+
+def nvfp4_block_scales(amax: np.ndarray, s_enc: float) -> np.ndarray:
+    a = np.ascontiguousarray(amax, dtype=np.float32)
+    out = np.empty(a.shape, np.uint8)
+    _load().oracle_nvfp4_block_scale_array(_ptr(a), float(s_enc), _ptr(out), a.size)
+    return out
+
+
+def nvfp4_multiplier(s: int, s_enc: float) -> float:
+    return float(_load().oracle_nvfp4_multiplier(int(s), float(s_enc)))
+
+
+def nvfp4_quantize(y: float, m: float) -> int:
+    return int(_load().oracle_nvfp4_quantize(float(y), float(m)))
+
+
+def nvfp4_block_dims(rows: int, cols: int):
+    return (rows, (cols + 15) // 16), ((rows + 15) // 16, cols)
+
+
+def nvfp4_partial_amax(frag: np.ndarray, rows: int, cols: int, start: int, amax_r: np.ndarray,
+                       amax_c: np.ndarray | None, amax_t: np.ndarray) -> None:
+    """In place: FP32 1x16 / 16x1 block maxima of the fragment into amax_r / amax_c, and
+    amax_t[0] max-accumulated with the fragment's largest |x|."""
+    frag = _c(np.ascontiguousarray(frag))
+    for a in (amax_r, amax_c, amax_t):
+        if a is not None and (a.dtype != np.float32 or not a.flags.c_contiguous):
+            raise TypeError("NVFP4 amax buffers are contiguous float32")
+    rc = _load().oracle_nvfp4_partial_amax(_ptr(frag), _dtype_code(frag), rows, cols, start,
+                                           frag.size, _ptr(amax_r), amax_r.shape[1], _ptr(amax_c),
+                                           0 if amax_c is None else amax_c.shape[1], _ptr(amax_t))
+    if rc:
+        raise MemoryError("oracle_nvfp4_partial_amax could not allocate its accumulators")
+
+
+def nvfp4_update_scales(amax: np.ndarray, nrows: int, ncols: int, g: float, scale: np.ndarray) -> None:
+    _c(amax)
+    _c(scale)
+    if amax.dtype != np.float32:
+        raise TypeError("NVFP4 amax grids are float32")
+    _load().oracle_nvfp4_update_scales(_ptr(amax), nrows, ncols, amax.shape[1], float(g),
+                                       _ptr(scale), scale.shape[1])
+
+
+def nvfp4_partial_cast(frag: np.ndarray, rows: int, cols: int, start: int, scale_r: np.ndarray,
+                       scale_c: np.ndarray | None, g: float, out_r: np.ndarray,
+                       out_c: np.ndarray | None, out_offset: int) -> None:
+    """In place: E2M1 codes of the fragment into nibble out_offset + (k - start) of the
+    packed outputs (low nibble = even position)."""
+    frag = _c(np.ascontiguousarray(frag))
+    for o in (out_r, out_c):
+        if o is not None:
+            _c(o)
+            if 2 * o.size < out_offset + frag.size:
+                raise ValueError("output too small")
+    if out_c is not None and scale_c is None:
+        raise ValueError("columnwise scales are required for a columnwise output")
+    _load().oracle_nvfp4_partial_cast(_ptr(frag), _dtype_code(frag), rows, cols, start, frag.size,
+                                      _ptr(scale_r), scale_r.shape[1],
+                                      _ptr(scale_c) if out_c is not None else None,
+                                      scale_c.shape[1] if out_c is not None else 0, float(g),
+                                      _ptr(out_r), _ptr(out_c), out_offset)
+
+
+def nvfp4_full_cast(x: np.ndarray, rows: int, cols: int, colwise: bool = True):
+    """Whole-weight NVFP4 flow.  Returns (amax_r, amax_c, amax_t, scale_r, scale_c, q_r,
+    q_c); columnwise items None for a row-only weight; q_* packed, ceil(n/2) bytes."""
+    x = np.ascontiguousarray(x).reshape(-1)
+    rdim, cdim = nvfp4_block_dims(rows, cols)
+    amax_r = np.zeros(rdim, np.float32)
+    amax_c = np.zeros(cdim, np.float32) if colwise else None
+    amax_t = np.zeros(1, np.float32)
+    nvfp4_partial_amax(x, rows, cols, 0, amax_r, amax_c, amax_t)
+    scale_r = np.zeros(rdim, np.uint8)
+    nvfp4_update_scales(amax_r, *rdim, amax_t[0], scale_r)
+    scale_c = None
+    if colwise:
+        scale_c = np.zeros(cdim, np.uint8)
+        nvfp4_update_scales(amax_c, *cdim, amax_t[0], scale_c)
+    nbytes = (rows * cols + 1) // 2
+    q_r = np.zeros(nbytes, np.uint8)
+    q_c = np.zeros(nbytes, np.uint8) if colwise else None
+    nvfp4_partial_cast(x, rows, cols, 0, scale_r, scale_c, amax_t[0], q_r, q_c, 0)
+    return amax_r, amax_c, amax_t, scale_r, scale_c, q_r, q_c

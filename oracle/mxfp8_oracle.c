@@ -37,6 +37,7 @@
  *
  * dtype codes: 0 = FP32 (float), 1 = BF16 (uint16_t bit patterns).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -359,4 +360,183 @@ void oracle_f16_bits_array(const double *v, uint16_t *out, int64_t n) {
 
 void oracle_e8m0_array(const double *amax, uint8_t *out, int64_t n) {
     for (int64_t k = 0; k < n; ++k) out[k] = oracle_e8m0_from_amax(amax[k]);
+}
+
+/* ======================================================================== *
+ * NVFP4 partial cast.                                                       *
+ *                                                                           *
+ * The subject page excludes NVFP4 from its scope and prints no rule for it; *
+ * this section follows one stated convention (the NVFP4 format as NVIDIA    *
+ * defines it: E2M1 data, 16-value blocks with E4M3 scales, one FP32 scale   *
+ * per tensor), taking the same distributed steps as the MXFP8 path: partial *
+ * block maxima of each fragment, MAX reduction, scale update, partial cast. *
+ *                                                                           *
+ *   blocks   1x16 along rows (rowwise), 16x1 along columns (columnwise);    *
+ *   G        tensor amax = max |x| over the whole weight (FP32);            *
+ *   S        tensor encode scale = 2688 / G in FP32 (2688 = 448 * 6, the   *
+ *            largest E4M3 value times the largest E2M1 value); G == 0 gives *
+ *            S = 1, a quotient past the largest finite float gives that     *
+ *            largest finite float;                                          *
+ *   s        block scale = E4M3(fp32(fp32(A / 6) * S)) for block amax A,    *
+ *            nearest-even, saturating at 448;                               *
+ *   M        block multiplier = fp32(S / decode(s)), 0 when s decodes to 0; *
+ *   q        data = E2M1(fp32(y * M)), y the master value rounded to BF16,  *
+ *            nearest-even, saturating at 6.                                 *
+ * Every FP32 operation here is one correctly rounded IEEE single-precision *
+ * operation (float arithmetic, no contraction), so the integer codes are    *
+ * decided in the same precision as on the GPU.  Non-finite inputs are       *
+ * outside this convention (E2M1 has no NaN or infinity).                    *
+ * ======================================================================== */
+
+/* E2M1: sign bit, 2 exponent bits (bias 1), 1 mantissa bit.  Magnitudes 0, 0.5
+ * (subnormal), 1, 1.5, 2, 3, 4, 6; code = sign << 3 | exponent << 1 | mantissa.
+ * Round to nearest, ties to the even code, then saturate to 6. */
+uint8_t oracle_e2m1_encode(double v) {
+    if (isnan(v)) return 0x7;                  /* outside the convention; any fixed code */
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    double a = fabs(v);
+    double quantum = a < 2.0 ? 0.5 : (a < 4.0 ? 1.0 : 2.0);   /* spacing of the binade */
+    double r = nearbyint(a / quantum) * quantum;
+    if (r > 6.0) r = 6.0;
+    uint8_t mag;
+    if (r < 1.0) mag = (uint8_t)(r * 2.0);                      /* 0 -> 0, 0.5 -> 1 */
+    else {
+        int e = floor_log2(r);                                   /* 0, 1 or 2 */
+        int m = (int)(ldexp(r, -e) * 2.0) - 2;                   /* 0 or 1 */
+        mag = (uint8_t)(((e + 1) << 1) | m);
+    }
+    return sign | mag;
+}
+
+double oracle_e2m1_decode(uint8_t c) {
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = e == 0 ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return s ? -v : v;
+}
+
+float oracle_nvfp4_tensor_scale(float g) {
+    if (g == 0.0f) return 1.0f;
+    float s = 2688.0f / g;
+    if (isinf(s)) s = FLT_MAX;
+    return s;
+}
+
+uint8_t oracle_nvfp4_block_scale(float amax, float s_enc) {
+    float t = amax / 6.0f;
+    float u = t * s_enc;
+    return oracle_e4m3_encode((double)u);
+}
+
+float oracle_nvfp4_multiplier(uint8_t s, float s_enc) {
+    float d = (float)oracle_e4m3_decode(s);   /* exact: every E4M3 value is a float */
+    if (d == 0.0f) return 0.0f;
+    return s_enc / d;
+}
+
+uint8_t oracle_nvfp4_quantize(float y, float m) {
+    float p = y * m;
+    return oracle_e2m1_encode((double)p);
+}
+
+/* Row-wise (1x16) and column-wise (16x1) block maxima of |x| over the fragment
+ * [start, start+len) of a rows x cols weight, in FP32; blocks with at least one
+ * fragment element are overwritten, others untouched (as the MXFP8 partial amax).
+ * amax_t (one float) is max-accumulated with the fragment's largest |x|.
+ * amax_r: [rows][ld_r] (ld_r >= ceil(cols/16)); amax_c: [ceil(rows/16)][ld_c] or
+ * NULL. */
+int oracle_nvfp4_partial_amax(const void *frag, int dtype, int64_t rows, int64_t cols,
+                              int64_t start, int64_t len, float *amax_r, int64_t ld_r,
+                              float *amax_c, int64_t ld_c, float *amax_t) {
+    (void)rows;
+    if (len == 0) return 0;
+    int64_t r0 = start / cols, r1 = (start + len - 1) / cols;
+    int64_t c0 = r0 / 16, c1 = r1 / 16;
+    int64_t nbr = (cols + 15) / 16;
+    int64_t nr = r1 - r0 + 1, nc = c1 - c0 + 1;
+    double *acc_r = calloc((size_t)(nr * nbr), sizeof(double));
+    unsigned char *hit_r = calloc((size_t)(nr * nbr), 1);
+    double *acc_c = amax_c ? calloc((size_t)(nc * cols), sizeof(double)) : NULL;
+    unsigned char *hit_c = amax_c ? calloc((size_t)(nc * cols), 1) : NULL;
+    if (!acc_r || !hit_r || (amax_c && (!acc_c || !hit_c))) {
+        free(acc_r); free(hit_r); free(acc_c); free(hit_c);
+        return 1;
+    }
+    double tmax = 0.0;
+    for (int64_t k = start; k < start + len; ++k) {
+        int64_t i = k / cols, j = k % cols;
+        double a = fabs(load_value(frag, dtype, k - start));
+        if (isnan(a) || isnan(tmax)) tmax = NAN;
+        else if (a > tmax) tmax = a;
+        int64_t br = (i - r0) * nbr + j / 16;          /* row block (i, j/16) */
+        hit_r[br] = 1;
+        if (isnan(a) || isnan(acc_r[br])) acc_r[br] = NAN;
+        else if (a > acc_r[br]) acc_r[br] = a;
+        if (amax_c) {
+            int64_t bc = (i / 16 - c0) * cols + j;     /* column block (i/16, j) */
+            hit_c[bc] = 1;
+            if (isnan(a) || isnan(acc_c[bc])) acc_c[bc] = NAN;
+            else if (a > acc_c[bc]) acc_c[bc] = a;
+        }
+    }
+    for (int64_t i = r0; i <= r1; ++i)
+        for (int64_t b = 0; b < nbr; ++b)
+            if (hit_r[(i - r0) * nbr + b])
+                store_value(amax_r, ORACLE_F32, i * ld_r + b, acc_r[(i - r0) * nbr + b]);
+    if (amax_c)
+        for (int64_t c = c0; c <= c1; ++c)
+            for (int64_t j = 0; j < cols; ++j)
+                if (hit_c[(c - c0) * cols + j])
+                    store_value(amax_c, ORACLE_F32, c * ld_c + j, acc_c[(c - c0) * cols + j]);
+    double prev = (double)*amax_t;
+    if (isnan(prev) || isnan(tmax)) store_value(amax_t, ORACLE_F32, 0, NAN);
+    else if (tmax > prev) store_value(amax_t, ORACLE_F32, 0, tmax);
+    free(acc_r); free(hit_r); free(acc_c); free(hit_c);
+    return 0;
+}
+
+/* scale[r][c] = E4M3 block scale of amax[r][c] under tensor amax g, r < nrows, c < ncols. */
+int oracle_nvfp4_update_scales(const float *amax, int64_t nrows, int64_t ncols, int64_t ld_a,
+                               float g, uint8_t *scale, int64_t ld_s) {
+    float s_enc = oracle_nvfp4_tensor_scale(g);
+    for (int64_t r = 0; r < nrows; ++r)
+        for (int64_t c = 0; c < ncols; ++c)
+            scale[r * ld_s + c] = oracle_nvfp4_block_scale(amax[r * ld_a + c], s_enc);
+    return 0;
+}
+
+/* Write E2M1 code q into nibble p of a packed buffer (low nibble = even position). */
+static void put_nibble(uint8_t *buf, int64_t p, uint8_t q) {
+    uint8_t *b = buf + p / 2;
+    if (p % 2 == 0) *b = (uint8_t)((*b & 0xF0) | q);
+    else *b = (uint8_t)((*b & 0x0F) | (q << 4));
+}
+
+/* For every fragment element k (element (i, j)): y = BF16 rounding of x (identity for
+ * BF16 input); rowwise code with the scale of row block (i, j/16), columnwise code
+ * (when out_c is non-NULL) with the scale of column block (i/16, j); each written to
+ * nibble out_offset + (k - start) of its output; nothing else is written. */
+int oracle_nvfp4_partial_cast(const void *frag, int dtype, int64_t rows, int64_t cols,
+                              int64_t start, int64_t len, const uint8_t *scale_r, int64_t ld_sr,
+                              const uint8_t *scale_c, int64_t ld_sc, float g,
+                              uint8_t *out_r, uint8_t *out_c, int64_t out_offset) {
+    (void)rows;
+    float s_enc = oracle_nvfp4_tensor_scale(g);
+    for (int64_t k = start; k < start + len; ++k) {
+        int64_t i = k / cols, j = k % cols;
+        double x = load_value(frag, dtype, k - start);
+        float y = (float)((dtype == ORACLE_F32) ? oracle_bf16_round((float)x) : x);
+        int64_t p = out_offset + (k - start);
+        put_nibble(out_r, p, oracle_nvfp4_quantize(y, oracle_nvfp4_multiplier(scale_r[i * ld_sr + j / 16], s_enc)));
+        if (out_c)
+            put_nibble(out_c, p, oracle_nvfp4_quantize(y, oracle_nvfp4_multiplier(scale_c[(i / 16) * ld_sc + j], s_enc)));
+    }
+    return 0;
+}
+
+void oracle_e2m1_encode_array(const double *v, uint8_t *out, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_e2m1_encode(v[k]);
+}
+
+void oracle_nvfp4_block_scale_array(const float *amax, float s_enc, uint8_t *out, int64_t n) {
+    for (int64_t k = 0; k < n; ++k) out[k] = oracle_nvfp4_block_scale(amax[k], s_enc);
 }

@@ -39,13 +39,17 @@ MUTATIONS = {
     "scale exponent off by one": (
         "return ldexp(y, 127 - (int)s);", "return ldexp(y, 126 - (int)s);"),
     "first fragment element dropped from the amax": (
-        "    for (int64_t k = start; k < start + len; ++k) {\n        int64_t i = k / cols, j = k % cols;\n        double a = fabs(",
-        "    for (int64_t k = start + 1; k < start + len; ++k) {\n        int64_t i = k / cols, j = k % cols;\n        double a = fabs("),
+        "    for (int64_t k = start; k < start + len; ++k) {\n        int64_t i = k / cols, j = k % cols;\n        double a = fabs(load_value(frag, dtype, k - start));\n        int64_t br = (i - r0) * nbr + j / 32;",
+        "    for (int64_t k = start + 1; k < start + len; ++k) {\n        int64_t i = k / cols, j = k % cols;\n        double a = fabs(load_value(frag, dtype, k - start));\n        int64_t br = (i - r0) * nbr + j / 32;"),
     "rowwise data scaled by the columnwise scale": (
         "out_r[o] = oracle_quantize(y, scale_r[i * ld_sr + j / 32]);",
         "out_r[o] = oracle_quantize(y, scale_c ? scale_c[(i / 32) * ld_sc + j] : scale_r[i * ld_sr + j / 32]);"),
     "untouched row blocks overwritten": (
-        "            if (hit_r[(i - r0) * nbr + b])", "            if (1)"),
+        "            if (hit_r[(i - r0) * nbr + b])\n                store_value(amax_r, dtype,",
+        "            if (1)\n                store_value(amax_r, dtype,"),
+    "nvfp4 untouched row blocks overwritten": (
+        "            if (hit_r[(i - r0) * nbr + b])\n                store_value(amax_r, ORACLE_F32,",
+        "            if (1)\n                store_value(amax_r, ORACLE_F32,"),
     "NaN not propagated by the reduction": (
         "            if (isnan(a) || isnan(m)) m = NAN;", "            if (isnan(m)) m = NAN;"),
     "GEMM layout with row fields swapped": (
@@ -75,9 +79,34 @@ MUTATIONS = {
     "scale update with the leading dimensions swapped": (
         "scale[r * ld_s + c] = oracle_e8m0_from_amax(load_value(amax, dtype, r * ld_a + c));",
         "scale[r * ld_a + c] = oracle_e8m0_from_amax(load_value(amax, dtype, r * ld_s + c));"),
+    "e2m1 ties away from zero": (
+        "    double r = nearbyint(a / quantum) * quantum;\n    if (r > 6.0)",
+        "    double r = round(a / quantum) * quantum;\n    if (r > 6.0)"),
+    "e2m1 saturates to the wrong code": (
+        "    if (r > 6.0) r = 6.0;", "    if (r > 6.0) r = 4.0;"),
+    "nvfp4 tensor scale with 448 * 8": (
+        "float s = 2688.0f / g;", "float s = 3584.0f / g;"),
+    "nvfp4 zero tensor amax gives scale 0": (
+        "if (g == 0.0f) return 1.0f;", "if (g == 0.0f) return 0.0f;"),
+    "nvfp4 block scale divides by 4": (
+        "float t = amax / 6.0f;", "float t = amax / 4.0f;"),
+    "nvfp4 multiplier inverted": (
+        "return s_enc / d;", "return d / s_enc;"),
+    "nvfp4 row blocks of 32": (
+        "int64_t br = (i - r0) * nbr + j / 16;", "int64_t br = (i - r0) * nbr + j / 32;"),
+    "nvfp4 column blocks of 32 rows": (
+        "int64_t bc = (i / 16 - c0) * cols + j;", "int64_t bc = (i / 32 - c0 / 2) * cols + j;"),
+    "nvfp4 nibbles swapped": (
+        "if (p % 2 == 0) *b", "if (p % 2 != 0) *b"),
+    "nvfp4 cast skips the BF16 rounding": (
+        "float y = (float)((dtype == ORACLE_F32) ? oracle_bf16_round((float)x) : x);",
+        "float y = (float)x;"),
+    "nvfp4 tensor amax misses the first element": (
+        "        if (isnan(a) || isnan(tmax)) tmax = NAN;\n        else if (a > tmax) tmax = a;",
+        "        if (k > start) { if (isnan(a) || isnan(tmax)) tmax = NAN;\n        else if (a > tmax) tmax = a; }"),
     "amax column index shifted by one": (
-        "        int64_t i = k / cols, j = k % cols;\n        double a = fabs(",
-        "        int64_t i = k / cols, j = (k + 1) % cols;\n        double a = fabs("),
+        "        int64_t i = k / cols, j = k % cols;\n        double a = fabs(load_value(frag, dtype, k - start));\n        int64_t br = (i - r0) * nbr + j / 32;",
+        "        int64_t i = k / cols, j = (k + 1) % cols;\n        double a = fabs(load_value(frag, dtype, k - start));\n        int64_t br = (i - r0) * nbr + j / 32;"),
 }
 
 

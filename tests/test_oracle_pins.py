@@ -504,3 +504,230 @@ def test_nan_amax_is_the_canonical_quiet_nan(oracle_mod):
         slots[2, 2] = 7.0
         red = oracle_mod.max_reduce(slots)
         assert red.view(np.uint32)[2] == 0x7FC00000 and red[0] == 0.0, hex(pat)
+
+
+# ------------------------------------------------------------------ NVFP4 (stated convention)
+
+def _e2m1_table():
+    """The 8 non-negative E2M1 values, from the format definition (bias 1, 1 mantissa bit)."""
+    vals = []
+    for c in range(8):
+        e, m = c >> 1, c & 1
+        vals.append(0.5 * m if e == 0 else (1 + m / 2) * 2.0 ** (e - 1))
+    return np.array(vals)
+
+
+def _e2m1_brute(v):
+    table = _e2m1_table()
+    out = np.empty(v.shape, np.uint8)
+    for k, x in enumerate(v):
+        a = min(abs(x), 6.0)
+        d = np.abs(table - a)
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        out[k] = code | (0x8 if np.signbit(x) else 0)
+    return out
+
+
+def test_e2m1_golden(oracle_mod):
+    for val, code in _golden_rows("e2m1_points.txt"):
+        got = int(oracle_mod.e2m1_encode(np.array([float(val)]))[0])
+        assert got == int(code, 16), (val, hex(got), code)
+
+
+def test_e2m1_vs_brute_force(oracle_mod):
+    table = _e2m1_table()
+    mids = (table[1:] + table[:-1]) / 2
+    rng = np.random.default_rng(41)
+    v = np.concatenate([table, mids, np.nextafter(mids, 0), np.nextafter(mids, 10), -table, -mids,
+                        rng.uniform(-8, 8, 20000), rng.uniform(-0.6, 0.6, 5000),
+                        [6.5, 7.0, 7.5, 8.0, 1e30, -1e30, -0.0]])
+    assert np.array_equal(oracle_mod.e2m1_encode(v), _e2m1_brute(v))
+    for c in range(16):  # every code decodes to its value and encodes back
+        d = float(oracle_mod.e2m1_decode(c))
+        assert d == (-1 if c & 8 else 1) * table[c & 7]
+        assert int(oracle_mod.e2m1_encode(np.array([d]))[0]) == c
+
+
+def test_nvfp4_tensor_scale_special_cases(oracle_mod):
+    """S = 2688 / G: exact for G = 2688 * 2^k and for divisors of 2688; 1 for G = 0;
+    the largest float when the quotient overflows."""
+    for k in range(-20, 21):
+        assert oracle_mod.nvfp4_tensor_scale(2688.0 * 2.0 ** k) == 2.0 ** -k
+    assert oracle_mod.nvfp4_tensor_scale(448.0) == 6.0
+    assert oracle_mod.nvfp4_tensor_scale(12.0) == 224.0
+    assert oracle_mod.nvfp4_tensor_scale(0.0) == 1.0
+    assert oracle_mod.nvfp4_tensor_scale(1e-40) == float(np.finfo(np.float32).max)
+
+
+def test_nvfp4_block_scale_points_and_bound(oracle_mod):
+    s224 = np.float32(224.0)
+    got = oracle_mod.nvfp4_block_scales(np.array([6.0, 3.0, 12.0, 0.0, 1e-3], np.float32), s224)
+    # 224 = 1.75*2^7, 112 = 1.75*2^6, 448 = 1.75*2^8; 1e-3/6*224 = 0.03733 -> 1.25*2^-5
+    assert list(got) == [0x76, 0x6E, 0x7E, 0x00, 0x12]
+    # the block holding the tensor maximum always gets the largest E4M3 scale, 448
+    rng = np.random.default_rng(42)
+    g = np.float32(np.abs(rng.standard_normal(200)) * 10.0 ** rng.uniform(-30, 30, 200)).astype(np.float32)
+    for gv in g:
+        s = oracle_mod.nvfp4_tensor_scale(gv)
+        assert int(oracle_mod.nvfp4_block_scales(np.array([gv], np.float32), s)[0]) == 0x7E, gv
+    # every block scale is the E4M3 value nearest A*S/6 (within half a unit of E4M3)
+    a = np.float32(rng.uniform(0, 1, 5000)) * np.float32(12.0)
+    sc = oracle_mod.nvfp4_block_scales(a.astype(np.float32), s224)
+    dec = oracle_mod.e4m3_decode(sc)
+    u = a.astype(np.float64) / 6 * 224
+    table = np.array(sorted(set(oracle_mod.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).tolist())))
+    nearest = table[np.abs(table[None, :] - u[:, None]).argmin(axis=1)]
+    assert np.all(np.abs(dec - u) <= np.abs(nearest - u) + 1e-9 * u)
+
+
+def test_nvfp4_worked_block(oracle_mod):
+    rows = _golden_rows("nvfp4_worked_block.txt")
+    vals = np.array([float(v) for v, _ in rows], np.float32)
+    codes = np.array([int(c, 16) for _, c in rows], np.uint8)
+    with open(os.path.join(GOLDEN, "nvfp4_worked_block.txt")) as f:
+        scales = [int(t, 16) for t in next(l for l in f if l.startswith("scale")).split()[1:]]
+    ar, ac, at, sr, sc, qr, qc = oracle_mod.nvfp4_full_cast(vals, 1, 48, False)
+    assert at[0] == 12.0 and list(ar[0]) == [6.0, 3.0, 12.0]
+    assert list(sr[0]) == scales
+    nib = np.stack([qr & 0xF, qr >> 4], axis=1).reshape(-1)
+    assert np.array_equal(nib, codes)
+
+
+def _nvfp4_inputs(rng, rows, cols, spread=2.0):
+    n = rows * cols
+    return (wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-spread, spread, n).astype(np.float32))
+
+
+def _nibbles(q, n):
+    return np.stack([q & 0xF, q >> 4], axis=1).reshape(-1)[:n]
+
+
+def test_nvfp4_partial_amax_brute_force(oracle_mod):
+    """Block membership by dicts of members (no index algebra), 1x16 and 16x1 blocks,
+    and the tensor amax as the maximum over every fragment element."""
+    rng = np.random.default_rng(43)
+    for rows, cols in ((40, 38), (33, 16), (17, 70)):
+        n = rows * cols
+        x = np.abs(_nvfp4_inputs(rng, rows, cols))
+        for start, length in [(0, n), (3, n // 2), (n - 7, 7), (cols + 5, 2 * cols)]:
+            frag = x[start:start + length]
+            (rr, rc), (cr, cc) = oracle_mod.nvfp4_block_dims(rows, cols)
+            ar = np.full((rr, rc), -1.0, np.float32)
+            ac = np.full((cr, cc), -1.0, np.float32)
+            at = np.array([0.5], np.float32)
+            oracle_mod.nvfp4_partial_amax(frag, rows, cols, start, ar, ac, at)
+            rb, cb = {}, {}
+            for k in range(start, start + length):
+                i, j = k // cols, k % cols
+                rb.setdefault((i, j // 16), []).append(x[k])
+                cb.setdefault((i // 16, j), []).append(x[k])
+            want_r = np.full((rr, rc), -1.0, np.float32)
+            want_c = np.full((cr, cc), -1.0, np.float32)
+            for (i, b), m in rb.items():
+                want_r[i, b] = max(m)
+            for (c, j), m in cb.items():
+                want_c[c, j] = max(m)
+            assert np.array_equal(ar, want_r) and np.array_equal(ac, want_c)
+            assert at[0] == max(0.5, frag.max())
+
+
+def test_nvfp4_cast_invariants_and_error_bound(oracle_mod):
+    """On a whole weight: every block whose scale is a normal E4M3 value has its largest
+    element at E2M1 6 (the scale maps the block maximum near 6); every code is the
+    E2M1 value nearest y*M (within the FP32 rounding of the product); the dequantised
+    value decode(q) * decode(s) / S lies within half an E2M1 spacing (scaled) of y."""
+    rng = np.random.default_rng(44)
+    rows, cols = 48, 80
+    x = _nvfp4_inputs(rng, rows, cols)
+    ar, ac, at, sr, sc, qr, qc = oracle_mod.nvfp4_full_cast(x, rows, cols, True)
+    s_enc = oracle_mod.nvfp4_tensor_scale(at[0])
+    y = wl.bf16_bits_to_f32(oracle_mod.bf16_rne_bits(x)).astype(np.float64).reshape(rows, cols)
+    table = _e2m1_table()
+    for name, q, sgrid, blk in (("row", qr, sr, lambda i, j: (i, j // 16)),
+                                ("col", qc, sc, lambda i, j: (i // 16, j))):
+        codes = _nibbles(q, rows * cols).reshape(rows, cols)
+        vals = oracle_mod.e2m1_decode(codes)
+        groups = {}
+        for i in range(rows):
+            for j in range(cols):
+                groups.setdefault(blk(i, j), []).append((i, j))
+        for b, members in groups.items():
+            s = int(sgrid[b])
+            d = float(oracle_mod.e4m3_decode(np.array([s], np.uint8))[0])
+            m = oracle_mod.nvfp4_multiplier(s, s_enc)
+            if d >= 2.0 ** -6:
+                assert max(abs(vals[i, j]) for i, j in members) == 6.0, (name, b)
+            for i, j in members:
+                p = y[i, j] * m
+                spacing = 0.5 if abs(p) < 2 else (1.0 if abs(p) < 4 else 2.0)
+                if abs(p) <= 6.0:
+                    assert abs(abs(vals[i, j]) - abs(p)) <= spacing / 2 * (1 + 1e-6), (name, i, j)
+                    assert abs(vals[i, j] * d / s_enc - y[i, j]) <= spacing / 2 * d / s_enc * (1 + 1e-5) + 1e-30
+                assert np.signbit(vals[i, j]) == np.signbit(y[i, j]) or vals[i, j] == 0 and codes[i, j] in (0, 8)
+
+
+def test_nvfp4_union_row_only_and_empty_fragment(oracle_mod):
+    """Fragments with their own amax slots, MAX-reduced, give the whole-weight result bit
+    for bit (full-size and fragment-size outputs); the row-only result is the rowwise
+    half; an empty fragment writes nothing; a boundary inside a 16-value block gives the
+    whole-block scale after the reduction."""
+    rng = np.random.default_rng(45)
+    rows, cols = 40, 48
+    n = rows * cols
+    x = _nvfp4_inputs(rng, rows, cols)
+    full = oracle_mod.nvfp4_full_cast(x, rows, cols, True)
+    cuts = [0, 6, 6, 16 * cols + 10, n - 2, n]   # an empty fragment; boundaries inside blocks
+    (rr, rc), (cr, cc) = oracle_mod.nvfp4_block_dims(rows, cols)
+    slots_r = np.zeros((len(cuts) - 1, rr, rc), np.float32)
+    slots_c = np.zeros((len(cuts) - 1, cr, cc), np.float32)
+    slots_t = np.zeros((len(cuts) - 1, 1), np.float32)
+    for s, (a, b) in enumerate(zip(cuts[:-1], cuts[1:])):
+        oracle_mod.nvfp4_partial_amax(x[a:b], rows, cols, a, slots_r[s], slots_c[s], slots_t[s])
+    red_r = oracle_mod.max_reduce(slots_r.reshape(len(cuts) - 1, -1)).reshape(rr, rc)
+    red_c = oracle_mod.max_reduce(slots_c.reshape(len(cuts) - 1, -1)).reshape(cr, cc)
+    g = oracle_mod.max_reduce(slots_t)[0]
+    assert g == full[2][0] and np.array_equal(red_r, full[0]) and np.array_equal(red_c, full[1])
+    sr = np.zeros((rr, rc), np.uint8)
+    sc = np.zeros((cr, cc), np.uint8)
+    oracle_mod.nvfp4_update_scales(red_r, rr, rc, g, sr)
+    oracle_mod.nvfp4_update_scales(red_c, cr, cc, g, sc)
+    assert np.array_equal(sr, full[3]) and np.array_equal(sc, full[4])
+    qr = np.full(n // 2, 0xA5, np.uint8)
+    qc = np.full(n // 2, 0xA5, np.uint8)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        before = (qr.copy(), qc.copy())
+        oracle_mod.nvfp4_partial_cast(x[a:b], rows, cols, a, sr, sc, g, qr, qc, a)
+        if a == b:
+            assert np.array_equal(before[0], qr) and np.array_equal(before[1], qc)
+        # fragment-size output: the same codes, packed from nibble 0
+        fr = np.full((b - a + 1) // 2, 0x5A, np.uint8)
+        oracle_mod.nvfp4_partial_cast(x[a:b], rows, cols, a, sr, None, g, fr, None, 0)
+        assert np.array_equal(_nibbles(fr, b - a), _nibbles(full[5], n)[a:b])
+    assert np.array_equal(qr, full[5]) and np.array_equal(qc, full[6])
+    ro = oracle_mod.nvfp4_full_cast(x, rows, cols, False)
+    assert np.array_equal(ro[5], full[5]) and np.array_equal(ro[3], full[3]) and ro[6] is None
+
+
+def test_nvfp4_bf16_input_is_not_rounded_again(oracle_mod):
+    rng = np.random.default_rng(46)
+    x = _nvfp4_inputs(rng, 32, 64)
+    xb = oracle_mod.bf16_rne_bits(x)
+    xf = wl.bf16_bits_to_f32(xb)
+    a = oracle_mod.nvfp4_full_cast(xb, 32, 64, True)
+    b = oracle_mod.nvfp4_full_cast(xf, 32, 64, True)
+    for k in (0, 1, 2, 3, 4, 5, 6):
+        assert np.array_equal(a[k], b[k]), k
+
+
+def test_nvfp4_rounds_through_bf16_first(oracle_mod):
+    """FP32 values just below an E2M1 midpoint whose BF16 rounding lands on it: the code
+    follows the BF16 value (ties to even), not the FP32 one.  G = 6 gives S = 448 and a
+    block scale of 448, so the multiplier is 1."""
+    x = np.zeros(16, np.float32)
+    x[:4] = [6.0, 0.7499, 1.7499, -4.9999]  # BF16: 0.75, 1.75, -5.0
+    ar, ac, at, sr, sc, qr, qc = oracle_mod.nvfp4_full_cast(x, 1, 16, False)
+    assert at[0] == 6.0 and sr[0, 0] == 0x7E
+    assert oracle_mod.nvfp4_multiplier(0x7E, oracle_mod.nvfp4_tensor_scale(6.0)) == 1.0
+    # 0.75 -> 1.0 (code 2), 1.75 -> 2.0 (code 4), -5.0 -> -4 (code 0xE)
+    assert list(_nibbles(qr, 4)) == [0x7, 0x2, 0x4, 0xE]
