@@ -65,24 +65,14 @@ def algorithmic_bytes(n: int, s_in: int = 4, colwise: bool = True) -> dict:
     }
 
 
-def sharded_step_bytes(specs, num_slots: int, packed_entries: int, s_in: int = 4) -> int:
-    """Compulsory HBM bytes of one multi-fragment driver step: every fragment's input and
-    block maxima, the packed slots read and the reduced amax + E8M0 bytes written, and
-    every fragment's input, scales and E4M3 outputs."""
-    total = 0
-    for sp in specs:
-        n = sp.rows * sp.cols
-        dirs = 2 if sp.colwise else 1
-        blocks = dirs * n // 32
-        total += n * s_in + blocks * s_in            # amax
-        total += n * s_in + blocks + dirs * n        # cast
-    total += num_slots * packed_entries * s_in       # reduction reads every slot
-    total += packed_entries * s_in + packed_entries  # reduced amax + scale bytes
-    return total
-
-
-def sharded_phase_bytes(specs, num_slots: int, packed_entries: int, s_in: int = 4) -> dict:
-    """sharded_step_bytes split by phase: amax, reduction + scales, cast."""
+def sharded_phase_bytes(specs, num_slots: int, packed_entries: int, s_in: int = 4,
+                        slot_entries_read: int | None = None) -> dict:
+    """Compulsory HBM bytes of one multi-fragment driver step by phase: every fragment's
+    input and block maxima (amax); the slot entries the reduction reads and the reduced
+    amax + E8M0 bytes it writes (reduce_scales); every fragment's input, scales and E4M3
+    outputs (cast).  The reduction reads every slot in full (num_slots * packed_entries
+    entries) unless `slot_entries_read` gives the entries the slots hold (the ranged
+    reduction reads a slot only where its shard's amax wrote)."""
     amax = cast = 0
     for sp in specs:
         n = sp.rows * sp.cols
@@ -90,8 +80,15 @@ def sharded_phase_bytes(specs, num_slots: int, packed_entries: int, s_in: int = 
         blocks = dirs * n // 32
         amax += n * s_in + blocks * s_in
         cast += n * s_in + blocks + dirs * n
-    red = num_slots * packed_entries * s_in + packed_entries * s_in + packed_entries
+    reads = num_slots * packed_entries if slot_entries_read is None else slot_entries_read
+    red = reads * s_in + packed_entries * s_in + packed_entries
     return {"amax": amax, "reduce_scales": red, "cast": cast}
+
+
+def sharded_step_bytes(specs, num_slots: int, packed_entries: int, s_in: int = 4,
+                       slot_entries_read: int | None = None) -> int:
+    """Total of sharded_phase_bytes."""
+    return sum(sharded_phase_bytes(specs, num_slots, packed_entries, s_in, slot_entries_read).values())
 
 
 def measured_peak():
@@ -447,6 +444,50 @@ def stats(samples) -> dict:
 KERNEL_SAMPLES = 256  # in-step samples per kernel, whatever --steps is
 
 
+def nvfp4_algorithmic_bytes(n: int, s_in: int = 4, colwise: bool = True) -> dict:
+    """Compulsory HBM bytes per call of the NVFP4 kernels for an n-element fragment: F32
+    1x16 / 16x1 block amaxes, E4M3 block scales, two E2M1 codes per byte."""
+    dirs = 2 if colwise else 1
+    blocks = dirs * n // 16
+    return {"amax": n * s_in + 4 * blocks,                # read x, write F32 block amaxes
+            "scales": 4 * blocks + blocks,                # read block amaxes, write E4M3 bytes
+            "cast": n * s_in + blocks + dirs * n // 2}    # read x and scales, write codes
+
+
+def measure_nvfp4(x, dev, peak: float, frac_key: str) -> dict:
+    """The NVFP4 steps on the headline weight (16384x6144 FP32, both directions): partial
+    amax, scale update, partial cast, each timed like other_configs (graphs of 10 calls,
+    20 replays, 7 rounds, median); the input is larger than L2, so these are HBM figures."""
+    import torch
+
+    from mxfp8_master_weight_gb300 import api
+
+    (rr, rc), (cr, cc) = api.nvfp4_block_shapes(ROWS, COLS)
+    ar = torch.zeros((rr, rc), device=dev)
+    ac = torch.zeros((cr, cc), device=dev)
+    at = torch.zeros(1, device=dev)
+    sr = torch.empty((rr, rc), dtype=torch.uint8, device=dev)
+    scl = torch.empty((cr, cc), dtype=torch.uint8, device=dev)
+    qr = torch.empty(ROWS * COLS // 2, dtype=torch.uint8, device=dev)
+    qc = torch.empty(ROWS * COLS // 2, dtype=torch.uint8, device=dev)
+    calls = {"amax": api.prepare_nvfp4_partial_amax(x, ar, ac, at, ROWS, COLS, 0),
+             "scales": api.prepare_nvfp4_update_scales(ar, ac, at, sr, scl, ROWS, COLS),
+             "cast": api.prepare_nvfp4_partial_cast(x, sr, scl, at, qr, qc, ROWS, COLS, 0)}
+    stream = torch.cuda.current_stream(dev)
+    for c in calls.values():
+        c.call(stream)
+    nb = nvfp4_algorithmic_bytes(ROWS * COLS)
+    out = {"workload": "16384x6144 FP32 headline weight, full fragment, rowwise+columnwise NVFP4 "
+                       "(E2M1, 16-value blocks with E4M3 scales, F32 tensor scale)",
+           "method": "CUDA graph of 10 calls, 20 replays per round, 7 rounds, median us per call"}
+    for nm, c in calls.items():
+        us = graph_us_per_call(c, stream, ROWS * COLS)
+        gbs = nb[nm] / (us * 1e-6) / 1e9
+        out[nm] = {"us_per_call": round(us, 3), "algorithmic_bytes": nb[nm], "gbs": round(gbs, 1),
+                   frac_key: round(gbs / peak, 4)}
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -539,9 +580,12 @@ def run_ours(args):
     g1.record(stream)
     torch.cuda.synchronize()
     b_us = g0.elapsed_time(g1) * 1e3 / b_steps
-    b_bytes = sharded_step_bytes(bspecs, bsc.num_shards, bsc.layout.total)
-    b_phase_bytes = sharded_phase_bytes(bspecs, bsc.num_shards, bsc.layout.total)
+    held = sum(e - a for _, a, e in bsc.ranges) if bsc.ranged else None
+    b_bytes = sharded_step_bytes(bspecs, bsc.num_shards, bsc.layout.total, slot_entries_read=held)
+    b_phase_bytes = sharded_phase_bytes(bspecs, bsc.num_shards, bsc.layout.total,
+                                        slot_entries_read=held)
     bsc_launches = bsc.launches_per_step()
+    bsc_ranged = bsc.ranged
     # per-phase split of the sharded step (events around the phases of sampled steps)
     phase_samples = sample_phases(lambda events=None: bsc.step(bshards, events=events), 64)
     b_phases = {}
@@ -551,6 +595,8 @@ def run_ours(args):
                         "gbs": round(b_phase_bytes[nm] / (med * 1e-6) / 1e9, 1)}
     del bshards, bsc, batch
     configs = measure_configs(x, dev)
+    peak, peak_kind = measured_peak()
+    nvfp4 = measure_nvfp4(x, dev, peak, "frac_of_" + peak_kind + "_peak")
 
     # End to end through the public API with host buffers, every step copying the 402.7 MB
     # input in from pinned host memory and both E4M3 outputs and both scale grids back.
@@ -661,6 +707,9 @@ def run_ours(args):
             "workload": "7 FP32 weights (8192x8192; 4096x4096 / 2048x8192, 3 row-only, 4 "
                         "bidirectional; 167.8M elements), 4 emulated shards in own buffers",
             "launches_per_step": bsc_launches, "steps": b_steps,
+            "reduction": (f"ranged: reads the {held} slot entries the shards' amax wrote "
+                          f"(of {bsc.num_shards} x {bsc.layout.total}); slots never zeroed"
+                          if bsc_ranged else "whole slots, zeroed before each step"),
             "us_per_step": round(b_us, 2), "phases": b_phases, "algorithmic_bytes": b_bytes,
             "gbs": round(b_bytes / (b_us * 1e-6) / 1e9, 1),
             frac_key: round(b_bytes / (b_us * 1e-6) / 1e9 / peak, 4)},
@@ -680,6 +729,7 @@ def run_ours(args):
                          "path": f"HostQuantizer: {len(hq.chunks)} chunks of {hq.chunk_rows} rows, "
                                  "3 streams, one-pass kernel per chunk",
                          "copy_gbs": round((h2d + d2h) * e2e_steps / hq_t / 1e9, 1)},
+        "nvfp4": nvfp4,
         "other_configs": {
             "method": "CUDA graph of 50 calls (fragments <= 4M elements) else 10, 20 replays per "
                       "round, 7 rounds, median us per call; outputs checked bitwise in the tests",

@@ -380,6 +380,75 @@ MXFP8_API int mxfp8_sharded_update_noalloc(const mxfp8_tensor* fragments, const 
                                  mxfp8_tensor* output_colwise, int64_t rows, int64_t cols,
                                  void* stream);
 
+/*
+ * NVFP4 partial cast.  The same distributed steps as the MXFP8 entry points above (partial
+ * amax of a fragment, MAX reduction of the packed amaxes over ranks with
+ * mxfp8_amax_max_reduce on F32 slots, scale update, partial cast in place) for the NVFP4
+ * format.  The page "Support row-only MXFP8 distributed master-weight casts" leaves NVFP4
+ * out of its scope (section "Scope") and gives no rule for it; the convention is:
+ *   blocks   1x16 along rows (rowwise), 16x1 along columns (columnwise);
+ *   G        tensor amax: max |x| over the whole weight, F32;
+ *   S        tensor encode scale 2688 / G in F32 (448 * 6); 1 when G == 0; the largest
+ *            finite float when the quotient overflows;
+ *   s        block scale byte: E4M3(fp32(fp32(A / 6) * S)), A the block amax
+ *            (nearest-even, saturating at 448);
+ *   data     E2M1(fp32(y * fp32(S / decode(s)))) (0 when s decodes to 0), y = x rounded
+ *            to BF16 (nearest-even; identity for BF16 input); E2M1 has magnitudes 0,
+ *            0.5, 1, 1.5, 2, 3, 4, 6 (codes 0-7, sign in bit 3), nearest-even,
+ *            saturating at 6.  Two codes per byte: element at nibble position p sits in
+ *            byte p / 2, the low nibble holding even p.
+ * Each F32 step is one correctly rounded operation.  Non-finite inputs are outside the
+ * convention (E2M1 has no NaN or infinity): their codes are unspecified.  A consumer
+ * dequantises a code q of block scale s as decode(q) * decode(s) / S.
+ */
+
+/*
+ * input         [in]     fragment as for mxfp8_partial_amax (F32 or BF16).
+ * amax_rowwise  [in,out] REQUIRED F32 [>= rows][>= ceil(cols/16)]: entry (i, b) = max |x|
+ *                        over the fragment's elements of row i, columns [16b, 16b+16).
+ * amax_colwise  [in,out] OPTIONAL F32 [>= ceil(rows/16)][>= cols]: entry (c, j) over
+ *                        rows [16c, 16c+16) of column j; empty => row-only.
+ * amax_tensor   [in,out] REQUIRED F32, at least 1 element: element 0 is max-accumulated
+ *                        with the fragment's largest |x| (it must hold +0 or a previous
+ *                        maximum: initialise it to +0 before the first fragment).
+ * Entries of blocks the fragment touches are overwritten, others untouched; NaN
+ * members give the canonical quiet NaN.  Errors as mxfp8_partial_amax; 4 also for a
+ * missing amax_tensor; 3 if an amax tensor is not F32.
+ */
+MXFP8_API int nvfp4_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+                       mxfp8_tensor* amax_colwise, mxfp8_tensor* amax_tensor, int64_t rows,
+                       int64_t cols, int64_t start_offset, void* stream);
+
+/*
+ * amax_rowwise [in] REQUIRED F32 [>= rows][>= ceil(cols/16)] (reduced over ranks);
+ * amax_colwise [in] OPTIONAL F32 [>= ceil(rows/16)][>= cols]; empty => no columnwise scales;
+ * amax_tensor  [in] REQUIRED F32: element 0 is G;
+ * scale_rowwise [out] REQUIRED U8 [>= rows][>= ceil(cols/16)] E4M3 block scales;
+ * scale_colwise [out] U8 [>= ceil(rows/16)][>= cols]; required iff amax_colwise present.
+ * Writes every entry of the compact grids; padding untouched.
+ */
+MXFP8_API int nvfp4_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
+                        const mxfp8_tensor* amax_tensor, mxfp8_tensor* scale_rowwise,
+                        mxfp8_tensor* scale_colwise, int64_t rows, int64_t cols, void* stream);
+
+/*
+ * input          [in]  fragment as for mxfp8_partial_cast.
+ * scale_rowwise  [in]  REQUIRED U8 [>= rows][>= ceil(cols/16)].
+ * scale_colwise  [in]  U8 [>= ceil(rows/16)][>= cols]; required iff output_colwise.
+ * amax_tensor    [in]  REQUIRED F32: element 0 is G (the same G the scales came from).
+ * output_rowwise [out] REQUIRED U8 packed codes, numel >= (out_offset + len) / 2.
+ * output_colwise [out] OPTIONAL U8 packed codes (empty => row-only), same size rule.
+ * Element k of the fragment goes to nibble position out_offset + k (out_offset =
+ * start_offset: full-size output of ceil(rows*cols/2) bytes, in place; 0: fragment-
+ * size output).  Two codes share a byte, so cols, start_offset, the fragment length and
+ * out_offset must be even (status 1 otherwise); then every byte a fragment writes
+ * belongs to it alone.  Other errors as mxfp8_partial_cast.
+ */
+MXFP8_API int nvfp4_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_rowwise,
+                       const mxfp8_tensor* scale_colwise, const mxfp8_tensor* amax_tensor,
+                       mxfp8_tensor* output_rowwise, mxfp8_tensor* output_colwise, int64_t rows,
+                       int64_t cols, int64_t start_offset, int64_t out_offset, void* stream);
+
 /* Message describing the calling thread's most recent non-zero status ("" if none). */
 MXFP8_API const char* mxfp8_last_error(void);
 

@@ -23,8 +23,8 @@ EXPORTED = ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales"
             "mxfp8_quantize_whole_blocks_batched", "mxfp8_swizzle_scales",
             "mxfp8_swizzled_scales_size", "mxfp8_device_can_access",
             "mxfp8_amax_max_reduce_update_scales", "mxfp8_amax_max_reduce_update_scales_ranged",
-            "mxfp8_sharded_update_noalloc",
-            "mxfp8_last_error", "mxfp8_version")
+            "mxfp8_sharded_update_noalloc", "nvfp4_partial_amax", "nvfp4_update_scales",
+            "nvfp4_partial_cast", "mxfp8_last_error", "mxfp8_version")
 
 
 class Tensor(ctypes.Structure):
@@ -111,6 +111,11 @@ def load(path: str | None = None):
         lib.mxfp8_amax_max_reduce_update_scales_ranged.argtypes = [
             T, T, ctypes.POINTER(ScaleJob), i32, ctypes.POINTER(i64), i32, vp]
         lib.mxfp8_amax_max_reduce_update_scales_ranged.restype = ctypes.c_int
+        lib.nvfp4_partial_amax.argtypes = [T, T, T, T, i64, i64, i64, vp]
+        lib.nvfp4_update_scales.argtypes = [T, T, T, T, T, i64, i64, vp]
+        lib.nvfp4_partial_cast.argtypes = [T, T, T, T, T, T, i64, i64, i64, i64, vp]
+        for name in ("nvfp4_partial_amax", "nvfp4_update_scales", "nvfp4_partial_cast"):
+            getattr(lib, name).restype = ctypes.c_int
         lib.mxfp8_device_can_access.argtypes = [vp, i64]
         lib.mxfp8_device_can_access.restype = ctypes.c_int
         for name in ("mxfp8_partial_amax", "mxfp8_amax_max_reduce", "mxfp8_update_scales",

@@ -320,6 +320,73 @@ def mxfp8_sharded_update_noalloc(fragments, start_offsets, scale_inv_rowwise, sc
           int(rows), int(cols), _stream(stream, output_rowwise))
 
 
+# ---------------------------------------------------------------- NVFP4
+def nvfp4_block_shapes(rows: int, cols: int):
+    """((rows, ceil(cols/16)), (ceil(rows/16), cols)): the NVFP4 rowwise and columnwise
+    block grids of a rows x cols weight."""
+    return (rows, (cols + 15) // 16), ((rows + 15) // 16, cols)
+
+
+def nvfp4_partial_amax(input, amax_rowwise, amax_colwise, amax_tensor, rows: int, cols: int,
+                       start_offset: int, stream=None) -> None:
+    """1x16 / 16x1 block maxima (F32) of a fragment, and its largest |x| max-accumulated
+    into ``amax_tensor[0]`` (see the C header for the NVFP4 convention)."""
+    hs = [handle(input, "input"), handle(amax_rowwise, "amax_rowwise"),
+          handle(amax_colwise, "amax_colwise"), handle(amax_tensor, "amax_tensor")]
+    _call("nvfp4_partial_amax", _device_of(input, amax_rowwise), *[ctypes.byref(h) for h in hs],
+          int(rows), int(cols), int(start_offset), _stream(stream, amax_rowwise))
+
+
+def nvfp4_update_scales(amax_rowwise, amax_colwise, amax_tensor, scale_rowwise, scale_colwise,
+                        rows: int, cols: int, stream=None) -> None:
+    """E4M3 block scales of the present directions under the tensor amax."""
+    hs = [handle(amax_rowwise, "amax_rowwise"), handle(amax_colwise, "amax_colwise"),
+          handle(amax_tensor, "amax_tensor"), handle(scale_rowwise, "scale_rowwise"),
+          handle(scale_colwise, "scale_colwise")]
+    _call("nvfp4_update_scales", _device_of(amax_rowwise, scale_rowwise),
+          *[ctypes.byref(h) for h in hs], int(rows), int(cols), _stream(stream, scale_rowwise))
+
+
+def nvfp4_partial_cast(input, scale_rowwise, scale_colwise, amax_tensor, output_rowwise,
+                       output_colwise, rows: int, cols: int, start_offset: int,
+                       out_offset: int | None = None, stream=None) -> None:
+    """Packed E2M1 codes of a fragment into the rowwise and (optional) columnwise outputs,
+    element k at nibble out_offset + k (default: start_offset, full-size outputs)."""
+    if out_offset is None:
+        out_offset = start_offset
+    hs = [handle(input, "input"), handle(scale_rowwise, "scale_rowwise"),
+          handle(scale_colwise, "scale_colwise"), handle(amax_tensor, "amax_tensor"),
+          handle(output_rowwise, "output_rowwise"), handle(output_colwise, "output_colwise")]
+    _call("nvfp4_partial_cast", _device_of(input, output_rowwise), *[ctypes.byref(h) for h in hs],
+          int(rows), int(cols), int(start_offset), int(out_offset), _stream(stream, output_rowwise))
+
+
+def prepare_nvfp4_partial_amax(input, amax_rowwise, amax_colwise, amax_tensor, rows, cols,
+                               start_offset):
+    ts = (input, amax_rowwise, amax_colwise, amax_tensor)
+    hs = [handle(t, n) for t, n in zip(ts, ("input", "amax_rowwise", "amax_colwise", "amax_tensor"))]
+    return Prepared("nvfp4_partial_amax", hs, (rows, cols, start_offset), [t for t in ts if t is not None])
+
+
+def prepare_nvfp4_update_scales(amax_rowwise, amax_colwise, amax_tensor, scale_rowwise,
+                                scale_colwise, rows, cols):
+    ts = (amax_rowwise, amax_colwise, amax_tensor, scale_rowwise, scale_colwise)
+    hs = [handle(t, n) for t, n in zip(ts, ("amax_rowwise", "amax_colwise", "amax_tensor",
+                                            "scale_rowwise", "scale_colwise"))]
+    return Prepared("nvfp4_update_scales", hs, (rows, cols), [t for t in ts if t is not None])
+
+
+def prepare_nvfp4_partial_cast(input, scale_rowwise, scale_colwise, amax_tensor, output_rowwise,
+                               output_colwise, rows, cols, start_offset, out_offset=None):
+    if out_offset is None:
+        out_offset = start_offset
+    ts = (input, scale_rowwise, scale_colwise, amax_tensor, output_rowwise, output_colwise)
+    hs = [handle(t, n) for t, n in zip(ts, ("input", "scale_rowwise", "scale_colwise", "amax_tensor",
+                                            "output_rowwise", "output_colwise"))]
+    return Prepared("nvfp4_partial_cast", hs, (rows, cols, start_offset, out_offset),
+                    [t for t in ts if t is not None])
+
+
 class Prepared:
     """One library call with its tensor handles marshalled once.
 

@@ -746,6 +746,171 @@ int mxfp8_quantize_whole_blocks_batched(const mxfp8_quantize_job* jobs, int32_t 
   return run_fused(jobs, njobs, stream);
 }
 
+// ---------------------------------------------------------------- NVFP4
+int nvfp4_partial_amax(const mxfp8_tensor* input, mxfp8_tensor* amax_rowwise,
+                       mxfp8_tensor* amax_colwise, mxfp8_tensor* amax_tensor, int64_t rows,
+                       int64_t cols, int64_t start_offset, void* stream) {
+  const bool in_empty = is_empty(input);
+  if (!in_empty) {
+    if (int rc = check_tensor(input, "input")) return rc;
+  }
+  const int64_t len = in_empty ? 0 : numel(input);
+  if (int rc = check_dims(rows, cols, start_offset, len)) return rc;
+  if (len == 0) return ok();
+  const int32_t dt = input->dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
+  if (is_empty(amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
+  if (is_empty(amax_tensor)) return fail(MXFP8_ERR_MISSING, "amax_tensor is required");
+  const int64_t nbr = (cols + 15) / 16, nbc = (rows + 15) / 16;
+  if (int rc = check_grid(amax_rowwise, "amax_rowwise", rows, nbr, MXFP8_DTYPE_F32)) return rc;
+  if (int rc = check_tensor(amax_tensor, "amax_tensor")) return rc;
+  if (amax_tensor->dtype != MXFP8_DTYPE_F32) return fail(MXFP8_ERR_DTYPE, "amax_tensor: dtype must be F32");
+  const bool colwise = !is_empty(amax_colwise);
+  if (colwise) {
+    if (int rc = check_grid(amax_colwise, "amax_colwise", nbc, cols, MXFP8_DTYPE_F32)) return rc;
+  }
+  const int64_t eb = elem_bytes(dt);
+  const int V = int(16 / eb);
+  mxfp8::Nvfp4AmaxParams p{};
+  p.g = make_geom(rows, cols, start_offset, len, mxfp8::tile_width_for(dt));
+  p.g.fast_ok = cols % V == 0;
+  p.g.shift = int32_t(virtual_base(input->data, start_offset, eb) % 16);
+  p.in = input->data;
+  p.amax_r = static_cast<float*>(amax_rowwise->data);
+  p.ld_r = amax_rowwise->shape[1];
+  p.amax_t = static_cast<uint32_t*>(amax_tensor->data);
+  if (colwise) {
+    p.amax_c = static_cast<float*>(amax_colwise->data);
+    p.ld_c = amax_colwise->shape[1];
+    p.vec_c = (reinterpret_cast<uintptr_t>(p.amax_c) % 16 == 0) && (p.ld_c % 4 == 0);
+  }
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  return cuda_status(mxfp8::launch_nvfp4_amax(p, dt == MXFP8_DTYPE_F32 ? 0 : 1, p.g.shift != 0, dev,
+                                              static_cast<cudaStream_t>(stream)),
+                     "nvfp4 partial amax launch");
+}
+
+int nvfp4_update_scales(const mxfp8_tensor* amax_rowwise, const mxfp8_tensor* amax_colwise,
+                        const mxfp8_tensor* amax_tensor, mxfp8_tensor* scale_rowwise,
+                        mxfp8_tensor* scale_colwise, int64_t rows, int64_t cols, void* stream) {
+  if (int rc = check_size(rows, cols)) return rc;
+  if (is_empty(amax_rowwise)) return fail(MXFP8_ERR_MISSING, "amax_rowwise is required");
+  if (is_empty(amax_tensor)) return fail(MXFP8_ERR_MISSING, "amax_tensor is required");
+  if (is_empty(scale_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_rowwise is required");
+  const int64_t nbr = (cols + 15) / 16, nbc = (rows + 15) / 16;
+  if (int rc = check_grid(amax_rowwise, "amax_rowwise", rows, nbr, MXFP8_DTYPE_F32)) return rc;
+  if (int rc = check_tensor(amax_tensor, "amax_tensor")) return rc;
+  if (amax_tensor->dtype != MXFP8_DTYPE_F32) return fail(MXFP8_ERR_DTYPE, "amax_tensor: dtype must be F32");
+  if (int rc = check_grid(scale_rowwise, "scale_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
+  const bool colwise = !is_empty(amax_colwise);
+  if (colwise) {
+    if (int rc = check_grid(amax_colwise, "amax_colwise", nbc, cols, MXFP8_DTYPE_F32)) return rc;
+    if (is_empty(scale_colwise))
+      return fail(MXFP8_ERR_MISSING, "scale_colwise is required when amax_colwise is present");
+    if (int rc = check_grid(scale_colwise, "scale_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
+  }
+  mxfp8::Nvfp4ScaleParams p{};
+  p.amax_t = static_cast<const float*>(amax_tensor->data);
+  auto seg = [](const mxfp8_tensor* a, mxfp8_tensor* sc, int64_t nr, int64_t nc) {
+    mxfp8::Nvfp4ScaleSegment g{};
+    g.amax = static_cast<const float*>(a->data);
+    g.scale = static_cast<uint8_t*>(sc->data);
+    g.nrows = nr;
+    g.ncols = nc;
+    g.ld_a = a->shape[1];
+    g.ld_s = sc->shape[1];
+    g.vec = g.ld_a == nc && g.ld_s == nc && (nr * nc) % 4 == 0 &&
+            reinterpret_cast<uintptr_t>(g.amax) % 16 == 0 && reinterpret_cast<uintptr_t>(g.scale) % 4 == 0;
+    return g;
+  };
+  p.seg[p.nseg++] = seg(amax_rowwise, scale_rowwise, rows, nbr);
+  if (colwise) p.seg[p.nseg++] = seg(amax_colwise, scale_colwise, nbc, cols);
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  return cuda_status(mxfp8::launch_nvfp4_scales(p, dev, static_cast<cudaStream_t>(stream)),
+                     "nvfp4 scale update launch");
+}
+
+int nvfp4_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* scale_rowwise,
+                       const mxfp8_tensor* scale_colwise, const mxfp8_tensor* amax_tensor,
+                       mxfp8_tensor* output_rowwise, mxfp8_tensor* output_colwise, int64_t rows,
+                       int64_t cols, int64_t start_offset, int64_t out_offset, void* stream) {
+  const bool in_empty = is_empty(input);
+  if (!in_empty) {
+    if (int rc = check_tensor(input, "input")) return rc;
+  }
+  const int64_t len = in_empty ? 0 : numel(input);
+  if (int rc = check_dims(rows, cols, start_offset, len)) return rc;
+  if (out_offset < 0) return fail(MXFP8_ERR_INVALID, "out_offset must be non-negative");
+  if (cols % 2 != 0 || start_offset % 2 != 0 || len % 2 != 0 || out_offset % 2 != 0)
+    return fail(MXFP8_ERR_INVALID,
+                "NVFP4 packs two codes per byte: cols, start_offset, the fragment length and "
+                "out_offset must be even");
+  if (len == 0) return ok();
+  const int32_t dt = input->dtype;
+  if (dt != MXFP8_DTYPE_F32 && dt != MXFP8_DTYPE_BF16)
+    return fail(MXFP8_ERR_DTYPE, "input: dtype must be F32 or BF16");
+  if (is_empty(scale_rowwise)) return fail(MXFP8_ERR_MISSING, "scale_rowwise is required");
+  if (is_empty(amax_tensor)) return fail(MXFP8_ERR_MISSING, "amax_tensor is required");
+  if (is_empty(output_rowwise)) return fail(MXFP8_ERR_MISSING, "output_rowwise is required");
+  const int64_t nbr = (cols + 15) / 16, nbc = (rows + 15) / 16;
+  if (int rc = check_grid(scale_rowwise, "scale_rowwise", rows, nbr, MXFP8_DTYPE_U8)) return rc;
+  if (int rc = check_tensor(amax_tensor, "amax_tensor")) return rc;
+  if (amax_tensor->dtype != MXFP8_DTYPE_F32) return fail(MXFP8_ERR_DTYPE, "amax_tensor: dtype must be F32");
+  const int64_t need = (out_offset + len) / 2;
+  auto check_out = [&](const mxfp8_tensor* o, const char* name) {
+    if (int rc = check_tensor(o, name)) return rc;
+    if (o->dtype != MXFP8_DTYPE_U8) return fail(MXFP8_ERR_DTYPE, "%s: dtype must be U8", name);
+    if (numel(o) < need)
+      return fail(MXFP8_ERR_SHAPE, "%s holds %lld bytes, needs (out_offset + len) / 2 = %lld", name,
+                  (long long)numel(o), (long long)need);
+    return int(MXFP8_OK);
+  };
+  if (int rc = check_out(output_rowwise, "output_rowwise")) return rc;
+  const bool colwise = !is_empty(output_colwise);
+  if (colwise) {
+    if (int rc = check_out(output_colwise, "output_colwise")) return rc;
+    if (is_empty(scale_colwise))
+      return fail(MXFP8_ERR_MISSING, "scale_colwise is required when output_colwise is present");
+    if (int rc = check_grid(scale_colwise, "scale_colwise", nbc, cols, MXFP8_DTYPE_U8)) return rc;
+  }
+  const int64_t eb = elem_bytes(dt);
+  const int V = int(16 / eb);
+  mxfp8::Nvfp4CastParams p{};
+  p.g = make_geom(rows, cols, start_offset, len, mxfp8::tile_width_for(dt));
+  p.g.fast_ok = cols % V == 0;
+  p.g.shift = int32_t(virtual_base(input->data, start_offset, eb) % 16);
+  p.in = input->data;
+  p.s_r = static_cast<const uint8_t*>(scale_rowwise->data);
+  p.ld_sr = scale_rowwise->shape[1];
+  p.amax_t = static_cast<const float*>(amax_tensor->data);
+  p.out_r = static_cast<uint8_t*>(output_rowwise->data);
+  p.out_shift = out_offset - start_offset;
+  // a lane's V codes (V/2 bytes) start at nibble address 2 * out + row * cols + j +
+  // out_shift, with cols and j multiples of V when whole tiles take the vector path: one
+  // V/2-byte word store when 2 * out + out_shift is a multiple of V
+  auto word_ok = [&](const void* o) {
+    const int64_t m = V;
+    const int64_t nib = (2 * int64_t(reinterpret_cast<uintptr_t>(o) % uintptr_t(m)) + p.out_shift % m) % m;
+    return (nib + m) % m == 0;
+  };
+  bool vec = p.g.fast_ok && word_ok(p.out_r);
+  if (colwise) {
+    p.s_c = static_cast<const uint8_t*>(scale_colwise->data);
+    p.ld_sc = scale_colwise->shape[1];
+    p.out_c = static_cast<uint8_t*>(output_colwise->data);
+    vec = vec && word_ok(p.out_c);
+  }
+  p.vec_out = vec;
+  DeviceInfo dev;
+  if (int rc = device_info(&dev)) return rc;
+  return cuda_status(mxfp8::launch_nvfp4_cast(p, dt == MXFP8_DTYPE_F32 ? 0 : 1, p.g.shift != 0, dev,
+                                              static_cast<cudaStream_t>(stream)),
+                     "nvfp4 partial cast launch");
+}
+
 int mxfp8_device_can_access(const void* ptr, int64_t bytes) {
   if (ptr == nullptr || bytes < 0) return 0;
   int dev = 0;

@@ -107,6 +107,49 @@ struct ReduceScaleSegment {
   int64_t e0, e1;
 };
 
+// NVFP4 (E2M1 data, 16-value blocks with E4M3 scales, one FP32 tensor scale).
+// Partial amax of one fragment: FP32 1x16 row-block and 16x1 column-block maxima, and
+// the fragment's largest |x| max-accumulated into the tensor amax (FP32 bits).
+struct Nvfp4AmaxParams {
+  FragGeom g;
+  const void* in;
+  float* amax_r;       // [rows][ld_r], ld_r >= ceil(cols/16)
+  int64_t ld_r;
+  float* amax_c;       // [ceil(rows/16)][ld_c] (colwise kernel only)
+  int64_t ld_c;
+  uint32_t* amax_t;    // one FP32, max-accumulated
+  int32_t vec_c;       // colwise amax rows may take 16-byte stores
+};
+
+// E4M3 block scales of up to two grids under one tensor amax.
+struct Nvfp4ScaleSegment {
+  const float* amax;
+  uint8_t* scale;
+  int64_t nrows, ncols, ld_a, ld_s;
+  int32_t vec;         // dense (ld == ncols), 4 | nrows*ncols, aligned: 4 entries per thread
+};
+struct Nvfp4ScaleParams {
+  const float* amax_t;
+  int32_t nseg;
+  Nvfp4ScaleSegment seg[2];
+};
+
+// Partial cast of one fragment to packed E2M1 (element f in nibble f + out_shift; the
+// low nibble of a byte holds the even position).
+struct Nvfp4CastParams {
+  FragGeom g;
+  const void* in;
+  const uint8_t* s_r;  // [rows][ld_sr] E4M3
+  int64_t ld_sr;
+  const uint8_t* s_c;  // [ceil(rows/16)][ld_sc] E4M3 (colwise kernel only)
+  int64_t ld_sc;
+  const float* amax_t;
+  uint8_t* out_r;
+  uint8_t* out_c;
+  int64_t out_shift;   // out_offset - start (even)
+  int32_t vec_out;     // a lane's V/2 output bytes may leave as one 2- (FP32) or 4-byte store
+};
+
 struct DeviceInfo {
   int device;
   int sms;
@@ -199,6 +242,13 @@ cudaError_t launch_swizzle_scales(const SwizzleParams& p, const DeviceInfo& dev,
                                   cudaStream_t stream);
 cudaError_t launch_max_reduce(const void* slots, void* out, int64_t slot_elems, int num_slots,
                               int dtype, const DeviceInfo& dev, cudaStream_t stream);
+
+cudaError_t launch_nvfp4_amax(const Nvfp4AmaxParams& p, int dtype, bool shifted,
+                              const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_nvfp4_scales(const Nvfp4ScaleParams& p, const DeviceInfo& dev,
+                                cudaStream_t stream);
+cudaError_t launch_nvfp4_cast(const Nvfp4CastParams& p, int dtype, bool shifted,
+                              const DeviceInfo& dev, cudaStream_t stream);
 
 // Record `msg` as the calling thread's last error (returned by mxfp8_last_error) and
 // return `code`.  For entry points defined outside capi.cu.

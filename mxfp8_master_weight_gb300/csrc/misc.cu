@@ -73,54 +73,31 @@ struct ReduceScaleBatch {
   ReduceScaleSegment seg[kMaxReduceSegments];
 };
 
-// Maximum of |.| over the contributing slots of entry idx (4 consecutive entries when
-// kQuad) of a segment, as raw bit patterns; NaN canonicalised.
-template <class T, bool kQuad>
-__device__ __forceinline__ void reduce_entries(const ReduceScaleSegment& s, int64_t idx, uint32_t (&m)[4]) {
-  constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
-  m[0] = m[1] = m[2] = m[3] = 0u;
-  const char* base = static_cast<const char*>(s.slot0) + idx * T::kBytes;
-  const int64_t slot_bytes = s.slot_stride * T::kBytes;
-  uint64_t mask = s.slots;
-  for (int k = 0;; ++k) {
-    int slot;
-    if (s.all_slots) {
-      if (k >= s.nslots) break;
-      slot = k;
-    } else {
-      if (mask == 0) break;
-      slot = __ffsll(static_cast<long long>(mask)) - 1;
-      mask &= mask - 1;
-    }
-    const char* p = base + slot * slot_bytes;
-    if constexpr (kQuad) {
-      if constexpr (T::kBytes == 4) {
-        const uint4 a = ld_stream16(p);
-        m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], a.y & kAbs);
-        m[2] = max(m[2], a.z & kAbs); m[3] = max(m[3], a.w & kAbs);
-      } else {
-        const uint2 a = *reinterpret_cast<const uint2*>(p);
-        m[0] = max(m[0], a.x & kAbs); m[1] = max(m[1], (a.x >> 16) & kAbs);
-        m[2] = max(m[2], a.y & kAbs); m[3] = max(m[3], (a.y >> 16) & kAbs);
-      }
-    } else {
-      m[0] = max(m[0], load_bits<T>(p, 0) & kAbs);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < 4; ++k) m[k] = canonical_nan<T>(m[k]);
-}
+// Work items per thread and iteration: their slot loads are issued together (the slot
+// loop is outermost), so a thread keeps several 16-byte loads in flight.
+constexpr int kItems = 4;
 
-// One work item: its segment, the linear entry it starts at, and the reduced values.
+// One work item: its segment, the linear entry it starts at, the slots still to read,
+// and the maxima so far.
 struct ReduceItem {
   int seg;
+  int next;          // all_slots: next slot index
   int64_t e;
+  uint64_t mask;     // !all_slots: slots still to read
   bool live;
   uint32_t m[4];
 };
 
 template <class T>
-__device__ __forceinline__ void load_item(const ReduceScaleBatch& b, int64_t t, ReduceItem& it) {
+__device__ __forceinline__ void find_item(const ReduceScaleBatch& b, int64_t t, int64_t total,
+                                          ReduceItem& it) {
+  it.live = t < total;
+  it.m[0] = it.m[1] = it.m[2] = it.m[3] = 0u;
+  it.next = 0;
+  it.mask = 0;
+  it.seg = 0;
+  it.e = 0;
+  if (!it.live) return;
   int lo = 0, hi = b.nseg;  // prefix[lo] <= t < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -129,21 +106,27 @@ __device__ __forceinline__ void load_item(const ReduceScaleBatch& b, int64_t t, 
   const ReduceScaleSegment& s = b.seg[lo];
   const int64_t k = t - b.prefix[lo];
   it.seg = lo;
-  if (s.vec) {
-    it.e = s.e0 + 4 * k;
-    it.live = true;
-    reduce_entries<T, true>(s, it.e, it.m);
-  } else {
-    it.e = s.e0 + k;
-    it.live = (it.e % s.ld_a) < s.ncols;  // padding columns of a padded grid: nothing to do
-    if (it.live) reduce_entries<T, false>(s, it.e, it.m);
-  }
+  it.e = s.vec ? s.e0 + 4 * k : s.e0 + k;
+  if (!s.vec && it.e % s.ld_a >= s.ncols) it.live = false;  // a padding column: nothing to do
+  it.mask = s.all_slots ? 0 : s.slots;
+}
+
+// The item's next contributing slot, or -1 when none is left.
+__device__ __forceinline__ int next_slot(const ReduceScaleSegment& s, ReduceItem& it) {
+  if (!it.live) return -1;
+  if (s.all_slots) return it.next < s.nslots ? it.next++ : -1;
+  if (it.mask == 0) return -1;
+  const int slot = __ffsll(static_cast<long long>(it.mask)) - 1;
+  it.mask &= it.mask - 1;
+  return slot;
 }
 
 template <class T>
-__device__ __forceinline__ void store_item(const ReduceScaleBatch& b, const ReduceItem& it) {
+__device__ __forceinline__ void store_item(const ReduceScaleBatch& b, ReduceItem& it) {
   if (!it.live) return;
   const ReduceScaleSegment& s = b.seg[it.seg];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) it.m[k] = canonical_nan<T>(it.m[k]);
   if (s.vec) {
     if constexpr (T::kBytes == 4) {
       *reinterpret_cast<uint4*>(static_cast<uint32_t*>(s.reduced) + it.e) =
@@ -167,15 +150,47 @@ template <class T>
 __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
     const __grid_constant__ ReduceScaleBatch b) {
   grid_dependency_sync();
+  constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
   const int64_t total = b.prefix[b.nseg];
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t t = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t < total; t += 2 * stride) {
-    ReduceItem a, c;
-    load_item<T>(b, t, a);
-    const bool two = t + stride < total;
-    if (two) load_item<T>(b, t + stride, c);
-    store_item<T>(b, a);
-    if (two) store_item<T>(b, c);
+  for (int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t0 < total; t0 += kItems * stride) {
+    ReduceItem it[kItems];
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) find_item<T>(b, t0 + u * stride, total, it[u]);
+    for (bool more = true; more;) {
+      more = false;
+      uint4 v[kItems];
+      bool got[kItems];
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {  // one slot of every item: loads issued together
+        const ReduceScaleSegment& s = b.seg[it[u].seg];
+        const int slot = next_slot(s, it[u]);
+        got[u] = slot >= 0;
+        v[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (got[u]) {
+          const char* p = static_cast<const char*>(s.slot0) + (slot * s.slot_stride + it[u].e) * T::kBytes;
+          if (s.vec) {
+            if constexpr (T::kBytes == 4) {
+              v[u] = ld_stream16(p);
+            } else {
+              const uint2 w = *reinterpret_cast<const uint2*>(p);
+              v[u] = make_uint4(w.x & 0xffffu, w.x >> 16, w.y & 0xffffu, w.y >> 16);
+            }
+          } else {
+            v[u].x = load_bits<T>(p, 0);
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kItems; ++u) {
+        if (!got[u]) continue;
+        more = true;
+        it[u].m[0] = max(it[u].m[0], v[u].x & kAbs); it[u].m[1] = max(it[u].m[1], v[u].y & kAbs);
+        it[u].m[2] = max(it[u].m[2], v[u].z & kAbs); it[u].m[3] = max(it[u].m[3], v[u].w & kAbs);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kItems; ++u) store_item<T>(b, it[u]);
   }
 }
 
@@ -287,7 +302,7 @@ cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg
     }
     const int64_t total = b.prefix[b.nseg];
     if (total == 0) continue;
-    const unsigned grid = grid_for((total + 1) / 2, dev);
+    const unsigned grid = grid_for((total + kItems - 1) / kItems, dev);
     const cudaError_t e = dtype == 0
                               ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
                               : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);

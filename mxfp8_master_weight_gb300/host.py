@@ -207,7 +207,10 @@ class HostPartialFlow:
         """Quantise ``host_x`` (pinned, rows*cols elements) into the pinned host outputs.
 
         Asynchronous with respect to the host, like HostQuantizer.run: the caller's
-        current stream waits for the last copy out."""
+        current stream waits for the last copy out.  ``host_x`` must hold its values
+        when run() is called (the copy-in is not ordered after GPU work queued on the
+        caller's stream); the host outputs may not be read before that stream reaches
+        this call's end."""
         rows, cols = self.rows, self.cols
         for t, name in ((host_x, "host_x"), (host_qr, "host_qr"), (host_qc, "host_qc"),
                         (host_sr, "host_sr"), (host_sc, "host_sc")):
@@ -224,8 +227,12 @@ class HostPartialFlow:
         b = self._calls % 2
         self._calls += 1
         caller = torch.cuda.current_stream(self.device)
-        for s in (self.h2d, self.comp, self.d2h):
-            s.wait_stream(caller)
+        # The copy-in reads host memory only: it does not wait for the caller's stream
+        # (which, after a previous call, waits for that call's copies out), so one call's
+        # copy-in overlaps the previous call's copy-out.  Kernels and copies out follow
+        # the caller's stream.
+        self.comp.wait_stream(caller)
+        self.d2h.wait_stream(caller)
         dx = self.dev_x[b]
         raw_comp = api._stream(self.comp, None)
         # copy in, chunk by chunk (the buffer is free once the casts of two calls ago ran)
@@ -242,21 +249,25 @@ class HostPartialFlow:
             # the previous call's scales must have left before they are rewritten
             self.comp.wait_event(self.scales_out)
             self._reduce.call(raw_comp)
-            for k, (r0, r1) in enumerate(self.chunks):
-                s = k % self.depth
+        # cast chunk k, then copy it out; the two streams are fed chunk by chunk so that
+        # every event wait refers to the chunk before in this order
+        for k, (r0, r1) in enumerate(self.chunks):
+            s = k % self.depth
+            with torch.cuda.stream(self.comp):
                 self.comp.wait_event(self.d2h_done[s])  # staging buffer s has been copied out
                 self._cast[b][k].call(raw_comp)
                 self.comp_done[s].record(self.comp)
-            self.x_free[b].record(self.comp)
-        with torch.cuda.stream(self.d2h):
-            for k, (r0, r1) in enumerate(self.chunks):
-                s = k % self.depth
+            with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(self.comp_done[s])
                 n = (r1 - r0) * cols
                 qr[r0 * cols:r1 * cols].copy_(self.dev_qr[s][:n], non_blocking=True)
                 if qc is not None:
                     qc[r0 * cols:r1 * cols].copy_(self.dev_qc[s][:n], non_blocking=True)
                 self.d2h_done[s].record(self.d2h)
+        with torch.cuda.stream(self.comp):
+            self.x_free[b].record(self.comp)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_stream(self.comp)
             host_sr.copy_(self.scale_r, non_blocking=True)
             if host_sc is not None:
                 host_sc.copy_(self.scale_c, non_blocking=True)

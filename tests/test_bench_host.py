@@ -96,3 +96,11 @@ def test_cpu_all_cores_run_matches_single_core_bytes():
     _, b1 = bench.cpu_sample_run(data, 0, rows)
     assert used == 2 and b == b1 and wall > 0
     assert isinstance(bench.cpu_model(), str)
+
+
+def test_nvfp4_algorithmic_bytes_per_element():
+    n = 16384 * 6144
+    b = bench.nvfp4_algorithmic_bytes(n)
+    assert b["amax"] / n == pytest.approx(4.5)        # read 4 B, write 2 x 4 B / 16
+    assert b["scales"] / n == pytest.approx(0.625)    # read 2 x 4 B / 16, write 2 B / 16
+    assert b["cast"] / n == pytest.approx(5.125)      # read 4 B + 2 B / 16, write 2 x 0.5 B

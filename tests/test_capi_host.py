@@ -26,7 +26,7 @@ def _declared_symbols():
         with open(h) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names.update(re.findall(r"^\s*(?:MXFP8_API\s+)?(?:const\s+)?\w+\s*\*?\s*(mxfp8_\w+)\s*\(",
+        names.update(re.findall(r"^\s*(?:MXFP8_API\s+)?(?:const\s+)?\w+\s*\*?\s*((?:mxfp8|nvfp4)_\w+)\s*\(",
                                 text, flags=re.M))
     return sorted(names)
 
@@ -316,3 +316,30 @@ def test_ranged_reduction_validation(lib):
     assert call([(0, 0, 10)], T(P, F32, 65, 100)) == 1  # ranges need at most 64 slots
     assert b"64" in lib.mxfp8_last_error()
     assert fn(ctypes.byref(slots), ctypes.byref(red), ctypes.byref(job), 1, None, 1, None) == 1
+
+
+def test_nvfp4_validation(lib):
+    F = F32
+    inp = T(P, F, 100)
+    ar, ac, at = T(P, F, 64, 4), T(P, F, 4, 64), T(P, F, 1)
+    sr, sc = T(P, U8, 64, 4), T(P, U8, 4, 64)
+    q = T(P, U8, 64 * 32)
+    amax = lambda *a: lib.nvfp4_partial_amax(*[ctypes.byref(t) for t in a[:4]], *a[4:], None)
+    cast = lambda *a: lib.nvfp4_partial_cast(*[ctypes.byref(t) for t in a[:6]], *a[6:], None)
+    up = lambda *a: lib.nvfp4_update_scales(*[ctypes.byref(t) for t in a[:5]], *a[5:], None)
+    assert amax(inp, ar, ac, E(), 64, 64, 0) == 4            # tensor amax required
+    assert amax(inp, ar, ac, T(P, BF16, 1), 64, 64, 0) == 3  # tensor amax must be F32
+    assert amax(inp, T(P, F, 64, 3), ac, at, 64, 64, 0) == 2  # 4 row blocks of 16 needed
+    assert amax(inp, T(P, BF16, 64, 4), ac, at, 64, 64, 0) == 3  # NVFP4 amax grids are F32
+    assert amax(E(), E(), E(), E(), 64, 64, 3) == 0           # empty fragment: nothing to do
+    assert cast(inp, sr, sc, at, q, q, 64, 64, 1, 1) == 1       # odd start
+    assert b"even" in lib.mxfp8_last_error()
+    assert cast(T(P, F, 99), sr, sc, at, q, q, 64, 64, 0, 0) == 1  # odd length
+    assert cast(inp, sr, sc, at, q, q, 64, 63, 0, 0) == 1      # odd cols
+    assert cast(inp, sr, sc, at, q, q, 64, 64, 0, 3) == 1      # odd out_offset
+    assert cast(inp, sr, E(), at, q, q, 64, 64, 0, 0) == 4     # colwise output needs scales
+    assert cast(inp, sr, sc, E(), q, q, 64, 64, 0, 0) == 4     # tensor amax required
+    assert cast(inp, sr, sc, at, T(P, U8, 49), E(), 64, 64, 0, 0) == 2  # 100 codes need 50 bytes
+    assert cast(inp, T(P, U8, 64, 3), sc, at, q, q, 64, 64, 0, 0) == 2
+    assert up(ar, ac, at, sr, E(), 64, 64) == 4
+    assert up(ar, ac, at, T(P, U8, 4, 63), sc, 64, 64) == 2
