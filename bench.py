@@ -585,7 +585,7 @@ def run_ours(args):
     b_phase_bytes = sharded_phase_bytes(bspecs, bsc.num_shards, bsc.layout.total,
                                         slot_entries_read=held)
     bsc_launches = bsc.launches_per_step()
-    bsc_ranged = bsc.ranged
+    bsc_ranged, bsc_slots, bsc_packed = bsc.ranged, bsc.num_shards, bsc.layout.total
     # per-phase split of the sharded step (events around the phases of sampled steps)
     phase_samples = sample_phases(lambda events=None: bsc.step(bshards, events=events), 64)
     b_phases = {}
@@ -708,7 +708,7 @@ def run_ours(args):
                         "bidirectional; 167.8M elements), 4 emulated shards in own buffers",
             "launches_per_step": bsc_launches, "steps": b_steps,
             "reduction": (f"ranged: reads the {held} slot entries the shards' amax wrote "
-                          f"(of {bsc.num_shards} x {bsc.layout.total}); slots never zeroed"
+                          f"(of {bsc_slots} x {bsc_packed}); slots never zeroed"
                           if bsc_ranged else "whole slots, zeroed before each step"),
             "us_per_step": round(b_us, 2), "phases": b_phases, "algorithmic_bytes": b_bytes,
             "gbs": round(b_bytes / (b_us * 1e-6) / 1e9, 1),

@@ -77,7 +77,38 @@ __device__ __forceinline__ void store_col_stats(const FusedParams& p, int64_t ro
   }
 }
 
-template <class T, bool kCol, int kS, bool kVec, int kModel>
+// Exponent-only maxima.  A block's E8M0 scale depends only on the exponent field of its
+// amax, and the maximum of |x| commutes with keeping the top 16 bits of the FP32 pattern
+// (a monotone map on non-negative patterns), so when no amax output is requested the
+// FP32 maxima are taken on packed high halves: two columns per register, two rows per
+// butterfly.
+__device__ __forceinline__ uint32_t e8m0_from_half(uint32_t h) {
+  const uint32_t e = (h >> 7) & 0xffu;
+  return e == 0xffu ? 0xffu : (e > 8u ? e - 8u : 0u);
+}
+
+// High halves of two FP32 words, sign cleared: (|b| >> 16) << 16 | |a| >> 16.
+__device__ __forceinline__ uint32_t abs_hi_halves(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x7632) & 0x7fff7fffu;
+}
+
+template <bool kCol>
+__device__ __forceinline__ void store_col_scales_half(const FusedParams& p, int64_t row0, int64_t j,
+                                                      uint32_t c01, uint32_t c23, float (&mc)[4]) {
+  const uint32_t sb[4] = {e8m0_from_half(c01 & 0xffffu), e8m0_from_half(c01 >> 16),
+                          e8m0_from_half(c23 & 0xffffu), e8m0_from_half(c23 >> 16)};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) mc[k] = scale_multiplier(sb[k]);
+  uint8_t* dst = p.s_c + (row0 >> 5) * p.ld_sc + j;
+  if (p.vec_sc) {
+    *reinterpret_cast<uint32_t*>(dst) = sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+  } else {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) dst[k] = static_cast<uint8_t>(sb[k]);
+  }
+}
+
+template <class T, bool kCol, int kS, bool kVec, int kModel, bool kExp>
 __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t row0, int64_t col0,
                                                 int lane, RowScales& rsc, int warp) {
   const int64_t cols = p.g.cols;
@@ -91,27 +122,61 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
   const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
 
   // pass 1: block maxima -> scales
-  uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
+  float mc[T::V];
+  if constexpr (kExp) {
+    static_assert(T::kBytes == 4, "exponent-only maxima are taken on FP32 high halves");
+    uint32_t c01 = 0u, c23 = 0u;  // column maxima, two columns per register
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += NB) {
-    uint4 v[NB];
-    load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, keep);
+    for (int rb = 0; rb < 32; rb += NB) {
+      uint4 v[NB];
+      load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, keep);
 #pragma unroll
-    for (int r = 0; r < NB; ++r) {
-      const uint4 a = chunk_abs<T>(v[r]);
-      if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
-      const uint32_t m = group_max<T>(chunk_reduce<T>(a));
-      if (writer) {
-        const int64_t i = row0 + rb + r;
-        const uint32_t e = e8m0_from_bits<T>(m);
-        rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
-        p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
-        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, canonical_nan<T>(m));
+      for (int r = 0; r < NB; r += 2) {
+        const uint32_t a01 = abs_hi_halves(v[r].x, v[r].y), a23 = abs_hi_halves(v[r].z, v[r].w);
+        const uint32_t b01 = abs_hi_halves(v[r + 1].x, v[r + 1].y);
+        const uint32_t b23 = abs_hi_halves(v[r + 1].z, v[r + 1].w);
+        if constexpr (kCol) {
+          c01 = __vmaxu2(c01, __vmaxu2(a01, b01));
+          c23 = __vmaxu2(c23, __vmaxu2(a23, b23));
+        }
+        // rows r and r+1 in the low and high halves of one word, one butterfly for both
+        const uint32_t ha = __vmaxu2(a01, a23), hb = __vmaxu2(b01, b23);
+        uint32_t w = __vmaxu2(__byte_perm(ha, hb, 0x5410), __byte_perm(ha, hb, 0x7632));
+#pragma unroll
+        for (int off = 1; off < T::G; off <<= 1) w = __vmaxu2(w, __shfl_xor_sync(kFullMask, w, off));
+        if (writer) {
+          const int64_t i = row0 + rb + r;
+          const uint32_t ea = e8m0_from_half(w & 0xffffu), eb = e8m0_from_half(w >> 16);
+          rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(ea);
+          rsc.b[warp][rb + r + 1][grp] = static_cast<uint8_t>(eb);
+          p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(ea);
+          p.s_r[(i + 1) * p.ld_sr + blk] = static_cast<uint8_t>(eb);
+        }
       }
     }
+    if constexpr (kCol) store_col_scales_half<kCol>(p, row0, j, c01, c23, mc);
+  } else {
+    uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+    for (int rb = 0; rb < 32; rb += NB) {
+      uint4 v[NB];
+      load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, keep);
+#pragma unroll
+      for (int r = 0; r < NB; ++r) {
+        const uint4 a = chunk_abs<T>(v[r]);
+        if constexpr (kCol) colmax = chunk_max<T>(colmax, a);
+        const uint32_t m = group_max<T>(chunk_reduce<T>(a));
+        if (writer) {
+          const int64_t i = row0 + rb + r;
+          const uint32_t e = e8m0_from_bits<T>(m);
+          rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
+          p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
+          if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, canonical_nan<T>(m));
+        }
+      }
+    }
+    if constexpr (kCol) store_col_stats<T, kCol>(p, row0, j, colmax, mc);
   }
-  float mc[T::V];
-  if constexpr (kCol) store_col_stats<T, kCol>(p, row0, j, colmax, mc);
   __syncwarp();
 
   // pass 2: cast (the tile's lines are still in L2)
@@ -137,15 +202,15 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
 }
 
 // A fast tile of a launch whose fragments are all aligned or all shifted.
-template <class T, bool kCol, bool kShift, bool kVec, int kModel>
+template <class T, bool kCol, bool kShift, bool kVec, int kModel, bool kExp>
 __device__ __forceinline__ void fused_fast(const FusedParams& p, int64_t row0, int64_t col0, int lane,
                                            RowScales& rsc, int warp) {
   if constexpr (kShift) {
     with_shift<T>(p.g.shift, [&](auto s) {
-      fused_tile_fast<T, kCol, decltype(s)::value, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+      fused_tile_fast<T, kCol, decltype(s)::value, kVec, kModel, kExp>(p, row0, col0, lane, rsc, warp);
     });
   } else {
-    fused_tile_fast<T, kCol, 0, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+    fused_tile_fast<T, kCol, 0, kVec, kModel, kExp>(p, row0, col0, lane, rsc, warp);
   }
 }
 
@@ -234,7 +299,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
   __syncwarp();
 }
 
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N, bool kExp>
 __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const __grid_constant__ JobBatch<FusedParams, N> b) {
   __shared__ RowScales rsc;
@@ -251,9 +316,9 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) fused_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+        if constexpr (kDirs != kRowOnly) fused_fast<T, true, kShift, kVec, kModel, kExp>(p, row0, col0, lane, rsc, warp);
       } else {
-        if constexpr (kDirs != kBidir) fused_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, rsc, warp);
+        if constexpr (kDirs != kBidir) fused_fast<T, false, kShift, kVec, kModel, kExp>(p, row0, col0, lane, rsc, warp);
       }
     } else if (kind == kTileMasked) {
       if (col) {
@@ -265,13 +330,13 @@ __global__ void __launch_bounds__(kThreads, kFusedMinBlocks) k_fused_quantize(
   }
 }
 
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N, bool kExp>
 cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   static std::atomic<int> occupancy[kMaxDevices];
   int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
   if (occ == 0) {
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        &occ, k_fused_quantize<T, kDirs, kShift, kVec, kModel, N>, kThreads, 0);
+        &occ, k_fused_quantize<T, kDirs, kShift, kVec, kModel, N, kExp>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
     if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
@@ -280,18 +345,19 @@ cudaError_t launch_n(const FusedParams* jobs, int n, const DeviceInfo& dev, cuda
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
   const unsigned grid = balanced_grid(total, kWarps, int64_t(dev.sms) * occ);
-  return launch_kernel(k_fused_quantize<T, kDirs, kShift, kVec, kModel, N>, grid, kThreads, 0, stream, b);
+  return launch_kernel(k_fused_quantize<T, kDirs, kShift, kVec, kModel, N, kExp>, grid, kThreads, 0,
+                       stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's
 // direction set; single BF16-model jobs use the one-entry job table.
-template <class T, bool kShift, bool kVec, int kModel>
+template <class T, bool kShift, bool kVec, int kModel, bool kExp>
 cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
   auto colwise = [](const FusedParams& p) { return p.out_c != nullptr; };
   if constexpr (kModel == kModelBF16) {
     if (n == 1) {
-      return colwise(jobs[0]) ? launch_n<T, kBidir, kShift, kVec, kModel, 1>(jobs, 1, dev, stream)
-                              : launch_n<T, kRowOnly, kShift, kVec, kModel, 1>(jobs, 1, dev, stream);
+      return colwise(jobs[0]) ? launch_n<T, kBidir, kShift, kVec, kModel, 1, kExp>(jobs, 1, dev, stream)
+                              : launch_n<T, kRowOnly, kShift, kVec, kModel, 1, kExp>(jobs, 1, dev, stream);
     }
   }
   for (int k = 0; k < n; k += kMaxBatchJobs) {
@@ -299,13 +365,13 @@ cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaSt
     cudaError_t e;
     switch (batch_dirs(jobs + k, m, colwise)) {
       case kRowOnly:
-        e = launch_n<T, kRowOnly, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kRowOnly, kShift, kVec, kModel, kMaxBatchJobs, kExp>(jobs + k, m, dev, stream);
         break;
       case kBidir:
-        e = launch_n<T, kBidir, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kBidir, kShift, kVec, kModel, kMaxBatchJobs, kExp>(jobs + k, m, dev, stream);
         break;
       default:
-        e = launch_n<T, kMixed, kShift, kVec, kModel, kMaxBatchJobs>(jobs + k, m, dev, stream);
+        e = launch_n<T, kMixed, kShift, kVec, kModel, kMaxBatchJobs, kExp>(jobs + k, m, dev, stream);
         break;
     }
     if (e != cudaSuccess) return e;
@@ -316,12 +382,22 @@ cudaError_t launch(const FusedParams* jobs, int n, const DeviceInfo& dev, cudaSt
 template <class T, int kModel>
 cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool vec_out,
                            const DeviceInfo& dev, cudaStream_t stream) {
-  if (shifted) {
-    return vec_out ? launch<T, true, true, kModel>(jobs, n, dev, stream)
-                   : launch<T, true, false, kModel>(jobs, n, dev, stream);
+  // FP32 input with word-aligned outputs and no amax output requested: exponent-only
+  // maxima (packed high halves)
+  if constexpr (T::kBytes == 4 && kModel == kModelBF16) {
+    bool exp_only = vec_out;
+    for (int k = 0; k < n && exp_only; ++k) exp_only = jobs[k].amax_r == nullptr && jobs[k].amax_c == nullptr;
+    if (exp_only) {
+      return shifted ? launch<T, true, true, kModel, true>(jobs, n, dev, stream)
+                     : launch<T, false, true, kModel, true>(jobs, n, dev, stream);
+    }
   }
-  return vec_out ? launch<T, false, true, kModel>(jobs, n, dev, stream)
-                 : launch<T, false, false, kModel>(jobs, n, dev, stream);
+  if (shifted) {
+    return vec_out ? launch<T, true, true, kModel, false>(jobs, n, dev, stream)
+                   : launch<T, true, false, kModel, false>(jobs, n, dev, stream);
+  }
+  return vec_out ? launch<T, false, true, kModel, false>(jobs, n, dev, stream)
+                 : launch<T, false, false, kModel, false>(jobs, n, dev, stream);
 }
 
 // All launches for one input dtype T (instantiated by that dtype's translation unit).

@@ -61,88 +61,40 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
   }
 }
 
-// Fused packed MAX reduction + scale update over runs of grid entries.  The work items
-// of every segment of a launch form one index space (prefix sums in the parameters), over
-// which the grid strides, so large and small grids share the SMs evenly; each thread
-// loads the contributing slots of two items before it stores either.
+// Fused packed MAX reduction + scale update over runs of grid entries.  Every run is cut
+// into chunks of kChunk work items (an item is 4 entries of a dense run, else one entry);
+// a block takes one chunk at a time, so the run -- its slots and pointers -- is the same
+// for all of its threads, and each thread loads its kItems items of every contributing
+// slot before it folds any of them, keeping several 16-byte loads in flight.  Chunks of
+// all runs form one index space (prefix sums in the parameters), so large and small
+// grids share the SMs evenly.
 constexpr int kMaxReduceSegments = 64;
+constexpr int kItems = 4;
+constexpr int kChunk = kThreads * kItems;
 
 struct ReduceScaleBatch {
   int32_t nseg;
-  int64_t prefix[kMaxReduceSegments + 1];  // items before segment k
+  int64_t chunk_prefix[kMaxReduceSegments + 1];  // chunks before run k
   ReduceScaleSegment seg[kMaxReduceSegments];
 };
 
-// Work items per thread and iteration: their slot loads are issued together (the slot
-// loop is outermost), so a thread keeps several 16-byte loads in flight.
-constexpr int kItems = 4;
-
-// One work item: its segment, the linear entry it starts at, the slots still to read,
-// and the maxima so far.
-struct ReduceItem {
-  int seg;
-  int next;          // all_slots: next slot index
-  int64_t e;
-  uint64_t mask;     // !all_slots: slots still to read
-  bool live;
-  uint32_t m[4];
-};
-
 template <class T>
-__device__ __forceinline__ void find_item(const ReduceScaleBatch& b, int64_t t, int64_t total,
-                                          ReduceItem& it) {
-  it.live = t < total;
-  it.m[0] = it.m[1] = it.m[2] = it.m[3] = 0u;
-  it.next = 0;
-  it.mask = 0;
-  it.seg = 0;
-  it.e = 0;
-  if (!it.live) return;
-  int lo = 0, hi = b.nseg;  // prefix[lo] <= t < prefix[hi]
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (b.prefix[mid] <= t) lo = mid; else hi = mid;
-  }
-  const ReduceScaleSegment& s = b.seg[lo];
-  const int64_t k = t - b.prefix[lo];
-  it.seg = lo;
-  it.e = s.vec ? s.e0 + 4 * k : s.e0 + k;
-  if (!s.vec && it.e % s.ld_a >= s.ncols) it.live = false;  // a padding column: nothing to do
-  it.mask = s.all_slots ? 0 : s.slots;
-}
-
-// The item's next contributing slot, or -1 when none is left.
-__device__ __forceinline__ int next_slot(const ReduceScaleSegment& s, ReduceItem& it) {
-  if (!it.live) return -1;
-  if (s.all_slots) return it.next < s.nslots ? it.next++ : -1;
-  if (it.mask == 0) return -1;
-  const int slot = __ffsll(static_cast<long long>(it.mask)) - 1;
-  it.mask &= it.mask - 1;
-  return slot;
-}
-
-template <class T>
-__device__ __forceinline__ void store_item(const ReduceScaleBatch& b, ReduceItem& it) {
-  if (!it.live) return;
-  const ReduceScaleSegment& s = b.seg[it.seg];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) it.m[k] = canonical_nan<T>(it.m[k]);
+__device__ __forceinline__ void store_reduced(const ReduceScaleSegment& s, int64_t e, const uint32_t (&m)[4]) {
   if (s.vec) {
     if constexpr (T::kBytes == 4) {
-      *reinterpret_cast<uint4*>(static_cast<uint32_t*>(s.reduced) + it.e) =
-          make_uint4(it.m[0], it.m[1], it.m[2], it.m[3]);
+      *reinterpret_cast<uint4*>(static_cast<uint32_t*>(s.reduced) + e) = make_uint4(m[0], m[1], m[2], m[3]);
     } else {
-      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(s.reduced) + it.e) =
-          make_uint2(it.m[0] | (it.m[1] << 16), it.m[2] | (it.m[3] << 16));
+      *reinterpret_cast<uint2*>(static_cast<uint16_t*>(s.reduced) + e) =
+          make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
     }
     uint32_t out = 0;
 #pragma unroll
-    for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(it.m[k]) << (8 * k);
-    *reinterpret_cast<uint32_t*>(s.scale + it.e) = out;  // dense: ld_s == ld_a == ncols
+    for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[k]) << (8 * k);
+    *reinterpret_cast<uint32_t*>(s.scale + e) = out;  // dense: ld_s == ld_a == ncols
   } else {
-    const int64_t r = it.e / s.ld_a, c = it.e % s.ld_a;
-    store_bits<T>(s.reduced, it.e, it.m[0]);
-    s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(it.m[0]));
+    const int64_t r = e / s.ld_a, c = e % s.ld_a;
+    store_bits<T>(s.reduced, e, m[0]);
+    s.scale[r * s.ld_s + c] = static_cast<uint8_t>(e8m0_from_bits<T>(m[0]));
   }
 }
 
@@ -151,46 +103,69 @@ __global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
     const __grid_constant__ ReduceScaleBatch b) {
   grid_dependency_sync();
   constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
-  const int64_t total = b.prefix[b.nseg];
-  const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-  for (int64_t t0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; t0 < total; t0 += kItems * stride) {
-    ReduceItem it[kItems];
+  const int64_t chunks = b.chunk_prefix[b.nseg];
+  for (int64_t c = blockIdx.x; c < chunks; c += gridDim.x) {
+    int lo = 0, hi = b.nseg;  // chunk_prefix[lo] <= c < chunk_prefix[hi]; uniform in the block
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (b.chunk_prefix[mid] <= c) lo = mid; else hi = mid;
+    }
+    const ReduceScaleSegment& s = b.seg[lo];
+    const int64_t items = s.vec ? (s.e1 - s.e0) / 4 : s.e1 - s.e0;
+    const int64_t first = (c - b.chunk_prefix[lo]) * kChunk + threadIdx.x;
+    const int step = s.vec ? 4 : 1;
+    int64_t e[kItems];
+    bool live[kItems];
+    uint32_t m[kItems][4];
 #pragma unroll
-    for (int u = 0; u < kItems; ++u) find_item<T>(b, t0 + u * stride, total, it[u]);
-    for (bool more = true; more;) {
-      more = false;
-      uint4 v[kItems];
-      bool got[kItems];
+    for (int u = 0; u < kItems; ++u) {
+      const int64_t t = first + u * kThreads;
+      e[u] = s.e0 + t * step;
+      live[u] = t < items && (s.vec || e[u] % s.ld_a < s.ncols);  // skip padding columns
+      m[u][0] = m[u][1] = m[u][2] = m[u][3] = 0u;
+    }
+    uint64_t mask = s.slots;
+    for (int k = 0;; ++k) {  // contributing slots, uniform in the block
+      int slot;
+      if (s.all_slots) {
+        if (k >= s.nslots) break;
+        slot = k;
+      } else {
+        if (mask == 0) break;
+        slot = __ffsll(static_cast<long long>(mask)) - 1;
+        mask &= mask - 1;
+      }
+      const char* base = static_cast<const char*>(s.slot0) + slot * s.slot_stride * T::kBytes;
+      uint32_t v[kItems][4];
 #pragma unroll
-      for (int u = 0; u < kItems; ++u) {  // one slot of every item: loads issued together
-        const ReduceScaleSegment& s = b.seg[it[u].seg];
-        const int slot = next_slot(s, it[u]);
-        got[u] = slot >= 0;
-        v[u] = make_uint4(0u, 0u, 0u, 0u);
-        if (got[u]) {
-          const char* p = static_cast<const char*>(s.slot0) + (slot * s.slot_stride + it[u].e) * T::kBytes;
-          if (s.vec) {
-            if constexpr (T::kBytes == 4) {
-              v[u] = ld_stream16(p);
-            } else {
-              const uint2 w = *reinterpret_cast<const uint2*>(p);
-              v[u] = make_uint4(w.x & 0xffffu, w.x >> 16, w.y & 0xffffu, w.y >> 16);
-            }
+      for (int u = 0; u < kItems; ++u) {
+        v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0u;
+        if (!live[u]) continue;
+        const char* p = base + e[u] * T::kBytes;
+        if (s.vec) {
+          if constexpr (T::kBytes == 4) {
+            const uint4 w = ld_stream16(p);
+            v[u][0] = w.x; v[u][1] = w.y; v[u][2] = w.z; v[u][3] = w.w;
           } else {
-            v[u].x = load_bits<T>(p, 0);
+            const uint2 w = *reinterpret_cast<const uint2*>(p);
+            v[u][0] = w.x & 0xffffu; v[u][1] = w.x >> 16; v[u][2] = w.y & 0xffffu; v[u][3] = w.y >> 16;
           }
+        } else {
+          v[u][0] = load_bits<T>(p, 0);
         }
       }
 #pragma unroll
-      for (int u = 0; u < kItems; ++u) {
-        if (!got[u]) continue;
-        more = true;
-        it[u].m[0] = max(it[u].m[0], v[u].x & kAbs); it[u].m[1] = max(it[u].m[1], v[u].y & kAbs);
-        it[u].m[2] = max(it[u].m[2], v[u].z & kAbs); it[u].m[3] = max(it[u].m[3], v[u].w & kAbs);
-      }
+      for (int u = 0; u < kItems; ++u)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m[u][q] = max(m[u][q], v[u][q] & kAbs);
     }
 #pragma unroll
-    for (int u = 0; u < kItems; ++u) store_item<T>(b, it[u]);
+    for (int u = 0; u < kItems; ++u) {
+      if (!live[u]) continue;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m[u][q] = canonical_nan<T>(m[u][q]);
+      store_reduced<T>(s, e[u], m[u]);
+    }
   }
 }
 
@@ -294,15 +269,17 @@ cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg
   for (int k0 = 0; k0 < nseg; k0 += kMaxReduceSegments) {
     ReduceScaleBatch b;
     b.nseg = nseg - k0 < kMaxReduceSegments ? nseg - k0 : kMaxReduceSegments;
-    b.prefix[0] = 0;
+    b.chunk_prefix[0] = 0;
     for (int k = 0; k < b.nseg; ++k) {
       b.seg[k] = segs[k0 + k];
       const int64_t n = b.seg[k].e1 - b.seg[k].e0;
-      b.prefix[k + 1] = b.prefix[k] + (b.seg[k].vec ? n / 4 : n);
+      const int64_t items = b.seg[k].vec ? n / 4 : n;
+      b.chunk_prefix[k + 1] = b.chunk_prefix[k] + (items + kChunk - 1) / kChunk;
     }
-    const int64_t total = b.prefix[b.nseg];
-    if (total == 0) continue;
-    const unsigned grid = grid_for((total + kItems - 1) / kItems, dev);
+    const int64_t chunks = b.chunk_prefix[b.nseg];
+    if (chunks == 0) continue;
+    const int64_t cap = int64_t(dev.sms) * 8;
+    const unsigned grid = unsigned(chunks < cap ? chunks : cap);
     const cudaError_t e = dtype == 0
                               ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
                               : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);

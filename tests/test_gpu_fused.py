@@ -200,3 +200,27 @@ def test_batched_cast_mixed_model_dtypes():
         want = np.zeros(rows * cols, np.uint8)
         oracle.partial_cast(x, rows, cols, 0, hs, None, want, None, 0, model=m)
         assert np.array_equal(to_host(q), want), m
+
+
+@pytest.mark.parametrize("colwise", [True, False])
+@pytest.mark.parametrize("shift", [0, 1, 2, 3])
+def test_fused_without_amax_outputs(colwise, shift):
+    """No amax output requested (FP32 input, word-aligned outputs): the one-pass kernel
+    takes block maxima on exponents only (packed high halves); scales and data stay
+    bit-identical to the oracle, on the headline-like value spread, whole weights,
+    band-aligned fragments and fragment buffers at every element offset, and blocks whose
+    maximum sits on an exponent boundary, a subnormal, zero, infinity or NaN."""
+    rows, cols = 192, 640
+    rng = np.random.default_rng(60 + shift)
+    n = rows * cols
+    x = (wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-6, 6, n).astype(np.float32))
+    specials = np.array([2.0, np.nextafter(np.float32(2.0), np.float32(0)), 1e-40, 0.0, -0.0,
+                         np.inf, -np.inf, np.nan, 448.0 * 2 ** 100, 2.0 ** -126], np.float32)
+    for k, v in enumerate(specials):  # one special per row block, in the first rows
+        x[k * cols + 7 * k] = v
+    x[5 * cols:6 * cols] = 0.0        # a whole zero row
+    for start, length in ((0, n), (32 * cols, 64 * cols), (cols * 96, n - cols * 96)):
+        frag = np.ascontiguousarray(x[start:start + length])
+        got = _fused(frag, rows, cols, start, colwise, shift=shift, with_amax=False)
+        want = _oracle_fragment(frag, rows, cols, start, colwise)
+        assert_bitwise(got[2:], want[2:], f"no amax out, shift {shift} [{start},+{length})")
