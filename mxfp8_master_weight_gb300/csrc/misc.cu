@@ -65,12 +65,13 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
 // into chunks of kChunk work items (an item is 4 entries of a dense run, else one entry);
 // a block takes one chunk at a time, so the run -- its slots and pointers -- is the same
 // for all of its threads, and each thread loads its kItems items of every contributing
-// slot before it folds any of them, keeping several 16-byte loads in flight.  Chunks of
+// slot before it folds any of them, keeping two 16-byte loads in flight at full occupancy.  Chunks of
 // all runs form one index space (prefix sums in the parameters), so large and small
 // grids share the SMs evenly.
 constexpr int kMaxReduceSegments = 64;
-constexpr int kItems = 4;
+constexpr int kItems = 2;
 constexpr int kChunk = kThreads * kItems;
+constexpr int kReduceBlocksPerSM = 8;  // 8 x 256 threads: every SM full, at most 32 registers
 
 struct ReduceScaleBatch {
   int32_t nseg;
@@ -99,7 +100,7 @@ __device__ __forceinline__ void store_reduced(const ReduceScaleSegment& s, int64
 }
 
 template <class T>
-__global__ void __launch_bounds__(kThreads) k_reduce_update_scales(
+__global__ void __launch_bounds__(kThreads, kReduceBlocksPerSM) k_reduce_update_scales(
     const __grid_constant__ ReduceScaleBatch b) {
   grid_dependency_sync();
   constexpr uint32_t kAbs = T::kBytes == 4 ? 0x7fffffffu : 0x7fffu;
@@ -278,8 +279,8 @@ cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg
     }
     const int64_t chunks = b.chunk_prefix[b.nseg];
     if (chunks == 0) continue;
-    const int64_t cap = int64_t(dev.sms) * 8;
-    const unsigned grid = unsigned(chunks < cap ? chunks : cap);
+    // every block takes the same number of chunks (within one): no mostly idle last round
+    const unsigned grid = balanced_grid(chunks, 1, int64_t(dev.sms) * kReduceBlocksPerSM);
     const cudaError_t e = dtype == 0
                               ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
                               : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);
