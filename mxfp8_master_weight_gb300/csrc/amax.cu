@@ -28,6 +28,12 @@ constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loa
 // streaming read, and 3 blocks (24 warps, at most 85 registers) keep more loads in flight
 // than the 2 an unconstrained allocation leaves room for.
 constexpr int kMinBlocks = 3;
+// The realigning (shifted) kernels: their per-row shuffles add latency that only more
+// resident warps hide.
+#ifndef MXFP8_AMAX_SHIFT_MIN_BLOCKS
+#define MXFP8_AMAX_SHIFT_MIN_BLOCKS 3
+#endif
+constexpr int kShiftMinBlocks = MXFP8_AMAX_SHIFT_MIN_BLOCKS;
 
 // Per-row work shared by both tile paths: fold |x| of one chunk into the column
 // maxima and return the maximum of the chunk's 32-element row block (all lanes of
@@ -129,7 +135,7 @@ __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t ro
 }
 
 template <class T, int kDirs, bool kShift, int N>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) k_partial_amax(
+__global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlocks) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();

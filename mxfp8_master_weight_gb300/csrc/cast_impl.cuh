@@ -33,8 +33,13 @@ constexpr int kMaskBatch = 4;    // rows per batch of predicated per-element loa
 // leaves room for 1-2): 3, where some variants then spill a few dozen bytes to L1 and
 // still run faster (FP32 config-5 cast phase -4 %, BF16 16384x6144 cast -4 %); 2 for the
 // BF16 kernels with unaligned outputs, whose piece stores spill more.
-template <class T, int N, bool kVec>
-constexpr int min_blocks() { return (T::kBytes == 2 && !kVec) ? 2 : 3; }
+#ifndef MXFP8_CAST_SHIFT_MIN_BLOCKS
+#define MXFP8_CAST_SHIFT_MIN_BLOCKS 3
+#endif
+template <class T, int N, bool kVec, bool kShift>
+constexpr int min_blocks() {
+  return (T::kBytes == 2 && !kVec) ? 2 : (kShift ? MXFP8_CAST_SHIFT_MIN_BLOCKS : 3);
+}
 
 // Columnwise multipliers 2^(127 - s) of this lane's V columns in column band row0/32.
 template <class T>
@@ -211,7 +216,7 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
 }
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
-__global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec>()) k_partial_cast(
+__global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec, kShift>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();

@@ -279,8 +279,9 @@ cudaError_t launch_reduce_update_scales(const ReduceScaleSegment* segs, int nseg
     }
     const int64_t chunks = b.chunk_prefix[b.nseg];
     if (chunks == 0) continue;
-    // every block takes the same number of chunks (within one): no mostly idle last round
-    const unsigned grid = balanced_grid(chunks, 1, int64_t(dev.sms) * kReduceBlocksPerSM);
+    // one chunk per block: the block scheduler keeps every SM full and hands out the
+    // small chunks dynamically (the loop covers anything past the grid limit)
+    const unsigned grid = unsigned(chunks < 2147483647 ? chunks : 2147483647);
     const cudaError_t e = dtype == 0
                               ? launch_kernel(k_reduce_update_scales<F32T>, grid, kThreads, 0, stream, b)
                               : launch_kernel(k_reduce_update_scales<BF16T>, grid, kThreads, 0, stream, b);
