@@ -684,13 +684,41 @@ int mxfp8_amax_max_reduce_update_scales_ranged(const mxfp8_tensor* slots, mxfp8_
       }
     }
   }
-  for (ReduceScaleSegment& r : runs) {
-    r.vec = r.ld_a == r.ncols && r.ld_s == r.ncols && r.e0 % 4 == 0 && r.e1 % 4 == 0 &&
-            (P % 4 == 0) && (reinterpret_cast<uintptr_t>(r.slot0) % uintptr_t(4 * eb) == 0) &&
-            (reinterpret_cast<uintptr_t>(r.reduced) % uintptr_t(4 * eb) == 0) &&
-            (reinterpret_cast<uintptr_t>(r.scale) % 4 == 0);
+  // A run of a dense, aligned grid takes 4 entries per work item from the first multiple
+  // of 4 to the last: its ragged ends (a shard boundary falls anywhere) become runs of
+  // single entries of their own.
+  std::vector<ReduceScaleSegment> pieces;
+  pieces.reserve(runs.size() * 3);
+  for (const ReduceScaleSegment& r : runs) {
+    const bool dense = r.ld_a == r.ncols && r.ld_s == r.ncols && (P % 4 == 0) &&
+                       (reinterpret_cast<uintptr_t>(r.slot0) % uintptr_t(4 * eb) == 0) &&
+                       (reinterpret_cast<uintptr_t>(r.reduced) % uintptr_t(4 * eb) == 0) &&
+                       (reinterpret_cast<uintptr_t>(r.scale) % 4 == 0);
+    const int64_t a = (r.e0 + 3) / 4 * 4, z = r.e1 / 4 * 4;
+    if (!dense || a >= z) {
+      pieces.push_back(r);
+      pieces.back().vec = 0;
+      continue;
+    }
+    ReduceScaleSegment q = r;
+    q.vec = 0;
+    if (r.e0 < a) {
+      q.e0 = r.e0;
+      q.e1 = a;
+      pieces.push_back(q);
+    }
+    q.vec = 1;
+    q.e0 = a;
+    q.e1 = z;
+    pieces.push_back(q);
+    if (z < r.e1) {
+      q.vec = 0;
+      q.e0 = z;
+      q.e1 = r.e1;
+      pieces.push_back(q);
+    }
   }
-  return cuda_status(mxfp8::launch_reduce_update_scales(runs.data(), int(runs.size()),
+  return cuda_status(mxfp8::launch_reduce_update_scales(pieces.data(), int(pieces.size()),
                                                         dt == MXFP8_DTYPE_F32 ? 0 : 1, dev,
                                                         static_cast<cudaStream_t>(stream)),
                      "reduce and update scales launch");

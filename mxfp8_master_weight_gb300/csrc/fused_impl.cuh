@@ -36,9 +36,11 @@ constexpr int kMaxGroups = 8;  // row blocks per warp tile (BF16: 256 columns / 
 #endif
 constexpr int kFusedMinBlocks = MXFP8_FUSED_MIN_BLOCKS;
 
-// E8M0 bytes of the 32 rows' row blocks of each warp's tile, handed from pass 1 to pass 2.
+// Multipliers 2^(127 - s) of the E8M0 scales of the 32 rows' row blocks of each warp's
+// tile, handed from pass 1 (where one lane per block derives them) to pass 2 (where every
+// lane of the block reads its row's multiplier).
 struct RowScales {
-  uint8_t b[kWarps][32][kMaxGroups];
+  float m[kWarps][32][kMaxGroups];
 };
 
 template <class T, bool kCol>
@@ -147,8 +149,8 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
         if (writer) {
           const int64_t i = row0 + rb + r;
           const uint32_t ea = e8m0_from_half(w & 0xffffu), eb = e8m0_from_half(w >> 16);
-          rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(ea);
-          rsc.b[warp][rb + r + 1][grp] = static_cast<uint8_t>(eb);
+          rsc.m[warp][rb + r][grp] = scale_multiplier(ea);
+          rsc.m[warp][rb + r + 1][grp] = scale_multiplier(eb);
           p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(ea);
           p.s_r[(i + 1) * p.ld_sr + blk] = static_cast<uint8_t>(eb);
         }
@@ -169,7 +171,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
         if (writer) {
           const int64_t i = row0 + rb + r;
           const uint32_t e = e8m0_from_bits<T>(m);
-          rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
+          rsc.m[warp][rb + r][grp] = scale_multiplier(e);
           p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
           if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, canonical_nan<T>(m));
         }
@@ -190,7 +192,7 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
       float y[T::V];
       model_values<T, kModel>(v[r], y);
       float mr[T::V];
-      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
+      const float m = rsc.m[warp][rb + r][grp];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const int64_t o = o0 + (rb + r) * cols;
@@ -238,7 +240,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       const uint32_t m = group_max<T>(chunk_reduce<T>(a));
       const int64_t i = row0 + rb + r;
       const uint32_t e = e8m0_from_bits<T>(m);
-      if (writer) rsc.b[warp][rb + r][grp] = static_cast<uint8_t>(e);
+      if (writer) rsc.m[warp][rb + r][grp] = scale_multiplier(e);
       if (writer && i < g.rows && b0 < g.cols &&
           row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1))) {
         p.s_r[i * p.ld_sr + (b0 >> 5)] = static_cast<uint8_t>(e);
@@ -274,7 +276,7 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
       float y[T::V];
       model_values<T, kModel>(v[r], y);
       float mr[T::V];
-      const float m = scale_multiplier(rsc.b[warp][rb + r][grp]);
+      const float m = rsc.m[warp][rb + r][grp];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
       const uint2 qr = quantize_chunk<T>(y, mr);

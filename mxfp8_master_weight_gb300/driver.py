@@ -177,7 +177,7 @@ class PackedLayout:
         return vr, vc
 
 
-def _count_launches(amax_jobs, cast_jobs, n_reduce_runs, specs, fused_reduce=False) -> int:
+def _count_launches(amax_jobs, cast_jobs, n_reduce_pieces, specs, fused_reduce=False) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
     entries launch once per group of at most 16 jobs sharing dtype and alignment class
     (fragment virtual base on a 16-byte boundary; for the cast also the outputs'
@@ -198,33 +198,46 @@ def _count_launches(amax_jobs, cast_jobs, n_reduce_runs, specs, fused_reduce=Fal
         vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
         ckeys.append((frag.dtype, vbase(frag, start) % 16 != 0, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
-    if fused_reduce:  # one launch per 64 runs of grid entries with one set of slots
-        reduce_and_scales = (n_reduce_runs + 63) // 64
+    if fused_reduce:  # one launch per 64 pieces of grid entries with one set of slots
+        reduce_and_scales = (n_reduce_pieces + 63) // 64
     else:             # the reduction, then one scale launch per 32 grids
         reduce_and_scales = 1 + (n_grids + 31) // 32
     return groups(akeys, 16) + reduce_and_scales + groups(ckeys, 16)
 
 
-def reduce_runs(layout: PackedLayout, ranges) -> int:
-    """Runs the fused reduction splits the block grids into: each grid is cut at every
-    slot range end inside it, and neighbouring pieces read by the same slots are joined
-    (without ranges, one run per grid)."""
-    runs = 0
+def reduce_runs(layout: PackedLayout, ranges):
+    """Runs the fused reduction splits the block grids into, as (grid offset, first, end)
+    in grid entries: each grid is cut at every slot range end inside it, and neighbouring
+    pieces read by the same slots are joined (without ranges, one run per grid)."""
+    runs = []
     grids = [g for w in range(len(layout.specs)) for g in (layout.rowwise[w], layout.colwise[w])
              if g is not None]
     for off, (nr, nc) in grids:
         span = nr * nc
         if not ranges:
-            runs += 1
+            runs.append((off, 0, span))
             continue
         cuts = sorted({0, span} | {e - off for _, a, b in ranges for e in (a, b) if 0 < e - off < span})
         prev = None
         for lo, hi in zip(cuts[:-1], cuts[1:]):
             mask = frozenset(s for s, a, b in ranges if a - off <= lo and b - off >= hi)
             if mask != prev:
-                runs += 1
+                runs.append((off, lo, hi))
+            else:
+                runs[-1] = (off, runs[-1][1], hi)
             prev = mask
     return runs
+
+
+def reduce_pieces(layout: PackedLayout, ranges) -> int:
+    """Work pieces the library makes of those runs (the driver's grids are dense and
+    aligned): 4 entries per item from the first multiple of 4 to the last, and the ragged
+    ends as pieces of single entries."""
+    n = 0
+    for _, lo, hi in reduce_runs(layout, ranges):
+        a, z = (lo + 3) // 4 * 4, hi // 4 * 4
+        n += 1 if a >= z else 1 + (lo < a) + (z < hi)
+    return n
 
 
 def _round_up(x: int, a: int) -> int:
@@ -317,7 +330,7 @@ class ShardedCast:
         # one batched call per phase: every fragment of every shard (each shard writes
         # its own slot, so no two jobs write the same amax entry), one reduction, every
         # weight's scales, every fragment's cast
-        self._launches = _count_launches(amax_jobs, cast_jobs, reduce_runs(self.layout, self.ranges),
+        self._launches = _count_launches(amax_jobs, cast_jobs, reduce_pieces(self.layout, self.ranges),
                                          self.specs, self.fuse_reduce_scales)
         amax = [api.prepare_partial_amax_batched(amax_jobs)]
         if self.ranged:

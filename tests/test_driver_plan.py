@@ -142,12 +142,22 @@ def test_slot_ranges_cover_each_grid_and_count_runs():
         for e in range(off, off + nr * nc):
             assert 1 <= len(holders.get(e, ())) <= 2
     # brute-force runs: consecutive grid entries with the same holder set
-    want = 0
+    want = []
     for off, (nr, nc) in grids:
         prev = None
         for e in range(off, off + nr * nc):
             h = frozenset(holders[e])
-            want += h != prev
+            if h != prev:
+                want.append([off, e - off, e - off + 1])
+            else:
+                want[-1][2] += 1
             prev = h
-    assert driver.reduce_runs(layout, ranges) == want
-    assert driver.reduce_runs(layout, None) == len(grids)
+    assert [list(r) for r in driver.reduce_runs(layout, ranges)] == want
+    assert len(driver.reduce_runs(layout, None)) == len(grids)
+    # pieces: each run's entries from the first multiple of 4 to the last in one piece,
+    # each ragged end in its own
+    pieces = 0
+    for _, lo, hi in want:
+        quads = [e for e in range(lo, hi) if e % 4 == 0 and e + 4 <= hi]
+        pieces += 1 if not quads else 1 + (lo < quads[0]) + (quads[-1] + 4 < hi)
+    assert driver.reduce_pieces(layout, ranges) == pieces

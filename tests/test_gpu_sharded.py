@@ -158,15 +158,18 @@ def test_ranged_reduction_never_reads_untouched_slot_entries(dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_ranged_entry_matches_whole_slot_reduction(dtype):
-    """Random slot ranges over a packed buffer with padded views: the ranged reduction
-    equals the whole-slot reduction of slots zeroed outside their ranges (entries no slot
-    holds reduce to +0), both bit for bit against the oracle."""
+@pytest.mark.parametrize("padded", [True, False])
+def test_ranged_entry_matches_whole_slot_reduction(dtype, padded):
+    """Random slot ranges (ends anywhere, so runs of dense grids have ragged ends around
+    their 4-entry vector middle) over a packed buffer with padded or dense views: the
+    ranged reduction equals the whole-slot reduction of slots zeroed outside their ranges
+    (entries no slot holds reduce to +0), both bit for bit against the oracle."""
     from mxfp8_master_weight_gb300 import api
-    rng = np.random.default_rng(11)
+    rng = np.random.default_rng(11 + padded)
     S, rows, cols = 5, 96, 200
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
-    P = rr * 9 + 64 + cr * 203
+    ldr, ldc = (9, 203) if padded else (rc, cc)
+    P = rr * ldr + 64 + cr * ldc
     garbage = np.abs(wl.normal_f32(rng, (S, P))) * np.float32(1e3)
     ranges = []
     for s in range(S):
@@ -185,15 +188,15 @@ def test_ranged_entry_matches_whole_slot_reduction(dtype):
     want = oracle.max_reduce(zeroed)
     slots = to_device(garbage).view(S, P)
     reduced = torch.full((P,), 7.0, dtype=dtype, device="cuda")
-    vr = reduced[:rr * 9].view(rr, 9)
-    vc = reduced[rr * 9 + 64:].view(cr, 203)
+    vr = reduced[:rr * ldr].view(rr, ldr)
+    vc = reduced[rr * ldr + 64:].view(cr, ldc)
     sr = torch.zeros((rr, rc), dtype=torch.uint8, device="cuda")
     scl = torch.zeros((cr, cc), dtype=torch.uint8, device="cuda")
     api.mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, [(vr, vc, sr, scl, rows, cols)], ranges)
     torch.cuda.synchronize()
     got = to_host(reduced)
     wf = want if dtype == torch.float32 else wl.bf16_bits_to_f32(want)
-    for o, ld, nr, nc, st in ((0, 9, rr, rc, sr), (rr * 9 + 64, 203, cr, cc, scl)):
+    for o, ld, nr, nc, st in ((0, ldr, rr, rc, sr), (rr * ldr + 64, ldc, cr, cc, scl)):
         g = got[o:o + nr * ld].reshape(nr, ld)[:, :nc]
         w_ = want[o:o + nr * ld].reshape(nr, ld)[:, :nc]
         assert np.array_equal(g.view(np.uint16 if dtype == torch.bfloat16 else np.uint32),
