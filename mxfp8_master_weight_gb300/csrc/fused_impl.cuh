@@ -402,11 +402,231 @@ cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool ve
                  : launch<T, false, false, kModel, false>(jobs, n, dev, stream);
 }
 
+// ---------------------------------------------------------------- staged one-pass kernel
+// A single fragment made of whole 32-row bands, columns a multiple of the tile width, a
+// 16-byte aligned virtual base and word-aligned outputs (a rank or a host pipeline chunk
+// holding whole bands, a single rank holding a whole weight): a block of 8 warps owns one
+// tile at a time.  Every thread copies 4 of the tile's 16-byte chunks into shared memory
+// with cp.async, kStages tiles deep, so the DRAM reads of the next tiles run while the
+// block works on this one; both passes then read shared memory.  Warp w owns rows 4w..4w+3
+// of the tile: pass 1 folds their row-block maxima (butterflies, as in the register
+// kernel) and their column maxima, which go to shared memory; after one barrier every lane
+// combines the 8 warps' column maxima of its V columns, and pass 2 casts the warp's rows.
+constexpr int kStages = 3;
+constexpr int kTileChunks = 32 * 32;                    // 16-byte chunks per tile
+constexpr int kStagedSmem = (kStages * kTileChunks + kWarps * 32) * 16;  // 52 KB
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <class T, bool kCol, bool kExp>
+__device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&tile)[32][32],
+                                            uint4 (&colpart)[kWarps][32], int64_t row0, int64_t col0,
+                                            int warp, int lane) {
+  const int64_t cols = p.g.cols;
+  const int64_t j = col0 + lane * T::V;
+  const int64_t blk = j >> 5;
+  const bool writer = (lane % T::G) == 0;
+  float rowmul[4];
+  // pass 1: rows 4w .. 4w+3
+  if constexpr (kExp) {
+    static_assert(T::kBytes == 4, "exponent-only maxima are taken on FP32 high halves");
+    uint32_t c01 = 0u, c23 = 0u;
+#pragma unroll
+    for (int rr = 0; rr < 4; rr += 2) {
+      const int r = warp * 4 + rr;
+      const uint4 va = tile[r][lane], vb = tile[r + 1][lane];
+      const uint32_t a01 = abs_hi_halves(va.x, va.y), a23 = abs_hi_halves(va.z, va.w);
+      const uint32_t b01 = abs_hi_halves(vb.x, vb.y), b23 = abs_hi_halves(vb.z, vb.w);
+      if constexpr (kCol) {
+        c01 = __vmaxu2(c01, __vmaxu2(a01, b01));
+        c23 = __vmaxu2(c23, __vmaxu2(a23, b23));
+      }
+      const uint32_t ha = __vmaxu2(a01, a23), hb = __vmaxu2(b01, b23);
+      uint32_t w = __vmaxu2(__byte_perm(ha, hb, 0x5410), __byte_perm(ha, hb, 0x7632));
+#pragma unroll
+      for (int off = 1; off < T::G; off <<= 1) w = __vmaxu2(w, __shfl_xor_sync(kFullMask, w, off));
+      const uint32_t ea = e8m0_from_half(w & 0xffffu), eb = e8m0_from_half(w >> 16);
+      rowmul[rr] = scale_multiplier(ea);
+      rowmul[rr + 1] = scale_multiplier(eb);
+      if (writer) {
+        const int64_t i = row0 + r;
+        p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(ea);
+        p.s_r[(i + 1) * p.ld_sr + blk] = static_cast<uint8_t>(eb);
+      }
+    }
+    if constexpr (kCol) colpart[warp][lane] = make_uint4(c01, c23, 0u, 0u);
+  } else {
+    uint4 cm = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      const int r = warp * 4 + rr;
+      const uint4 a = chunk_abs<T>(tile[r][lane]);
+      if constexpr (kCol) cm = chunk_max<T>(cm, a);
+      const uint32_t m = group_max<T>(chunk_reduce<T>(a));
+      const uint32_t e = e8m0_from_bits<T>(m);
+      rowmul[rr] = scale_multiplier(e);
+      if (writer) {
+        const int64_t i = row0 + r;
+        p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
+        if (p.amax_r != nullptr) store_bits<T>(p.amax_r, i * p.ld_r + blk, canonical_nan<T>(m));
+      }
+    }
+    if constexpr (kCol) colpart[warp][lane] = cm;
+  }
+  // column maxima of this lane's V columns over the 32 rows, scales, multipliers
+  float mc[T::V];
+  if constexpr (kCol) {
+    __syncthreads();
+    if constexpr (kExp) {
+      uint32_t c01 = 0u, c23 = 0u;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const uint4 q = colpart[w][lane];
+        c01 = __vmaxu2(c01, q.x);
+        c23 = __vmaxu2(c23, q.y);
+      }
+      const uint32_t sb[4] = {e8m0_from_half(c01 & 0xffffu), e8m0_from_half(c01 >> 16),
+                              e8m0_from_half(c23 & 0xffffu), e8m0_from_half(c23 >> 16)};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mc[k] = scale_multiplier(sb[k]);
+      if (warp == 0) {
+        uint8_t* dst = p.s_c + (row0 >> 5) * p.ld_sc + j;
+        if (p.vec_sc) {
+          *reinterpret_cast<uint32_t*>(dst) = sb[0] | (sb[1] << 8) | (sb[2] << 16) | (sb[3] << 24);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = static_cast<uint8_t>(sb[k]);
+        }
+      }
+    } else {
+      uint4 cm = colpart[0][lane];
+#pragma unroll
+      for (int w = 1; w < kWarps; ++w) cm = chunk_max<T>(cm, colpart[w][lane]);
+      if (warp == 0) {
+        store_col_stats<T, kCol>(p, row0, j, cm, mc);
+      } else {
+#pragma unroll
+        for (int k = 0; k < T::V; ++k) mc[k] = scale_multiplier(e8m0_from_bits<T>(chunk_get<T>(cm, k)));
+      }
+    }
+  }
+  // pass 2: cast the warp's rows
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    const int r = warp * 4 + rr;
+    float y[T::V];
+    model_values<T, kModelBF16>(tile[r][lane], y);
+    float mr[T::V];
+#pragma unroll
+    for (int k = 0; k < T::V; ++k) mr[k] = rowmul[rr];
+    const int64_t o = (row0 + r) * cols + j + p.out_shift;
+    store_chunk<T, true>(p.out_r + o, quantize_chunk<T>(y, mr));
+    if constexpr (kCol) store_chunk<T, true>(p.out_c + o, quantize_chunk<T>(y, mc));
+  }
+}
+
+template <class T, bool kCol, bool kExp>
+__global__ void __launch_bounds__(kThreads) k_fused_staged(const __grid_constant__ FusedParams p) {
+  extern __shared__ __align__(16) unsigned char staged_smem[];
+  auto tiles = reinterpret_cast<uint4 (*)[32][32]>(staged_smem);
+  auto& colpart = *reinterpret_cast<uint4 (*)[kWarps][32]>(staged_smem + kStages * kTileChunks * 16);
+  grid_dependency_sync();
+  constexpr int TW = tile_width<T>();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const FragGeom& g = p.g;
+  const int64_t ntiles = g.ntiles, cols = g.cols;
+  const int64_t row_bytes = cols * T::kBytes;
+  const char* in = static_cast<const char*>(p.in);
+  auto origin = [&](int64_t t, int64_t& row0, int64_t& col0) {
+    row0 = (g.band0 + t / g.coltiles) * 32;
+    col0 = (t % g.coltiles) * TW;
+  };
+  // every thread copies chunks c = k * 256 + tid of the tile: row c / 32, chunk c % 32
+  auto issue = [&](int64_t t, int stage) {
+    int64_t row0, col0;
+    origin(t, row0, col0);
+    const char* src = in + (row0 * cols + col0 - g.start) * T::kBytes;
+#pragma unroll
+    for (int k = 0; k < kTileChunks / kThreads; ++k) {
+      const int c = k * kThreads + int(threadIdx.x);
+      cp_async16(&tiles[stage][c >> 5][c & 31], src + (c >> 5) * row_bytes + (c & 31) * 16);
+    }
+  };
+  const int64_t step = gridDim.x;
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    const int64_t t = blockIdx.x + s * step;
+    if (t < ntiles) issue(t, s);
+    cp_async_commit();  // one group per tile slot, empty past the last tile
+  }
+  int stage = 0;
+  for (int64_t t = blockIdx.x; t < ntiles; t += step) {
+    const int64_t tn = t + (kStages - 1) * step;
+    if (tn < ntiles) issue(tn, (stage + kStages - 1) % kStages);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();  // this thread's copies of tile t have landed
+    __syncthreads();               // and every thread's
+    int64_t row0, col0;
+    origin(t, row0, col0);
+    staged_tile<T, kCol, kExp>(p, tiles[stage], colpart, row0, col0, warp, lane);
+    __syncthreads();               // the stage and the column partials may be reused
+    stage = stage + 1 == kStages ? 0 : stage + 1;
+  }
+  cp_async_wait<0>();
+}
+
+template <class T, bool kCol, bool kExp>
+cudaError_t launch_staged_kernel(const FusedParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+  static std::atomic<int> occupancy[kMaxDevices];
+  const auto kernel = k_fused_staged<T, kCol, kExp>;
+  int occ = dev.device < kMaxDevices ? occupancy[dev.device].load() : 0;
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStagedSmem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, kStagedSmem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) occ = 1;
+    if (dev.device < kMaxDevices) occupancy[dev.device].store(occ);
+  }
+  const unsigned grid = balanced_grid(p.g.ntiles, 1, int64_t(dev.sms) * occ);
+  return launch_kernel(kernel, grid, kThreads, kStagedSmem, stream, p);
+}
+
+// Whether one job can take the staged kernel (see above).
+template <class T>
+bool staged_ok(const FusedParams& p, bool shifted, bool vec_out) {
+  const FragGeom& g = p.g;
+  const int64_t band = 32 * g.cols;
+  return !shifted && vec_out && g.cols % tile_width<T>() == 0 && g.end > g.start &&
+         g.start % band == 0 && g.end % band == 0;
+}
+
+template <class T>
+cudaError_t launch_staged(const FusedParams& p, const DeviceInfo& dev, cudaStream_t stream) {
+  const bool col = p.out_c != nullptr;
+  if constexpr (T::kBytes == 4) {
+    if (p.amax_r == nullptr && p.amax_c == nullptr) {
+      return col ? launch_staged_kernel<T, true, true>(p, dev, stream)
+                 : launch_staged_kernel<T, false, true>(p, dev, stream);
+    }
+  }
+  return col ? launch_staged_kernel<T, true, false>(p, dev, stream)
+             : launch_staged_kernel<T, false, false>(p, dev, stream);
+}
+
 // All launches for one input dtype T (instantiated by that dtype's translation unit).
 template <class T>
 cudaError_t launch_for_dtype(const FusedParams* jobs, int n, bool shifted, bool vec_out, int model,
                              const DeviceInfo& dev, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
+  if (n == 1 && model == kModelBF16 && staged_ok<T>(jobs[0], shifted, vec_out))
+    return launch_staged<T>(jobs[0], dev, stream);
   if (model == kModelF16) return launch_variant<T, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
   return launch_variant<T, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
 }

@@ -224,3 +224,30 @@ def test_fused_without_amax_outputs(colwise, shift):
         got = _fused(frag, rows, cols, start, colwise, shift=shift, with_amax=False)
         want = _oracle_fragment(frag, rows, cols, start, colwise)
         assert_bitwise(got[2:], want[2:], f"no amax out, shift {shift} [{start},+{length})")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("with_amax", [True, False])
+@pytest.mark.parametrize("colwise", [True, False])
+def test_fused_staged_path(dtype, with_amax, colwise):
+    """Fragments of whole 32-row bands of a weight whose columns are a multiple of the
+    tile width, aligned buffers and outputs: the one-pass kernel that stages tiles in
+    shared memory.  Whole weight, interior band ranges and a single band; bit-identical
+    to the oracle (values spread over 12 decades, special values in the first rows)."""
+    rows, cols = 32 * 13, 1024
+    rng = np.random.default_rng(70 + with_amax + 2 * colwise)
+    n = rows * cols
+    x = wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-6, 6, n).astype(np.float32)
+    x[:8] = np.array([0.0, -0.0, 1e-40, 2.0, np.nextafter(np.float32(2.0), np.float32(0)),
+                      448.0, -3.0e38, 1.5], np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    for a, b in ((0, rows), (32, 32 * 9), (32 * 12, rows), (64, 96)):
+        start, length = a * cols, (b - a) * cols
+        frag = np.ascontiguousarray(x[start:start + length])
+        got = _fused(frag, rows, cols, start, colwise, with_amax=with_amax)
+        want = _oracle_fragment(frag, rows, cols, start, colwise)
+        if with_amax:
+            assert_bitwise(got, want, f"{dtype} staged rows [{a},{b})")
+        else:
+            assert_bitwise(got[2:], want[2:], f"{dtype} staged rows [{a},{b}) no amax")
