@@ -412,7 +412,10 @@ cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool ve
 // of the tile: pass 1 folds their row-block maxima (butterflies, as in the register
 // kernel) and their column maxima, which go to shared memory; after one barrier every lane
 // combines the 8 warps' column maxima of its V columns, and pass 2 casts the warp's rows.
-constexpr int kStages = 3;
+#ifndef MXFP8_STAGED_STAGES
+#define MXFP8_STAGED_STAGES 3
+#endif
+constexpr int kStages = MXFP8_STAGED_STAGES;
 constexpr int kTileChunks = 32 * 32;                    // 16-byte chunks per tile
 constexpr int kStagedSmem = (kStages * kTileChunks + kWarps * 32) * 16;  // 52 KB
 
@@ -531,6 +534,24 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
   }
 }
 
+// Position of a tile: its first row and its column-tile index.  A block's tiles are
+// blockIdx.x, blockIdx.x + gridDim.x, ...; the position advances by that stride with a
+// carry instead of a 64-bit division per tile.
+struct TilePos {
+  int64_t row0;
+  int32_t ct;
+};
+
+__device__ __forceinline__ void advance(TilePos& p, int32_t step_bands, int32_t step_ct, int32_t coltiles) {
+  p.ct += step_ct;
+  int64_t bands = step_bands;
+  if (p.ct >= coltiles) {
+    p.ct -= coltiles;
+    bands += 1;
+  }
+  p.row0 += 32 * bands;
+}
+
 template <class T, bool kCol, bool kExp>
 __global__ void __launch_bounds__(kThreads) k_fused_staged(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(16) unsigned char staged_smem[];
@@ -542,41 +563,44 @@ __global__ void __launch_bounds__(kThreads) k_fused_staged(const __grid_constant
   const FragGeom& g = p.g;
   const int64_t ntiles = g.ntiles, cols = g.cols;
   const int64_t row_bytes = cols * T::kBytes;
-  const char* in = static_cast<const char*>(p.in);
-  auto origin = [&](int64_t t, int64_t& row0, int64_t& col0) {
-    row0 = (g.band0 + t / g.coltiles) * 32;
-    col0 = (t % g.coltiles) * TW;
-  };
-  // every thread copies chunks c = k * 256 + tid of the tile: row c / 32, chunk c % 32
-  auto issue = [&](int64_t t, int stage) {
-    int64_t row0, col0;
-    origin(t, row0, col0);
-    const char* src = in + (row0 * cols + col0 - g.start) * T::kBytes;
+  // this thread copies chunks c = k * 256 + tid of every tile: row 8k + warp, chunk lane
+  int64_t off[kTileChunks / kThreads];
 #pragma unroll
-    for (int k = 0; k < kTileChunks / kThreads; ++k) {
-      const int c = k * kThreads + int(threadIdx.x);
-      cp_async16(&tiles[stage][c >> 5][c & 31], src + (c >> 5) * row_bytes + (c & 31) * 16);
-    }
+  for (int k = 0; k < kTileChunks / kThreads; ++k) off[k] = (8 * k + warp) * row_bytes + lane * 16;
+  const char* base = static_cast<const char*>(p.in) - g.start * T::kBytes;  // weight element 0
+  auto issue = [&](const TilePos& tp, int stage) {
+    const char* src = base + (tp.row0 * cols + int64_t(tp.ct) * TW) * T::kBytes;
+#pragma unroll
+    for (int k = 0; k < kTileChunks / kThreads; ++k)
+      cp_async16(&tiles[stage][8 * k + warp][lane], src + off[k]);
   };
+  const int32_t coltiles = g.coltiles;
+  const int32_t step_bands = int32_t(gridDim.x / coltiles), step_ct = int32_t(gridDim.x % coltiles);
+  const TilePos first = {(g.band0 + int64_t(blockIdx.x / coltiles)) * 32, int32_t(blockIdx.x % coltiles)};
   const int64_t step = gridDim.x;
+  TilePos ip = first;
+  int64_t ti = blockIdx.x;
 #pragma unroll
   for (int s = 0; s < kStages - 1; ++s) {
-    const int64_t t = blockIdx.x + s * step;
-    if (t < ntiles) issue(t, s);
+    if (ti < ntiles) issue(ip, s);
     cp_async_commit();  // one group per tile slot, empty past the last tile
+    ti += step;
+    advance(ip, step_bands, step_ct, coltiles);
   }
-  int stage = 0;
+  TilePos tp = first;
+  int stage = 0, istage = kStages - 1;
   for (int64_t t = blockIdx.x; t < ntiles; t += step) {
-    const int64_t tn = t + (kStages - 1) * step;
-    if (tn < ntiles) issue(tn, (stage + kStages - 1) % kStages);
+    if (ti < ntiles) issue(ip, istage);
     cp_async_commit();
+    ti += step;
+    advance(ip, step_bands, step_ct, coltiles);
+    istage = istage + 1 == kStages ? 0 : istage + 1;
     cp_async_wait<kStages - 1>();  // this thread's copies of tile t have landed
     __syncthreads();               // and every thread's
-    int64_t row0, col0;
-    origin(t, row0, col0);
-    staged_tile<T, kCol, kExp>(p, tiles[stage], colpart, row0, col0, warp, lane);
+    staged_tile<T, kCol, kExp>(p, tiles[stage], colpart, tp.row0, int64_t(tp.ct) * TW, warp, lane);
     __syncthreads();               // the stage and the column partials may be reused
     stage = stage + 1 == kStages ? 0 : stage + 1;
+    advance(tp, step_bands, step_ct, coltiles);
   }
   cp_async_wait<0>();
 }
@@ -625,8 +649,10 @@ template <class T>
 cudaError_t launch_for_dtype(const FusedParams* jobs, int n, bool shifted, bool vec_out, int model,
                              const DeviceInfo& dev, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
+#ifndef MXFP8_NO_STAGED
   if (n == 1 && model == kModelBF16 && staged_ok<T>(jobs[0], shifted, vec_out))
     return launch_staged<T>(jobs[0], dev, stream);
+#endif
   if (model == kModelF16) return launch_variant<T, kModelF16>(jobs, n, shifted, vec_out, dev, stream);
   return launch_variant<T, kModelBF16>(jobs, n, shifted, vec_out, dev, stream);
 }
