@@ -93,15 +93,15 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
     load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
-      float y[T::V];
-      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = scale_multiplier(sb[r]);
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
+      uint2 qr, qc;
+      cast_chunk<T, kModel, kCol>(v[r], mr, mc, qr, qc);
       const int64_t o = o0 + (rb + r) * cols;
-      store_chunk_at<T, kM>(p.out_r + o, quantize_chunk<T>(y, mr));
-      if constexpr (kCol) store_chunk_at<T, kM>(p.out_c + o, quantize_chunk<T>(y, mc));
+      store_chunk_at<T, kM>(p.out_r + o, qr);
+      if constexpr (kCol) store_chunk_at<T, kM>(p.out_c + o, qc);
     }
   }
 }
@@ -189,14 +189,11 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
       const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
       if (bits == 0) continue;
       const int64_t i = row0 + rb + r;
-      float y[T::V];
-      model_values<T, kModel>(v[r], y);
       float mr[T::V];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = mrow[r];
-      const uint2 qr = quantize_chunk<T>(y, mr);
-      uint2 qc = make_uint2(0u, 0u);
-      if constexpr (kCol) qc = quantize_chunk<T>(y, mc);
+      uint2 qr, qc = make_uint2(0u, 0u);
+      cast_chunk<T, kModel, kCol>(v[r], mr, mc, qr, qc);
       const int64_t o = i * g.cols + j + p.out_shift;
       if (word_ok && bits == kChunkBits) {
         store_chunk<T, true>(p.out_r + o, qr);

@@ -317,8 +317,13 @@ template <class T>
 __device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
   uint2 q;
   float p[T::V];
+#ifdef MXFP8_SCALAR_MUL
+#pragma unroll
+  for (int k = 0; k < T::V; ++k) p[k] = __fmul_rn(y[k], mult[k]);
+#else
 #pragma unroll
   for (int k = 0; k < T::V; k += 2) mul2_rn(y[k], y[k + 1], mult[k], mult[k + 1], p[k], p[k + 1]);
+#endif
   q.x = e4m3x2_rn_sat(p[0], p[1]) | (e4m3x2_rn_sat(p[2], p[3]) << 16);
   if constexpr (T::V == 8) {
     q.y = e4m3x2_rn_sat(p[4], p[5]) | (e4m3x2_rn_sat(p[6], p[7]) << 16);
@@ -326,6 +331,16 @@ __device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const fl
     q.y = 0;
   }
   return q;
+}
+
+// Rowwise and (kCol) columnwise E4M3 bytes of one input chunk through the model dtype.
+template <class T, int kModel, bool kCol>
+__device__ __forceinline__ void cast_chunk(const uint4& c, const float (&mr)[T::V], const float (&mc)[T::V],
+                                           uint2& qr, uint2& qc) {
+  float y[T::V];
+  model_values<T, kModel>(c, y);
+  qr = quantize_chunk<T>(y, mr);
+  if constexpr (kCol) qc = quantize_chunk<T>(y, mc);
 }
 
 // Store V bytes: one 4- or 8-byte word when the destination is aligned, else bytes.

@@ -189,15 +189,15 @@ __device__ __forceinline__ void fused_tile_fast(const FusedParams& p, int64_t ro
     load_rows<NB, kS, true>(v, src + rb * row_bytes, row_bytes, lane, drop);
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
-      float y[T::V];
-      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = rsc.m[warp][rb + r][grp];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
+      uint2 qr, qc;
+      cast_chunk<T, kModel, kCol>(v[r], mr, mc, qr, qc);
       const int64_t o = o0 + (rb + r) * cols;
-      store_chunk<T, kVec>(p.out_r + o, quantize_chunk<T>(y, mr));
-      if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, quantize_chunk<T>(y, mc));
+      store_chunk<T, kVec>(p.out_r + o, qr);
+      if constexpr (kCol) store_chunk<T, kVec>(p.out_c + o, qc);
     }
   }
   __syncwarp();
@@ -273,15 +273,12 @@ __device__ __noinline__ void fused_tile_masked(const FusedParams& p, int64_t row
     for (int r = 0; r < kMaskBatch; ++r) {
       const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
       if (bits == 0) continue;
-      float y[T::V];
-      model_values<T, kModel>(v[r], y);
       float mr[T::V];
       const float m = rsc.m[warp][rb + r][grp];
 #pragma unroll
       for (int k = 0; k < T::V; ++k) mr[k] = m;
-      const uint2 qr = quantize_chunk<T>(y, mr);
-      uint2 qc = make_uint2(0u, 0u);
-      if constexpr (kCol) qc = quantize_chunk<T>(y, mc);
+      uint2 qr, qc = make_uint2(0u, 0u);
+      cast_chunk<T, kModel, kCol>(v[r], mr, mc, qr, qc);
       const int64_t o = (row0 + rb + r) * g.cols + j + p.out_shift;
       if (word_ok && bits == kChunkBits) {
         store_chunk<T, true>(p.out_r + o, qr);
@@ -413,7 +410,7 @@ cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool ve
 // kernel) and their column maxima, which go to shared memory; after one barrier every lane
 // combines the 8 warps' column maxima of its V columns, and pass 2 casts the warp's rows.
 #ifndef MXFP8_STAGED_STAGES
-#define MXFP8_STAGED_STAGES 3
+#define MXFP8_STAGED_STAGES 2
 #endif
 constexpr int kStages = MXFP8_STAGED_STAGES;
 constexpr int kTileChunks = 32 * 32;                    // 16-byte chunks per tile
@@ -523,14 +520,14 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
 #pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
     const int r = warp * 4 + rr;
-    float y[T::V];
-    model_values<T, kModelBF16>(tile[r][lane], y);
     float mr[T::V];
 #pragma unroll
     for (int k = 0; k < T::V; ++k) mr[k] = rowmul[rr];
+    uint2 qr, qc;
+    cast_chunk<T, kModelBF16, kCol>(tile[r][lane], mr, mc, qr, qc);
     const int64_t o = (row0 + r) * cols + j + p.out_shift;
-    store_chunk<T, true>(p.out_r + o, quantize_chunk<T>(y, mr));
-    if constexpr (kCol) store_chunk<T, true>(p.out_c + o, quantize_chunk<T>(y, mc));
+    store_chunk<T, true>(p.out_r + o, qr);
+    if constexpr (kCol) store_chunk<T, true>(p.out_c + o, qc);
   }
 }
 
