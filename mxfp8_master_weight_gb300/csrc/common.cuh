@@ -317,13 +317,8 @@ template <class T>
 __device__ __forceinline__ uint2 quantize_chunk(const float (&y)[T::V], const float (&mult)[T::V]) {
   uint2 q;
   float p[T::V];
-#ifdef MXFP8_SCALAR_MUL
-#pragma unroll
-  for (int k = 0; k < T::V; ++k) p[k] = __fmul_rn(y[k], mult[k]);
-#else
 #pragma unroll
   for (int k = 0; k < T::V; k += 2) mul2_rn(y[k], y[k + 1], mult[k], mult[k + 1], p[k], p[k + 1]);
-#endif
   q.x = e4m3x2_rn_sat(p[0], p[1]) | (e4m3x2_rn_sat(p[2], p[3]) << 16);
   if constexpr (T::V == 8) {
     q.y = e4m3x2_rn_sat(p[4], p[5]) | (e4m3x2_rn_sat(p[6], p[7]) << 16);
