@@ -416,7 +416,8 @@ cudaError_t launch_variant(const FusedParams* jobs, int n, bool shifted, bool ve
 #endif
 constexpr int kStages = MXFP8_STAGED_STAGES;
 constexpr int kTileChunks = 32 * 32;                    // 16-byte chunks per tile
-constexpr int kStagedSmem = (kStages * kTileChunks + kWarps * 32) * 16;  // 36 KB at 2 stages
+// tiles, the warps' column maxima, and the 256 multipliers 2^(127 - s) of the E8M0 bytes
+constexpr int kStagedSmem = (kStages * kTileChunks + kWarps * 32) * 16 + 256 * 4;  // 37 KB at 2 stages
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
@@ -428,7 +429,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 
 template <class T, bool kCol, bool kExp>
 __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&tile)[32][32],
-                                            uint4 (&colpart)[kWarps][32], int64_t row0, int64_t col0,
+                                            uint4 (&colpart)[kWarps][32], const float* mult,
+                                            int64_t row0, int64_t col0,
                                             int warp, int lane) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
@@ -454,8 +456,8 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
 #pragma unroll
       for (int off = 1; off < T::G; off <<= 1) w = __vmaxu2(w, __shfl_xor_sync(kFullMask, w, off));
       const uint32_t ea = e8m0_from_half(w & 0xffffu), eb = e8m0_from_half(w >> 16);
-      rowmul[rr] = scale_multiplier(ea);
-      rowmul[rr + 1] = scale_multiplier(eb);
+      rowmul[rr] = mult[ea];
+      rowmul[rr + 1] = mult[eb];
       if (writer) {
         const int64_t i = row0 + r;
         p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(ea);
@@ -472,7 +474,7 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
       if constexpr (kCol) cm = chunk_max<T>(cm, a);
       const uint32_t m = group_max<T>(chunk_reduce<T>(a));
       const uint32_t e = e8m0_from_bits<T>(m);
-      rowmul[rr] = scale_multiplier(e);
+      rowmul[rr] = mult[e];
       if (writer) {
         const int64_t i = row0 + r;
         p.s_r[i * p.ld_sr + blk] = static_cast<uint8_t>(e);
@@ -496,7 +498,7 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
       const uint32_t sb[4] = {e8m0_from_half(c01 & 0xffffu), e8m0_from_half(c01 >> 16),
                               e8m0_from_half(c23 & 0xffffu), e8m0_from_half(c23 >> 16)};
 #pragma unroll
-      for (int k = 0; k < 4; ++k) mc[k] = scale_multiplier(sb[k]);
+      for (int k = 0; k < 4; ++k) mc[k] = mult[sb[k]];
       if (warp == 0) {
         uint8_t* dst = p.s_c + (row0 >> 5) * p.ld_sc + j;
         if (p.vec_sc) {
@@ -514,7 +516,7 @@ __device__ __forceinline__ void staged_tile(const FusedParams& p, const uint4 (&
         store_col_stats<T, kCol>(p, row0, j, cm, mc);
       } else {
 #pragma unroll
-        for (int k = 0; k < T::V; ++k) mc[k] = scale_multiplier(e8m0_from_bits<T>(chunk_get<T>(cm, k)));
+        for (int k = 0; k < T::V; ++k) mc[k] = mult[e8m0_from_bits<T>(chunk_get<T>(cm, k))];
       }
     }
   }
@@ -556,6 +558,9 @@ __global__ void __launch_bounds__(kThreads) k_fused_staged(const __grid_constant
   extern __shared__ __align__(16) unsigned char staged_smem[];
   auto tiles = reinterpret_cast<uint4 (*)[32][32]>(staged_smem);
   auto& colpart = *reinterpret_cast<uint4 (*)[kWarps][32]>(staged_smem + kStages * kTileChunks * 16);
+  float* mult = reinterpret_cast<float*>(staged_smem + (kStages * kTileChunks + kWarps * 32) * 16);
+  mult[threadIdx.x] = scale_multiplier(threadIdx.x);  // 256 threads, 256 E8M0 bytes; read after
+                                                      // the first barrier below
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -589,15 +594,16 @@ __global__ void __launch_bounds__(kThreads) k_fused_staged(const __grid_constant
   TilePos tp = first;
   int stage = 0, istage = kStages - 1;
   for (int64_t t = blockIdx.x; t < ntiles; t += step) {
+    cp_async_wait<kStages - 2>();  // this thread's copies of tile t have landed
+    // every thread's copies of tile t have landed, and every thread is done with tile t - 1:
+    // its stage may take the next tile and the column partials may be rewritten
+    __syncthreads();
     if (ti < ntiles) issue(ip, istage);
     cp_async_commit();
     ti += step;
     advance(ip, step_bands, step_ct, coltiles);
     istage = istage + 1 == kStages ? 0 : istage + 1;
-    cp_async_wait<kStages - 1>();  // this thread's copies of tile t have landed
-    __syncthreads();               // and every thread's
-    staged_tile<T, kCol, kExp>(p, tiles[stage], colpart, tp.row0, int64_t(tp.ct) * TW, warp, lane);
-    __syncthreads();               // the stage and the column partials may be reused
+    staged_tile<T, kCol, kExp>(p, tiles[stage], colpart, mult, tp.row0, int64_t(tp.ct) * TW, warp, lane);
     stage = stage + 1 == kStages ? 0 : stage + 1;
     advance(tp, step_bands, step_ct, coltiles);
   }
