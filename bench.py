@@ -20,7 +20,9 @@ for the current kernel code under profiles/).  `clocks` comes from nvidia-smi sa
 over at least a second of continuous load around the timed region.  `e2e` runs the
 same four-step flow on pinned host buffers (copy-in, per-chunk partial amax, MAX
 reduction + scales, per-chunk partial cast, copy-out, all inside its timed region);
-`e2e_one_pass` the pipelined one-pass path over its own bytes.  Outside the timed
+`e2e_one_pass` the one-pass kernel reading and writing the pinned host buffers directly
+(its staged-copy pipeline beside it), over its own bytes; both give per-step spreads and
+the flow its measured copy-engine bound.  Outside the timed
 steps: `fused_whole_blocks` (the one-pass kernel on the same weight), `sharded_batch`
 (the multi-fragment driver on the config-5 batch in four emulated shards, with its
 phases) and `other_configs` (configs 1-3 and the weight row-only, CUDA graphs of
@@ -445,6 +447,84 @@ KERNEL_SAMPLES = 256  # in-step samples per kernel, whatever --steps is
 FUSED_SAMPLES, FUSED_GROUP = 32, 8  # one-pass kernel: samples of back-to-back calls
 
 
+def spread(ms) -> dict:
+    """Median, 10th and 90th percentile and maximum of per-step milliseconds."""
+    v = sorted(ms)
+    if not v:
+        return {}
+    return {"median": round(statistics.median(v), 4), "p10": round(v[len(v) // 10], 4),
+            "p90": round(v[(9 * len(v)) // 10], 4), "max": round(v[-1], 4)}
+
+
+def copy_engine_rates(host_in, dev_in, host_out, dev_out, stream, reps: int = 4, rounds: int = 5) -> dict:
+    """GB/s of pinned-host <-> device copies on this GPU: host->device alone, device->host
+    alone, and each direction while the other runs (equal byte counts on two streams, each
+    timed to its own end); the best of `rounds` rounds of `reps` copies each, so that the
+    bound built from them is the lowest the engines have shown.  `host_in` and `dev_in` hold
+    the same bytes, so the copies leave the workload unchanged."""
+    import torch
+
+    dev = stream.device
+    nin = host_in.numel() * host_in.element_size()
+    nout = host_out.numel() * host_out.element_size()
+    m = min(nin, nout)
+    hin8, din8 = host_in.view(torch.uint8)[:m], dev_in.view(torch.uint8)[:m]
+
+    def timed(fn, nbytes):
+        fn()
+        torch.cuda.synchronize()
+        best = 0.0
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            best = max(best, nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9)
+        return round(best, 1)
+
+    h2d = timed(lambda: dev_in.copy_(host_in, non_blocking=True), nin)
+    d2h = timed(lambda: host_out.copy_(dev_out, non_blocking=True), nout)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    hout8, dout8 = host_out.view(torch.uint8)[:m], dev_out.view(torch.uint8)[:m]
+    c_in = c_out = 0.0
+    for _ in range(rounds):
+        start = torch.cuda.Event(enable_timing=True)
+        e_in, e_out = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for _ in range(reps):
+            with torch.cuda.stream(s_in):
+                din8.copy_(hin8, non_blocking=True)
+            with torch.cuda.stream(s_out):
+                hout8.copy_(dout8, non_blocking=True)
+        e_in.record(s_in)
+        e_out.record(s_out)
+        torch.cuda.synchronize()
+        c_in = max(c_in, m * reps / (start.elapsed_time(e_in) / 1e3) / 1e9)
+        c_out = max(c_out, m * reps / (start.elapsed_time(e_out) / 1e3) / 1e9)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
+    return {"h2d_gbs": h2d, "d2h_gbs": d2h, "concurrent_h2d_gbs": round(c_in, 1),
+            "concurrent_d2h_gbs": round(c_out, 1)}
+
+
+def copy_bound_s(h2d_bytes: int, d2h_bytes: int, link: dict) -> float:
+    """Seconds the copy engines need for one step's copies at the measured rates, with the
+    two directions overlapped as far as they go: both run together at their concurrent
+    rates until the shorter one ends, then the longer one runs alone at its own rate."""
+    r_in_c, r_out_c = link["concurrent_h2d_gbs"] * 1e9, link["concurrent_d2h_gbs"] * 1e9
+    r_in, r_out = link["h2d_gbs"] * 1e9, link["d2h_gbs"] * 1e9
+    if h2d_bytes / r_in_c >= d2h_bytes / r_out_c:
+        t = d2h_bytes / r_out_c
+        return t + (h2d_bytes - t * r_in_c) / r_in
+    t = h2d_bytes / r_in_c
+    return t + (d2h_bytes - t * r_out_c) / r_out
+
+
 def nvfp4_algorithmic_bytes(n: int, s_in: int = 4, colwise: bool = True) -> dict:
     """Compulsory HBM bytes per call of the NVFP4 kernels for an n-element fragment: F32
     1x16 / 16x1 block amaxes, E4M3 block scales, two E2M1 codes per byte."""
@@ -455,10 +535,13 @@ def nvfp4_algorithmic_bytes(n: int, s_in: int = 4, colwise: bool = True) -> dict
             "cast": n * s_in + blocks + dirs * n // 2}    # read x and scales, write codes
 
 
-def measure_nvfp4(x, dev, peak: float, frac_key: str) -> dict:
-    """The NVFP4 steps on the headline weight (16384x6144 FP32, both directions): partial
-    amax, scale update, partial cast, each timed like other_configs (graphs of 10 calls,
-    20 replays, 7 rounds, median); the input is larger than L2, so these are HBM figures."""
+def measure_nvfp4(x, dev, peak: float, frac_key: str, samples: int = 256, steps: int = 100) -> dict:
+    """The NVFP4 step on the headline weight (16384x6144 FP32, both directions): tensor amax
+    reset, partial amax, scale update, partial cast.  Each kernel's time is the median of
+    `samples` in-step samples (events around every phase), as for the MXFP8 step: the scale
+    update reads the block amaxes its predecessor just wrote, as it does in a real step
+    (timed alone its 63 MB would stay in L2).  The whole step is also timed over `steps`
+    back-to-back steps without events."""
     import torch
 
     from mxfp8_master_weight_gb300 import api
@@ -471,18 +554,51 @@ def measure_nvfp4(x, dev, peak: float, frac_key: str) -> dict:
     scl = torch.empty((cr, cc), dtype=torch.uint8, device=dev)
     qr = torch.empty(ROWS * COLS // 2, dtype=torch.uint8, device=dev)
     qc = torch.empty(ROWS * COLS // 2, dtype=torch.uint8, device=dev)
-    calls = {"amax": api.prepare_nvfp4_partial_amax(x, ar, ac, at, ROWS, COLS, 0),
-             "scales": api.prepare_nvfp4_update_scales(ar, ac, at, sr, scl, ROWS, COLS),
-             "cast": api.prepare_nvfp4_partial_cast(x, sr, scl, at, qr, qc, ROWS, COLS, 0)}
+    amax = api.prepare_nvfp4_partial_amax(x, ar, ac, at, ROWS, COLS, 0)
+    scales = api.prepare_nvfp4_update_scales(ar, ac, at, sr, scl, ROWS, COLS)
+    cast = api.prepare_nvfp4_partial_cast(x, sr, scl, at, qr, qc, ROWS, COLS, 0)
     stream = torch.cuda.current_stream(dev)
-    for c in calls.values():
-        c.call(stream)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        at.zero_()
+        amax.call(stream)
+        if ev:
+            ev[1].record(stream)
+        scales.call(stream)
+        if ev:
+            ev[2].record(stream)
+        cast.call(stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(5):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    step_us = a.elapsed_time(b) * 1e3 / steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(samples)]
+    for e in evs:
+        step(e)
+    torch.cuda.synchronize()
     nb = nvfp4_algorithmic_bytes(ROWS * COLS)
+    step_bytes = sum(nb.values())
     out = {"workload": "16384x6144 FP32 headline weight, full fragment, rowwise+columnwise NVFP4 "
                        "(E2M1, 16-value blocks with E4M3 scales, F32 tensor scale)",
-           "method": "CUDA graph of 10 calls, 20 replays per round, 7 rounds, median us per call"}
-    for nm, c in calls.items():
-        us = graph_us_per_call(c, stream, ROWS * COLS)
+           "method": f"median of {samples} in-step samples per kernel (events around each phase; "
+                     "the amax phase includes the 4-byte tensor-amax reset); step: "
+                     f"{steps} back-to-back steps without events",
+           "us_per_step": round(step_us, 2), "algorithmic_bytes_per_step": step_bytes,
+           "step_gbs": round(step_bytes / (step_us * 1e-6) / 1e9, 1),
+           "step_" + frac_key: round(step_bytes / (step_us * 1e-6) / 1e9 / peak, 4)}
+    for k, nm in enumerate(("amax", "scales", "cast")):
+        us = statistics.median(e[k].elapsed_time(e[k + 1]) * 1e3 for e in evs)
         gbs = nb[nm] / (us * 1e-6) / 1e9
         out[nm] = {"us_per_call": round(us, 3), "algorithmic_bytes": nb[nm], "gbs": round(gbs, 1),
                    frac_key: round(gbs / peak, 4)}
@@ -608,7 +724,7 @@ def run_ours(args):
     # (1) the four-step partial flow (partial amax per chunk as it lands, MAX reduction +
     # scales, partial cast per chunk, copies out) -- the same work as the timed step;
     # (2) the one-pass pipeline (chunks quantised by the one-pass kernel) over its own bytes.
-    from mxfp8_master_weight_gb300.host import HostPartialFlow, HostQuantizer
+    from mxfp8_master_weight_gb300.host import HostPartialFlow, HostQuantizer, ZeroCopyQuantizer
     out_r, out_c = sc.outputs[0]
     s_r, s_c = sc.scales[0]
     host_q = [torch.empty(out_r.shape, dtype=torch.uint8).pin_memory() for _ in range(2)]
@@ -619,27 +735,35 @@ def run_ours(args):
     d2h = 2 * n + s_r.numel() + s_c.numel()
 
     def time_host_path(run):
+        """Seconds for e2e_steps back-to-back calls, and each call's milliseconds (events
+        recorded on the caller's stream after every call: a call's copy-in does not wait
+        for that stream, so the events do not serialise consecutive calls)."""
         for _ in range(3):
             run()
         barrier(world)
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(e2e_steps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps + 1)]
+        ev[0].record(stream)
+        for i in range(e2e_steps):
             run()
-        e1.record(stream)
+            ev[i + 1].record(stream)
         torch.cuda.synchronize()
         barrier(world)
-        return e0.elapsed_time(e1) / 1e3
+        return ev[0].elapsed_time(ev[-1]) / 1e3, [ev[i].elapsed_time(ev[i + 1]) for i in range(e2e_steps)]
 
+    link = copy_engine_rates(host, x, host_q[0], out_r, stream)
+    bound_s = copy_bound_s(h2d, d2h, link)
     flow = HostPartialFlow(ROWS, COLS, True, device=dev, chunk_rows=args.e2e_chunk_rows)
-    flow_t = time_host_path(lambda: flow.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
+    flow_t, flow_per = time_host_path(lambda: flow.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
     flow_t, flow_bytes = aggregate_over_ranks(flow_t, step_bytes * e2e_steps, world, dev)
     flow_launches = flow.launches_per_run()
     flow_chunks = len(flow.chunks)
     del flow
-    hq = HostQuantizer(ROWS, COLS, True, device=dev, chunk_rows=args.e2e_chunk_rows, depth=3)
-    hq_t = time_host_path(lambda: hq.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
+    zc = ZeroCopyQuantizer(ROWS, COLS, True, device=dev)
+    zc_t, zc_per = time_host_path(lambda: zc.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
+    zc_t, zc_bytes = aggregate_over_ranks(zc_t, fused_bytes * e2e_steps, world, dev)
+    hq = HostQuantizer(ROWS, COLS, True, device=dev, chunk_rows=1024, depth=3)
+    hq_t, hq_per = time_host_path(lambda: hq.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
     hq_t, hq_bytes = aggregate_over_ranks(hq_t, fused_bytes * e2e_steps, world, dev)
 
     if rank != 0:
@@ -723,19 +847,33 @@ def run_ours(args):
         "e2e": {"value": round(flow_bytes / flow_t / 1e9, 1), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(flow_t / e2e_steps * 1e3, 4), "steps": e2e_steps,
+                "ms_per_step_spread": spread(flow_per),
                 "algorithmic_bytes_per_step": step_bytes,
                 "path": f"HostPartialFlow: partial amax per chunk as it lands ({flow_chunks} chunks of "
                         f"{args.e2e_chunk_rows} rows), MAX reduction + scales, partial cast per "
                         "chunk, copies out; 3 streams, device input double-buffered",
                 "gpu_launches_per_step": flow_launches,
-                "copy_gbs": round((h2d + d2h) * e2e_steps / flow_t / 1e9, 1)},
-        "e2e_one_pass": {"value": round(hq_bytes / hq_t / 1e9, 1), "unit": "GB/s",
+                "copy_gbs": round((h2d + d2h) * e2e_steps / flow_t / 1e9, 1),
+                "copy_engines": dict(link, bound_ms=round(bound_s * 1e3, 4),
+                                     frac_of_bound=round(bound_s * e2e_steps / flow_t, 4))},
+        "e2e_one_pass": {"value": round(zc_bytes / zc_t / 1e9, 1), "unit": "GB/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                         "ms_per_step": round(hq_t / e2e_steps * 1e3, 4), "steps": e2e_steps,
+                         "ms_per_step": round(zc_t / e2e_steps * 1e3, 4), "steps": e2e_steps,
+                         "ms_per_step_spread": spread(zc_per),
                          "algorithmic_bytes_per_step": fused_bytes,
-                         "path": f"HostQuantizer: {len(hq.chunks)} chunks of {hq.chunk_rows} rows, "
-                                 "3 streams, one-pass kernel per chunk",
-                         "copy_gbs": round((h2d + d2h) * e2e_steps / hq_t / 1e9, 1)},
+                         "path": "ZeroCopyQuantizer: one launch of the one-pass kernel reading the "
+                                 "pinned input and writing the pinned outputs over the CPU-GPU link "
+                                 "(the byte counts are those loads and stores; no copy engines)",
+                         "gpu_launches_per_step": 1,
+                         "link_gbs": round((h2d + d2h) * e2e_steps / zc_t / 1e9, 1),
+                         "staged_copies": {
+                             "path": f"HostQuantizer: {len(hq.chunks)} chunks of {hq.chunk_rows} rows, "
+                                     "3 streams, one-pass kernel per chunk",
+                             "value": round(hq_bytes / hq_t / 1e9, 1),
+                             "ms_per_step": round(hq_t / e2e_steps * 1e3, 4),
+                             "ms_per_step_spread": spread(hq_per),
+                             "copy_gbs": round((h2d + d2h) * e2e_steps / hq_t / 1e9, 1),
+                             "frac_of_copy_bound": round(bound_s * e2e_steps / hq_t, 4)}},
         "nvfp4": nvfp4,
         "other_configs": {
             "method": "CUDA graph of 50 calls (fragments <= 4M elements) else 10, 20 replays per "
@@ -758,8 +896,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--e2e-chunk-rows", type=int, default=1024,
-                    help="rows per chunk of the pipelined host-buffer (e2e) leg")
+    ap.add_argument("--e2e-chunk-rows", type=int, default=4096,
+                    help="rows per chunk of the four-step host-buffer (e2e) leg")
     ap.add_argument("--cpu-rows", type=int, default=8192,
                     help="rows of the workload the CPU-oracle baseline runs on")
     ap.add_argument("--clock-window-s", type=float, default=1.2,

@@ -104,3 +104,24 @@ def test_nvfp4_algorithmic_bytes_per_element():
     assert b["amax"] / n == pytest.approx(4.5)        # read 4 B, write 2 x 4 B / 16
     assert b["scales"] / n == pytest.approx(0.625)    # read 2 x 4 B / 16, write 2 B / 16
     assert b["cast"] / n == pytest.approx(5.125)      # read 4 B + 2 B / 16, write 2 x 0.5 B
+
+
+def test_copy_bound_closed_forms():
+    link = {"h2d_gbs": 200.0, "d2h_gbs": 100.0, "concurrent_h2d_gbs": 150.0, "concurrent_d2h_gbs": 50.0}
+    # one direction only: that direction alone at its own rate
+    assert bench.copy_bound_s(400e9, 0, link) == pytest.approx(2.0)
+    assert bench.copy_bound_s(0, 300e9, link) == pytest.approx(3.0)
+    # copy-out ends first: 50 GB at 50 GB/s (1 s, while 150 GB go in), then 250 GB alone at 200
+    assert bench.copy_bound_s(400e9, 50e9, link) == pytest.approx(1.0 + 250 / 200)
+    # copy-in ends first: 150 GB in 1 s (50 GB out meanwhile), then 50 GB out alone at 100
+    assert bench.copy_bound_s(150e9, 100e9, link) == pytest.approx(1.0 + 0.5)
+    # never below either direction alone, never above the two run one after the other
+    for a, b in ((400e9, 200e9), (10e9, 300e9), (1e9, 1e9)):
+        t = bench.copy_bound_s(a, b, link)
+        assert max(a / 200e9, b / 100e9) - 1e-12 <= t <= a / 150e9 + b / 50e9 + 1e-12
+
+
+def test_spread_percentiles():
+    assert bench.spread([]) == {}
+    s = bench.spread([float(v) for v in range(1, 21)])
+    assert s == {"median": 10.5, "p10": 3.0, "p90": 19.0, "max": 20.0}
