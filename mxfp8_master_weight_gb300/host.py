@@ -150,7 +150,7 @@ class HostPartialFlow:
     """
 
     def __init__(self, rows: int, cols: int, colwise: bool = True, dtype=torch.float32,
-                 device="cuda", chunk_rows: int = 1024, depth: int = 3):
+                 device="cuda", chunk_rows: int = 4096, depth: int = 3):
         if rows <= 0 or cols <= 0:
             raise ValueError("rows and cols must be positive")
         self.rows, self.cols, self.colwise, self.dtype = rows, cols, colwise, dtype
