@@ -13,7 +13,7 @@
 //   M       block multiplier fp32(S / decode(s)), 0 when s decodes to 0;
 //   q       data E2M1(fp32(y * M)), y the master value rounded to BF16 (nearest-even,
 //           saturating at 6), two codes per byte, the even position in the low nibble.
-// Every FP32 step is one correctly rounded operation (__fdiv_rn, mul.rn), so the codes
+// Every FP32 step is one correctly rounded operation (division, mul.rn), so the codes
 // are decided exactly as a scalar restatement of these steps decides them.
 //
 // Work unit as in the MXFP8 kernels: one warp per 32-row x (32*V)-column tile, one
@@ -72,9 +72,31 @@ __device__ __forceinline__ float tensor_scale(float g) {
   return isinf(s) ? FLT_MAX : s;
 }
 
+// fp32(a / 6), correctly rounded, by Markstein's division with a correctly rounded
+// reciprocal and an exact FMA remainder (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990):
+// q0 = a * RN(1/6), r = a - 6 q0 (exact), q = RN(q0 + r * RN(1/6)).  For every float a
+// from 2^-124 up to the largest float this equals the IEEE quotient (checked input by
+// input); below 2^-124 the remainder can be subnormal and inexact, so there, and for
+// negative, infinite and NaN inputs, the IEEE division is taken.  Three operations
+// instead of a full division per block amax.
+__device__ __forceinline__ float div6_rn(float a) {
+  constexpr float kInv6 = 0x1.555556p-3f;  // RN(1/6)
+  if (a >= 0x1p-124f && a <= FLT_MAX) {
+    const float q0 = __fmul_rn(a, kInv6);
+    const float r = __fmaf_rn(-6.0f, q0, a);
+    return __fmaf_rn(r, kInv6, q0);
+  }
+  return __fdiv_rn(a, 6.0f);
+}
+
+// fp32(fp32(A / 6) * S): the value the block scale is the E4M3 rounding of.
+__device__ __forceinline__ float block_scale_value(float a, float s_enc) {
+  return __fmul_rn(div6_rn(a), s_enc);
+}
+
 __device__ __forceinline__ uint32_t block_scale(float a, float s_enc) {
-  const float u = __fmul_rn(__fdiv_rn(a, 6.0f), s_enc);
-  return e4m3x2_rn_sat(u, 0.0f) & 0xffu;
+  return e4m3x2_rn_sat(block_scale_value(a, s_enc), 0.0f) & 0xffu;
 }
 
 // Value of an E4M3 byte (sign, 4 exponent bits with bias 7, 3 mantissa bits; 0x7F and
@@ -255,7 +277,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) k_nvfp4_amax(
 }
 
 // ---------------------------------------------------------------- scale update
-__global__ void __launch_bounds__(kThreads) k_nvfp4_scales(const __grid_constant__ Nvfp4ScaleParams p) {
+// Each thread loads kScaleItems 16-byte groups of amaxes (grid-strided) before it converts
+// any of them, so that several loads per thread are in flight.
+constexpr int kScaleItems = 4;
+constexpr int kScaleBlocksPerSM = 6;
+
+__global__ void __launch_bounds__(kThreads, kScaleBlocksPerSM) k_nvfp4_scales(
+    const __grid_constant__ Nvfp4ScaleParams p) {
   grid_dependency_sync();
   const float s_enc = tensor_scale(*p.amax_t);
   const Nvfp4ScaleSegment& s = p.seg[blockIdx.y];
@@ -263,13 +291,23 @@ __global__ void __launch_bounds__(kThreads) k_nvfp4_scales(const __grid_constant
   const int64_t stride = int64_t(gridDim.x) * blockDim.x;
   const int64_t tid = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
   if (s.vec) {
-    for (int64_t q = tid; q < n / 4; q += stride) {
-      const uint4 a = ld_stream16(s.amax + 4 * q);
-      const uint32_t out = block_scale(__uint_as_float(a.x), s_enc) |
-                           (block_scale(__uint_as_float(a.y), s_enc) << 8) |
-                           (block_scale(__uint_as_float(a.z), s_enc) << 16) |
-                           (block_scale(__uint_as_float(a.w), s_enc) << 24);
-      reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+    const int64_t nq = n / 4;
+    for (int64_t q0 = tid; q0 < nq; q0 += stride * kScaleItems) {
+      uint4 a[kScaleItems];
+#pragma unroll
+      for (int u = 0; u < kScaleItems; ++u)
+        if (q0 + u * stride < nq) a[u] = ld_stream16(s.amax + 4 * (q0 + u * stride));
+#pragma unroll
+      for (int u = 0; u < kScaleItems; ++u) {
+        const int64_t q = q0 + u * stride;
+        if (q >= nq) break;
+        const uint32_t out =
+            e4m3x2_rn_sat(block_scale_value(__uint_as_float(a[u].x), s_enc),
+                          block_scale_value(__uint_as_float(a[u].y), s_enc)) |
+            (e4m3x2_rn_sat(block_scale_value(__uint_as_float(a[u].z), s_enc),
+                           block_scale_value(__uint_as_float(a[u].w), s_enc)) << 16);
+        reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+      }
     }
   } else {
     for (int64_t e = tid; e < n; e += stride) {
@@ -470,8 +508,9 @@ cudaError_t launch_nvfp4_scales(const Nvfp4ScaleParams& p, const DeviceInfo& dev
     work = items > work ? items : work;
   }
   if (work == 0) return cudaSuccess;
-  const int64_t per_seg = (int64_t(dev.sms) * 8 + p.nseg - 1) / p.nseg;
-  const int64_t want = (work + kThreads - 1) / kThreads;
+  // at most one resident wave over the segments; each thread takes kScaleItems groups
+  const int64_t per_seg = (int64_t(dev.sms) * kScaleBlocksPerSM + p.nseg - 1) / p.nseg;
+  const int64_t want = (work + int64_t(kThreads) * kScaleItems - 1) / (int64_t(kThreads) * kScaleItems);
   const dim3 grid(unsigned(want < per_seg ? want : (per_seg < 1 ? 1 : per_seg)), unsigned(p.nseg));
   return launch_kernel(k_nvfp4_scales, grid, kThreads, 0, stream, p);
 }

@@ -253,3 +253,68 @@ def test_amax_with_odd_fragment_boundaries(dtype):
         torch.cuda.synchronize()
         assert np.array_equal(to_host(ar), war) and np.array_equal(to_host(ac), wac)
         assert to_host(at)[0] == wat[0]
+
+
+def _gpu_scales(a: np.ndarray, g: float) -> np.ndarray:
+    """Rowwise NVFP4 scale update of an FP32 amax grid of 64 columns (a weight of 1024
+    columns), tensor amax g, on the GPU."""
+    rows = a.shape[0]
+    (rr, rc), _ = api.nvfp4_block_shapes(rows, 1024)
+    assert (rr, rc) == a.shape
+    ad = to_device(a).view(a.shape)
+    at = torch.tensor([g], dtype=torch.float32, device="cuda")
+    sr = torch.full((rr, rc), 0xEE, dtype=torch.uint8, device="cuda")
+    api.nvfp4_update_scales(ad, None, at, sr, None, rows, 1024)
+    torch.cuda.synchronize()
+    return to_host(sr)
+
+
+def _oracle_scales(a: np.ndarray, g: float) -> np.ndarray:
+    s = np.full(a.shape, 0xEE, np.uint8)
+    oracle.nvfp4_update_scales(a, a.shape[0], a.shape[1], g, s)
+    return s
+
+
+def _grid64(v: np.ndarray) -> np.ndarray:
+    v = np.asarray(v, np.float32).reshape(-1)
+    pad = (-v.size) % 64
+    return np.concatenate([v, np.zeros(pad, np.float32)]).reshape(-1, 64)
+
+
+@pytest.mark.parametrize("j", [0, 3, -5, 20])
+def test_scale_update_rounds_the_quotient_at_e4m3_ties(j):
+    """fp32(A / 6) decides the E4M3 block scale where A / 6 * S falls on or next to a tie
+    between two E4M3 codes.  With S = 2^j (tensor amax 2688 / 2^j) the product is exact, so
+    amaxes 6 t +- k ulps around every E4M3 code value and midpoint t expose any error of
+    one unit in the quotient's last place."""
+    g = float(np.float32(2688.0) / np.float32(2.0 ** j))
+    codes = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8)).astype(np.float64)
+    points = np.unique(np.concatenate([codes, (codes[:-1] + codes[1:]) / 2]))
+    base = (points * 6.0 / 2.0 ** j).astype(np.float32)
+    base = base[np.isfinite(base) & (base > 0)]
+    k = np.arange(-48, 49, dtype=np.int64)
+    bits = base.view(np.int32).astype(np.int64)[:, None] + k[None, :]
+    bits = bits[(bits > 0) & (bits < 0x7F800000)]
+    a = _grid64(bits.astype(np.int32).view(np.float32))
+    assert np.array_equal(_gpu_scales(a, g), _oracle_scales(a, g))
+
+
+def test_scale_update_every_mantissa_and_edge_values():
+    """Every FP32 mantissa in binades around the quotient's exactness boundary (2^-126 to
+    2^-122), at 1 and near the top of the range, plus zeros, subnormals, infinities, NaNs
+    and negative amaxes, under several tensor amaxes (including 0 and a subnormal)."""
+    m = np.arange(1 << 23, dtype=np.uint32)
+    parts = [((np.uint32(e + 127) << np.uint32(23)) | m).view(np.float32)
+             for e in (-126, -125, -124, -123, -122, 0, 127)]
+    special = np.array([0.0, -0.0, np.inf, -np.inf, np.nan, -1.0, -448.0, 1e-45, 1e-40,
+                        1.1754942e-38, np.finfo(np.float32).max], np.float32)
+    sub = (np.arange(1, 1 << 16, dtype=np.uint32) * np.uint32(127)).view(np.float32)
+    a = _grid64(np.concatenate(parts + [special, sub]))
+    for g in (2688.0, 1.0, 6.0, 3.0e-39, 0.0, 3.0e38):
+        got, want = _gpu_scales(a, g), _oracle_scales(a, g)
+        if not np.array_equal(got, want):
+            bad = np.flatnonzero(got.reshape(-1) != want.reshape(-1))
+            v = a.reshape(-1)[bad[0]]
+            raise AssertionError(f"g={g}: {bad.size} mismatches, first amax {v!r} "
+                                 f"({np.float32(v).view(np.uint32):#x}): gpu {got.reshape(-1)[bad[0]]:#x} "
+                                 f"oracle {want.reshape(-1)[bad[0]]:#x}")
