@@ -88,12 +88,17 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   if constexpr (kCol) store_colmax<T, kCol>(p, row0, j, colmax);
 }
 
-// A fast tile of a launch whose fragments are all aligned (kShift false) or all
-// shifted (kShift true: the fragment's own offset picks the specialisation).
+// A fast tile of a launch whose fragments are all aligned (kShift false) or of a launch
+// that holds realigning fragments (kShift true: each fragment's own offset, 0 included,
+// picks the specialisation, so aligned and realigning fragments share one launch).
 template <class T, bool kCol, bool kShift>
 __device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int64_t col0, int lane) {
   if constexpr (kShift) {
-    with_shift<T>(p.g.shift, [&](auto s) { amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane); });
+    if (p.g.shift == 0) {
+      amax_tile_fast<T, kCol, 0>(p, row0, col0, lane);
+    } else {
+      with_shift<T>(p.g.shift, [&](auto s) { amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane); });
+    }
   } else {
     amax_tile_fast<T, kCol, 0>(p, row0, col0, lane);
   }

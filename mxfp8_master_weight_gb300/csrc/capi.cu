@@ -390,10 +390,16 @@ int run_amax(const mxfp8_amax_job* jobs, int32_t njobs, void* stream) {
   AmaxParams batch[kGroupChunk];
   for (int base = 0; base < njobs; base += kWindow) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
+    // aligned and realigning fragments of one dtype share a launch (the realigning
+    // kernel takes aligned tiles too): one grid tail per dtype instead of two
+    bool any_shift[2] = {false, false};
     for (int i = 0; i < m; ++i) {
       prep_amax(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : dt * 2 + (win[i].g.shift != 0);
+      key[i] = skip ? -1 : dt * 2;
+      if (!skip && win[i].g.shift != 0) any_shift[dt] = true;
     }
+    for (int i = 0; i < m; ++i)
+      if (key[i] >= 0 && any_shift[key[i] >> 1]) key[i] += 1;
     for (int kk = 0; kk < 4; ++kk) {  // dtype x shifted (direction sets may mix)
       int n = 0;
       for (int i = 0; i <= m; ++i) {
@@ -428,11 +434,16 @@ int run_cast(const mxfp8_cast_job* jobs, int32_t njobs, void* stream) {
   CastParams batch[kGroupChunk];
   for (int base = 0; base < njobs; base += kWindow) {
     const int m = njobs - base < kWindow ? njobs - base : kWindow;
+    // as for the amax: aligned and realigning fragments of one model, dtype and output
+    // alignment share a launch
+    bool any_shift[16] = {};
     for (int i = 0; i < m; ++i) {
       prep_cast(jobs[base + i], &win[i], &dt, &col, &skip);
-      key[i] = skip ? -1 : jobs[base + i].model_dtype * 8 + dt * 4 + (win[i].g.shift != 0) * 2 +
-                               (win[i].vec_out != 0);
+      key[i] = skip ? -1 : jobs[base + i].model_dtype * 8 + dt * 4 + (win[i].vec_out != 0);
+      if (!skip && win[i].g.shift != 0) any_shift[key[i]] = true;
     }
+    for (int i = 0; i < m; ++i)
+      if (key[i] >= 0 && any_shift[key[i]]) key[i] += 2;
     for (int kk = 0; kk < 16; ++kk) {  // model x dtype x shifted x aligned output
       int n = 0;
       for (int i = 0; i <= m; ++i) {

@@ -133,10 +133,20 @@ __device__ __forceinline__ void cast_tile_unaligned(const CastParams& p, int64_t
   }
 }
 
-// A fast tile of a launch whose fragments are all aligned or all shifted.
+// A fast tile of a launch whose fragments are all aligned (kShift false) or of a launch
+// that holds realigning fragments (kShift true: each fragment's own offset, 0 included,
+// picks the specialisation).
 template <class T, bool kCol, bool kShift, bool kVec, int kModel>
 __device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int64_t col0, int lane) {
   if constexpr (kShift) {
+    if (p.g.shift == 0) {
+      if constexpr (kVec) {
+        cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane);
+      } else {
+        cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane);
+      }
+      return;
+    }
     with_shift<T>(p.g.shift, [&](auto s) {
       if constexpr (kVec) {
         cast_tile_fast<T, kCol, decltype(s)::value, 0, kModel>(p, row0, col0, lane);

@@ -179,24 +179,21 @@ class PackedLayout:
 
 def _count_launches(amax_jobs, cast_jobs, n_reduce_pieces, specs, fused_reduce=False) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
-    entries launch once per group of at most 16 jobs sharing dtype and alignment class
-    (fragment virtual base on a 16-byte boundary; for the cast also the outputs'
-    virtual base on a V-byte boundary); row-only and bidirectional jobs share launches."""
+    entries launch once per group of at most 16 jobs sharing the input dtype (for the
+    cast also the outputs' virtual base on a V-byte boundary or not); row-only and
+    bidirectional jobs, and aligned and realigning fragments, share launches."""
     def groups(keys, cap):
         counts = {}
         for k in keys:
             counts[k] = counts.get(k, 0) + 1
         return sum((n + cap - 1) // cap for n in counts.values())
 
-    def vbase(t, start):
-        return t.data_ptr() - start * t.element_size()
-
-    akeys = [(a[0].dtype, vbase(a[0], a[5]) % 16 != 0) for a in amax_jobs]
+    akeys = [a[0].dtype for a in amax_jobs]
     ckeys = []
     for frag, sr, sc, qr, qc, rows, cols, start in cast_jobs:
         v = 16 // frag.element_size()
         vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
-        ckeys.append((frag.dtype, vbase(frag, start) % 16 != 0, vec))
+        ckeys.append((frag.dtype, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
     if fused_reduce:  # one launch per 64 pieces of grid entries with one set of slots
         reduce_and_scales = (n_reduce_pieces + 63) // 64
@@ -293,8 +290,8 @@ class ShardedCast:
 
     def launches_per_step(self) -> int:
         """Library kernel launches of one step: the batched amax and cast take one launch
-        per (dtype, alignment class) group of at most 16 fragments (row-only and
-        bidirectional fragments share launches), the reduction one, the batched scale
+        per dtype group of at most 16 fragments (row-only and bidirectional, aligned and
+        realigning fragments share launches), the reduction one, the batched scale
         update (when not fused with the reduction) one per 32 block grids."""
         return self._launches if hasattr(self, "_launches") else -1
 
