@@ -22,6 +22,18 @@ namespace {
 
 constexpr int kThreads = 256;
 
+// E8M0 bytes of four |amax| bit patterns at once, as e8m0_from_bits gives them one by one:
+// the exponent fields gathered as bytes (byte 3 of bits << 1 for F32, byte 1 for BF16),
+// then max(E - 8, 0) by a saturating byte subtract, and 0xFF where E is 0xFF (NaN / Inf).
+template <class T>
+__device__ __forceinline__ uint32_t e8m0x4(const uint32_t (&m)[4]) {
+  constexpr uint32_t kSel = T::kBytes == 4 ? 0x0073u : 0x0051u;
+  const uint32_t lo = __byte_perm(m[0] << 1, m[1] << 1, kSel);
+  const uint32_t hi = __byte_perm(m[2] << 1, m[3] << 1, kSel);
+  const uint32_t e = __byte_perm(lo, hi, 0x5410u);
+  return __vsubus4(e, 0x08080808u) | __vcmpeq4(e, 0xffffffffu);
+}
+
 constexpr int kMaxSegments = 32;
 
 struct ScaleBatch {
@@ -47,10 +59,7 @@ __global__ void __launch_bounds__(kThreads) k_update_scales(const __grid_constan
         const uint2 a = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(s.amax) + 4 * q);
         w[0] = a.x & 0xffffu; w[1] = a.x >> 16; w[2] = a.y & 0xffffu; w[3] = a.y >> 16;
       }
-      uint32_t out = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(w[k]) << (8 * k);
-      reinterpret_cast<uint32_t*>(s.scale)[q] = out;
+      reinterpret_cast<uint32_t*>(s.scale)[q] = e8m0x4<T>(w);
     }
   } else {
     for (int64_t e = tid; e < n; e += stride) {
@@ -95,10 +104,7 @@ __device__ __forceinline__ void store_reduced(const ReduceScaleSegment& s, int64
       *reinterpret_cast<uint2*>(static_cast<uint16_t*>(s.reduced) + e) =
           make_uint2(m[0] | (m[1] << 16), m[2] | (m[3] << 16));
     }
-    uint32_t out = 0;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) out |= e8m0_from_bits<T>(m[k]) << (8 * k);
-    *reinterpret_cast<uint32_t*>(s.scale + e) = out;  // dense: ld_s == ld_a == ncols
+    *reinterpret_cast<uint32_t*>(s.scale + e) = e8m0x4<T>(m);  // dense: ld_s == ld_a == ncols
   } else {
     const int64_t r = e / s.ld_a, c = e % s.ld_a;
     store_bits<T>(s.reduced, e, m[0]);
@@ -134,19 +140,9 @@ __global__ void __launch_bounds__(kThreads, kReduceBlocksPerSM) k_reduce_update_
       live[u] = t < items && (s.vec || e[u] % s.ld_a < s.ncols);  // skip padding columns
       m[u][0] = m[u][1] = m[u][2] = m[u][3] = 0u;
     }
-    uint64_t mask = s.slots;
-    for (int k = 0;; ++k) {  // contributing slots, uniform in the block
-      int slot;
-      if (s.all_slots) {
-        if (k >= s.nslots) break;
-        slot = k;
-      } else {
-        if (mask == 0) break;
-        slot = __ffsll(static_cast<long long>(mask)) - 1;
-        mask &= mask - 1;
-      }
+    // the items of one slot (zeros for items past the run)
+    auto load_slot = [&](int slot, uint32_t (&v)[kItems][4]) {
       const char* base = static_cast<const char*>(s.slot0) + slot * s.slot_stride * T::kBytes;
-      uint32_t v[kItems][4];
 #pragma unroll
       for (int u = 0; u < kItems; ++u) {
         v[u][0] = v[u][1] = v[u][2] = v[u][3] = 0u;
@@ -164,10 +160,34 @@ __global__ void __launch_bounds__(kThreads, kReduceBlocksPerSM) k_reduce_update_
           v[u][0] = load_bits<T>(p, 0);
         }
       }
+    };
+    // contributing slots, uniform in the block: the first one loads straight into m
+    // (a run read by one slot -- every run of a single-rank reduction, most runs of a
+    // ranged one -- then folds nothing), the others fold in
+    uint64_t mask = s.slots;
+    int next = 0;  // all_slots: the next slot
+    auto next_slot = [&]() -> int {
+      if (s.all_slots) return next < s.nslots ? next++ : -1;
+      if (mask == 0) return -1;
+      const int slot = __ffsll(static_cast<long long>(mask)) - 1;
+      mask &= mask - 1;
+      return slot;
+    };
+    int slot = next_slot();
+    if (slot >= 0) {
+      load_slot(slot, m);
 #pragma unroll
       for (int u = 0; u < kItems; ++u)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) m[u][q] = max(m[u][q], v[u][q] & kAbs);
+        for (int q = 0; q < 4; ++q) m[u][q] &= kAbs;
+      while ((slot = next_slot()) >= 0) {
+        uint32_t v[kItems][4];
+        load_slot(slot, v);
+#pragma unroll
+        for (int u = 0; u < kItems; ++u)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) m[u][q] = max(m[u][q], v[u][q] & kAbs);
+      }
     }
 #pragma unroll
     for (int u = 0; u < kItems; ++u) {

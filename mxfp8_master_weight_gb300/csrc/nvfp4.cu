@@ -36,7 +36,16 @@ constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowBatch = 8;
 constexpr int kMaskBatch = 4;
-constexpr int kMinBlocks = 3;
+// Resident blocks per SM the amax and cast kernels are compiled for (3: at most 85
+// registers, 8 rows of 16-byte loads in flight per lane).
+#ifndef MXFP8_NVFP4_AMAX_MIN_BLOCKS
+#define MXFP8_NVFP4_AMAX_MIN_BLOCKS 3
+#endif
+#ifndef MXFP8_NVFP4_CAST_MIN_BLOCKS
+#define MXFP8_NVFP4_CAST_MIN_BLOCKS 3
+#endif
+constexpr int kAmaxMinBlocks = MXFP8_NVFP4_AMAX_MIN_BLOCKS;
+constexpr int kCastMinBlocks = MXFP8_NVFP4_CAST_MIN_BLOCKS;
 
 // Lanes that hold one 1x16 row block.
 template <class T>
@@ -242,7 +251,7 @@ __device__ __forceinline__ uint32_t amax_tile_masked(const Nvfp4AmaxParams& p, i
 }
 
 template <class T, bool kCol, bool kShift>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) k_nvfp4_amax(
+__global__ void __launch_bounds__(kThreads, kAmaxMinBlocks) k_nvfp4_amax(
     const __grid_constant__ JobBatch<Nvfp4AmaxParams, 1> b) {
   __shared__ uint32_t block_max;
   grid_dependency_sync();
@@ -420,7 +429,7 @@ __device__ __forceinline__ void cast_tile_masked(const Nvfp4CastParams& p, const
 }
 
 template <class T, bool kCol, bool kShift>
-__global__ void __launch_bounds__(kThreads, kMinBlocks) k_nvfp4_cast(
+__global__ void __launch_bounds__(kThreads, kCastMinBlocks) k_nvfp4_cast(
     const __grid_constant__ JobBatch<Nvfp4CastParams, 1> b) {
   __shared__ float mult[256];
   grid_dependency_sync();

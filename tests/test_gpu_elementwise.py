@@ -165,3 +165,47 @@ def test_cast_f16_model_dtype(dtype):
     s_r, s_c = _scale_grids(rows, cols, 6)
     gr, gc, wr, wc = _cast_with_scales_model(x, rows, cols, s_r, s_c, "f16")
     assert_bitwise((gr, gc), (wr, wc), f"f16 model {dtype}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("nslots", [1, 3])
+def test_fused_reduce_scales_every_pattern(dtype, nslots):
+    """The reduction fused with the scale update, against the oracle's MAX over the slots
+    and E8M0 of the result: every BF16 bit pattern, or 512K random FP32 patterns plus
+    every exponent field with edge mantissas, spread over 1 or 3 slots (the other slots
+    holding smaller magnitudes or zeros)."""
+    rng = np.random.default_rng(40 + nslots)
+    if dtype == "bf16":
+        pats = np.arange(65536, dtype=np.uint32)
+        width = 16
+    else:
+        edge = (np.arange(256, dtype=np.uint32)[:, None] << 23) | np.array([0, 1, 0x400000, 0x7FFFFF], np.uint32)
+        pats = np.concatenate([rng.integers(0, 2 ** 32, 512 * 1024, dtype=np.uint64).astype(np.uint32),
+                               edge.reshape(-1), edge.reshape(-1) | 0x80000000])
+        width = 32
+    n = pats.size + (-pats.size) % 1024
+    pats = np.concatenate([pats, np.zeros(n - pats.size, np.uint32)])
+    slots = np.zeros((nslots, n), np.uint32)
+    owner = rng.integers(0, nslots, n)
+    slots[owner, np.arange(n)] = pats
+    for k in range(nslots):  # the other slots: the pattern with a lower exponent, or 0
+        other = owner != k
+        lower = np.where((pats >> (width - 9)) & 0xFF > 2, pats - (np.uint32(2) << (width - 9)), 0)
+        slots[k, other] = np.where(rng.random(other.sum()) < 0.5, lower[other], 0)
+    if dtype == "bf16":
+        x = slots.astype(np.uint16)
+    else:
+        x = slots.view(np.float32)
+    d = to_device(x).view(nslots, n)
+    red = torch.empty(n, dtype=d.dtype, device="cuda")
+    cols = 1024 * 32
+    sr = torch.empty((n // 1024, 1024), dtype=torch.uint8, device="cuda")
+    api.mxfp8_amax_max_reduce_update_scales(d, red, [(red.view(n // 1024, 1024), None, sr, None, n // 1024, cols)])
+    torch.cuda.synchronize()
+    want = oracle.max_reduce(x)
+    bits = (lambda a: a.view(np.uint32)) if dtype == "f32" else (lambda a: a)
+    assert np.array_equal(bits(to_host(red)), bits(want))
+    wf = want.astype(np.float32) if dtype == "f32" else wl.bf16_bits_to_f32(want)
+    with np.errstate(invalid="ignore"):
+        ws = oracle.e8m0_from_amax(np.abs(wf.astype(np.float64)))
+    assert np.array_equal(sr.cpu().numpy().reshape(-1), ws.reshape(-1))
