@@ -191,8 +191,10 @@ def _count_launches(amax_jobs, cast_jobs, n_reduce_pieces, specs, fused_reduce=F
     akeys = [a[0].dtype for a in amax_jobs]
     ckeys = []
     for frag, sr, sc, qr, qc, rows, cols, start in cast_jobs:
+        # full-size outputs (output offset = fragment start): the byte of element f is at
+        # out + f, so the outputs' virtual base is their own address
         v = 16 // frag.element_size()
-        vec = all((q.data_ptr() - start) % v == 0 for q in (qr, qc) if q is not None)
+        vec = all(q.data_ptr() % v == 0 for q in (qr, qc) if q is not None)
         ckeys.append((frag.dtype, vec))
     n_grids = sum(2 if s.colwise else 1 for s in specs)
     if fused_reduce:  # one launch per 64 pieces of grid entries with one set of slots

@@ -161,3 +161,35 @@ def test_slot_ranges_cover_each_grid_and_count_runs():
         quads = [e for e in range(lo, hi) if e % 4 == 0 and e + 4 <= hi]
         pieces += 1 if not quads else 1 + (lo < quads[0]) + (quads[-1] + 4 < hi)
     assert driver.reduce_pieces(layout, ranges) == pieces
+
+
+def test_launch_count_groups_by_dtype_and_output_alignment():
+    """Aligned and realigning fragments of one dtype share the amax and cast launches; a
+    cast launch is split only by dtype and by whether the outputs allow word stores
+    (full-size outputs: their own address), at most 16 jobs per launch."""
+    import torch
+    specs = [driver.WeightSpec(64, 64, True), driver.WeightSpec(32, 128, False)]
+    master = torch.zeros(64 * 64 + 32 * 128 + 8)
+    outs = [torch.zeros(64 * 64 + 16, dtype=torch.uint8), torch.zeros(32 * 128 + 16, dtype=torch.uint8)]
+
+    def jobs(frag_shift, out_shift):
+        amax, cast = [], []
+        for w, (spec, start, n) in enumerate(((specs[0], 3, 1000), (specs[1], 0, 512))):
+            frag = master[frag_shift + start:frag_shift + start + n]
+            q = outs[w][out_shift:out_shift + spec.numel]
+            amax.append((frag, None, None, spec.rows, spec.cols, start))
+            cast.append((frag, None, None, q, None, spec.rows, spec.cols, start))
+        return amax, cast
+
+    a0, c0 = jobs(0, 0)
+    a1, c1 = jobs(1, 0)        # other fragment offsets: realigning, same launches
+    a2, c2 = jobs(0, 1)        # outputs one byte off a word boundary
+    base = driver._count_launches(a0, c0, 1, specs, fused_reduce=True)
+    assert base == 1 + 1 + 1   # amax, reduction + scales, cast
+    assert driver._count_launches(a0 + a1, c0 + c1, 1, specs, fused_reduce=True) == 3
+    assert driver._count_launches(a0 + a2, c0 + c2, 1, specs, fused_reduce=True) == 4
+    many_a, many_c = a0 * 9, c0 * 9  # 18 jobs: two launches per phase
+    assert driver._count_launches(many_a, many_c, 1, specs, fused_reduce=True) == 2 + 1 + 2
+    bf = [(f.to(torch.bfloat16),) + j[1:] for f, j in ((j[0], j) for j in a0)]
+    bfc = [(f.to(torch.bfloat16),) + j[1:] for f, j in ((j[0], j) for j in c0)]
+    assert driver._count_launches(a0 + bf, c0 + bfc, 1, specs, fused_reduce=True) == 2 + 1 + 2
