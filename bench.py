@@ -25,8 +25,8 @@ reduction + scales, per-chunk partial cast, copy-out, all inside its timed regio
 the flow its measured copy-engine bound.  Outside the timed
 steps: `fused_whole_blocks` (the one-pass kernel on the same weight), `sharded_batch`
 (the multi-fragment driver on the config-5 batch in four emulated shards, with its
-phases) and `other_configs` (configs 1-3 and the weight row-only, CUDA graphs of
-repeated calls, median of 7 rounds).  `--impl reference` times the CPU oracle on a
+phases) and `other_configs` (configs 1-3, and the headline weight bidirectional and row-only,
+each kernel alone in CUDA graphs of repeated calls, median of 7 rounds: the pages' method).  `--impl reference` times the CPU oracle on a
 bounded sample of the same workload (the reference arm of this benchmark).
 N > 1 (torchrun): every rank runs its own replica of the workload on its GPU.
 """
@@ -362,9 +362,10 @@ def graph_us_per_call(call, stream, elems: int, rounds: int = 7, replays: int = 
 
 
 def measure_configs(x_headline, dev) -> dict:
-    """amax and cast µs per call on the other workloads (configs 1-3 and the headline weight
-    row-only), the pages' timing method: graphs of repeated calls, 7 rounds, median.
-    Configs 1-3 fit in L2 (126 MB), so their figures are L2-warm, not HBM measurements."""
+    """amax and cast µs per call, each kernel alone, on configs 1-3 and on the headline weight
+    (bidirectional and row-only), the pages' timing method: graphs of repeated calls, 7
+    rounds, median.  Configs 1-3 fit in L2 (126 MB), so their figures are L2-warm, not HBM
+    measurements; the headline weight's are HBM figures, with GB/s and peak fraction."""
     import torch
 
     from mxfp8_master_weight_gb300 import api
@@ -378,8 +379,10 @@ def measure_configs(x_headline, dev) -> dict:
         ("cfg2 1024x1024 BF16 [17, +262144) row-only", w2, 17, w2.numel // 4, False, "L2-warm"),
         ("cfg3 4096x4096 FP32 full bidirectional", w3, 0, w3.numel, True, "L2-warm"),
         ("cfg3 4096x4096 FP32 [17, +n/4) bidirectional", w3, 17, w3.numel // 4, True, "L2-warm"),
+        ("cfg4 16384x6144 FP32 full bidirectional", None, 0, ROWS * COLS, True, "HBM"),
         ("cfg4 16384x6144 FP32 full row-only", None, 0, ROWS * COLS, False, "HBM"),
     ]
+    peak, peak_kind = measured_peak()
     out = {}
     for name, w, start, length, colwise, mem in cases:
         if w is None:
@@ -402,8 +405,15 @@ def measure_configs(x_headline, dev) -> dict:
         amax.call(stream)
         api.mxfp8_update_scales(ar, ac, sr, scl, rows, cols)
         cast = api.prepare_partial_cast(frag, sr, scl, qr, qc, rows, cols, start)
-        out[name] = {"amax_us": round(graph_us_per_call(amax, stream, length), 3),
-                     "cast_us": round(graph_us_per_call(cast, stream, length), 3), "memory": mem}
+        rec = {"amax_us": round(graph_us_per_call(amax, stream, length), 3),
+               "cast_us": round(graph_us_per_call(cast, stream, length), 3), "memory": mem}
+        if mem == "HBM":  # larger than L2: HBM figures against the measured peak
+            ab = algorithmic_bytes(length, frag.element_size(), colwise)
+            for k in ("amax", "cast"):
+                gbs = ab[k] / (rec[k + "_us"] * 1e-6) / 1e9
+                rec[k + "_gbs"] = round(gbs, 1)
+                rec[k + "_frac_of_" + peak_kind + "_peak"] = round(gbs / peak, 4)
+        out[name] = rec
     return out
 
 
@@ -877,7 +887,9 @@ def run_ours(args):
         "nvfp4": nvfp4,
         "other_configs": {
             "method": "CUDA graph of 50 calls (fragments <= 4M elements) else 10, 20 replays per "
-                      "round, 7 rounds, median us per call; outputs checked bitwise in the tests",
+                      "round, 7 rounds, median us per call (the pages' method: their GB200 figures "
+                      "for the headline weight bidirectional are in pages_gb200_us_per_call); "
+                      "outputs checked bitwise in the tests",
             "cases": configs},
         "gpu_launches": sc.launches_per_step() * args.steps,
         "clocks": dict(clocks.summary(), window=f"{load_steps} load steps around the timed region "
