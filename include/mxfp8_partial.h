@@ -177,7 +177,7 @@ MXFP8_API int mxfp8_partial_cast(const mxfp8_tensor* input, const mxfp8_tensor* 
  * the same arguments means; the jobs are validated first (a failure launches nothing
  * and names the job), then run as few kernels as possible: jobs that share the input
  * dtype, the model dtype and (cast) whether the outputs allow word stores go into one
- * launch (at most 16 jobs each; row-only and bidirectional jobs, and fragments whose
+ * launch (at most 64 jobs each; row-only and bidirectional jobs, and fragments whose
  * virtual base is or is not 16-byte aligned, together, each tile taking its job's
  * specialisation), with the tiles of all jobs scheduled together.  Jobs may run concurrently:
  * jobs whose written entries overlap (two fragments of one weight writing the SAME

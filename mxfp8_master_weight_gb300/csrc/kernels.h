@@ -163,8 +163,10 @@ enum Dirs { kRowOnly = 0, kBidir = 1, kMixed = 2 };
 // A batch of fragments launched as one kernel: the warp tiles of every job's first
 // and last 32-row bands (the only bands a fragment boundary can cut) come first,
 // numbered by prefix_a, then every job's interior bands, numbered by prefix_b.
-// The table travels in kernel parameter space (no device allocation).
-constexpr int kMaxBatchJobs = 16;
+// The table travels in kernel parameter space (no device allocation): 64 jobs take 10-15 KB
+// of the 32 KB parameter space kernels have since CUDA 12.1, so a batch of many small
+// weights is a few launches, not one per 16 fragments.
+constexpr int kMaxBatchJobs = 64;
 
 template <class P, int N>
 struct JobBatch {

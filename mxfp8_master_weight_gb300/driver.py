@@ -33,6 +33,10 @@ _PHASE_NAMES = ("mxfp8.partial_amax", "mxfp8.max_reduce", "mxfp8.update_scales",
 
 _ALIGN = 16
 
+# fragments the library's batched entry points put into one launch (their job table
+# travels in kernel parameter space)
+_BATCH_JOBS = 64
+
 
 @dataclass(frozen=True)
 class WeightSpec:
@@ -179,7 +183,7 @@ class PackedLayout:
 
 def _count_launches(amax_jobs, cast_jobs, n_reduce_pieces, specs, fused_reduce=False) -> int:
     """Kernel launches the library issues for one step of these jobs: the batched
-    entries launch once per group of at most 16 jobs sharing the input dtype (for the
+    entries launch once per group of at most 64 jobs sharing the input dtype (for the
     cast also the outputs' virtual base on a V-byte boundary or not); row-only and
     bidirectional jobs, and aligned and realigning fragments, share launches."""
     def groups(keys, cap):
@@ -201,7 +205,7 @@ def _count_launches(amax_jobs, cast_jobs, n_reduce_pieces, specs, fused_reduce=F
         reduce_and_scales = (n_reduce_pieces + 63) // 64
     else:             # the reduction, then one scale launch per 32 grids
         reduce_and_scales = 1 + (n_grids + 31) // 32
-    return groups(akeys, 16) + reduce_and_scales + groups(ckeys, 16)
+    return groups(akeys, _BATCH_JOBS) + reduce_and_scales + groups(ckeys, _BATCH_JOBS)
 
 
 def reduce_runs(layout: PackedLayout, ranges):
@@ -292,7 +296,7 @@ class ShardedCast:
 
     def launches_per_step(self) -> int:
         """Library kernel launches of one step: the batched amax and cast take one launch
-        per dtype group of at most 16 fragments (row-only and bidirectional, aligned and
+        per dtype group of at most 64 fragments (row-only and bidirectional, aligned and
         realigning fragments share launches), the reduction one, the batched scale
         update (when not fused with the reduction) one per 32 block grids."""
         return self._launches if hasattr(self, "_launches") else -1
@@ -372,3 +376,25 @@ class ShardedCast:
                     torch.cuda.nvtx.range_pop()
                 if events is not None:
                     events[k + 1].record(torch_stream)
+
+    def capture(self, shards) -> torch.cuda.CUDAGraph:
+        """One step for these shard buffers, captured into a CUDA graph.
+
+        ``g.replay()`` then issues the step's launches (the same library calls as
+        ``step(shards)``, with their programmatic launch dependencies) from the host in one
+        go: for a batch of small weights, whose kernels last a few microseconds, the host's
+        per-launch cost otherwise sets the step time.  The graph holds buffer addresses: it
+        is valid while ``shards`` and this object's buffers live, and a replay reads what
+        the shard buffers hold at that moment.  The step runs once, uncaptured, first.
+        """
+        dev = self.slots.device
+        with torch.cuda.device(dev):
+            self._prepared(shards)  # the library calls are marshalled outside the capture
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            self.step(shards, stream=side)
+            torch.cuda.current_stream(dev).wait_stream(side)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                self.step(shards, stream=side)
+        return graph

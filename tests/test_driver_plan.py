@@ -166,7 +166,7 @@ def test_slot_ranges_cover_each_grid_and_count_runs():
 def test_launch_count_groups_by_dtype_and_output_alignment():
     """Aligned and realigning fragments of one dtype share the amax and cast launches; a
     cast launch is split only by dtype and by whether the outputs allow word stores
-    (full-size outputs: their own address), at most 16 jobs per launch."""
+    (full-size outputs: their own address), at most 64 jobs per launch."""
     import torch
     specs = [driver.WeightSpec(64, 64, True), driver.WeightSpec(32, 128, False)]
     master = torch.zeros(64 * 64 + 32 * 128 + 8)
@@ -188,7 +188,7 @@ def test_launch_count_groups_by_dtype_and_output_alignment():
     assert base == 1 + 1 + 1   # amax, reduction + scales, cast
     assert driver._count_launches(a0 + a1, c0 + c1, 1, specs, fused_reduce=True) == 3
     assert driver._count_launches(a0 + a2, c0 + c2, 1, specs, fused_reduce=True) == 4
-    many_a, many_c = a0 * 9, c0 * 9  # 18 jobs: two launches per phase
+    many_a, many_c = a0 * 33, c0 * 33  # 66 jobs: two launches per phase (64 per launch)
     assert driver._count_launches(many_a, many_c, 1, specs, fused_reduce=True) == 2 + 1 + 2
     bf = [(f.to(torch.bfloat16),) + j[1:] for f, j in ((j[0], j) for j in a0)]
     bfc = [(f.to(torch.bfloat16),) + j[1:] for f, j in ((j[0], j) for j in c0)]

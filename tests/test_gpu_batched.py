@@ -34,13 +34,16 @@ def _fragments(rows, cols, n_cuts, rng):
     return list(zip([0] + cuts, cuts + [n]))
 
 
-def test_batched_amax_scales_cast_match_oracle():
-    rng = np.random.default_rng(32)
+@pytest.mark.parametrize("n_cuts", [3, 40])
+def test_batched_amax_scales_cast_match_oracle(n_cuts):
+    """4 weights cut into n_cuts + 1 fragments each: 16 jobs per call, or 164 (more than one
+    64-job launch and more than one 64-job host window per call)."""
+    rng = np.random.default_rng(32 + n_cuts)
     amax_jobs, cast_jobs, checks = [], [], []
     keep = []
     for w, (rows, cols, x, col) in enumerate(_weights()):
         (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
-        frags = _fragments(rows, cols, 3, rng)
+        frags = _fragments(rows, cols, n_cuts, rng)
         dt = torch.float32 if x.dtype == np.float32 else torch.bfloat16
         slots_r = torch.zeros((len(frags), rr, rc), dtype=dt, device="cuda")
         slots_c = torch.zeros((len(frags), cr, cc), dtype=dt, device="cuda") if col else None

@@ -206,3 +206,31 @@ def test_ranged_entry_matches_whole_slot_reduction(dtype, padded):
     with pytest.raises(Exception):
         api.mxfp8_amax_max_reduce_update_scales_ranged(slots, reduced, [(vr, vc, sr, scl, rows, cols)],
                                                        [(S, 0, 4)])  # no such slot
+
+
+@pytest.mark.parametrize("ranged", [True, False])
+def test_captured_step_replays_on_new_master_values(ranged):
+    """A step captured into a CUDA graph, replayed after the shard buffers were refilled in
+    place, gives the oracle's casts of the new values (and every replay the same bytes)."""
+    batch = wl.cfg5_sharded_batch(seed=3, scale=16)
+    specs = [driver.WeightSpec(w.rows, w.cols, w.colwise) for w in batch.weights]
+    sc = driver.ShardedCast(specs, batch.bounds, "cuda", ranged=ranged)
+    shards = [torch.from_numpy(np.ascontiguousarray(batch.shard(s))).cuda() for s in range(sc.num_shards)]
+    graph = sc.capture(shards)
+    torch.cuda.synchronize()
+    _check_against_full(batch, sc)
+    rng = np.random.default_rng(123)
+    flat2 = wl.normal_f32(rng, batch.total) * np.float32(0.5)
+    weights2 = [wl.Weight(w.rows, w.cols, w.dtype, flat2[o:o + w.numel], w.colwise)
+                for w, o in zip(batch.weights, batch.offsets)]
+    batch2 = wl.ShardedBatch(weights2, batch.offsets, batch.bounds, flat2)
+    for s in range(sc.num_shards):
+        shards[s].copy_(torch.from_numpy(np.ascontiguousarray(batch2.shard(s))))
+    graph.replay()
+    torch.cuda.synchronize()
+    _check_against_full(batch2, sc)
+    first = [q[0].clone() for q in sc.outputs]
+    graph.replay()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, q[0]) for a, q in zip(first, sc.outputs))
