@@ -60,10 +60,12 @@ __device__ __forceinline__ void store_colmax(const AmaxParams& p, int64_t row0, 
 }
 
 // Whole tile inside the fragment: 16-byte loads (realigned when the fragment's
-// virtual base sits kS bytes past a 16-byte boundary), no per-element tests.
+// virtual base sits kS bytes past a 16-byte boundary), no per-element tests.  Rows
+// r_lo .. r_hi-1 of the tile (all 32, or a quarter of them when four warps share the
+// tile); the column maxima are stored, or left in *colpart for the warps to combine.
 template <class T, bool kCol, int kS>
 __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0, int64_t col0,
-                                               int lane) {
+                                               int lane, int r_lo, int r_hi, uint4* colpart) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
@@ -76,7 +78,7 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   constexpr int NB = kRowBatch;
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += NB) {
+  for (int rb = r_lo; rb < r_hi; rb += NB) {
     uint4 v[NB];
     load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
@@ -85,22 +87,31 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
       if (writer) store_bits<T>(p.amax_r, out_r + (rb + r) * p.ld_r, canonical_nan<T>(m));
     }
   }
-  if constexpr (kCol) store_colmax<T, kCol>(p, row0, j, colmax);
+  if constexpr (kCol) {
+    if (colpart != nullptr) {
+      *colpart = colmax;
+    } else {
+      store_colmax<T, kCol>(p, row0, j, colmax);
+    }
+  }
 }
 
 // A fast tile of a launch whose fragments are all aligned (kShift false) or of a launch
 // that holds realigning fragments (kShift true: each fragment's own offset, 0 included,
 // picks the specialisation, so aligned and realigning fragments share one launch).
 template <class T, bool kCol, bool kShift>
-__device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int64_t col0, int lane) {
+__device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int64_t col0, int lane,
+                                          int r_lo = 0, int r_hi = 32, uint4* colpart = nullptr) {
   if constexpr (kShift) {
     if (p.g.shift == 0) {
-      amax_tile_fast<T, kCol, 0>(p, row0, col0, lane);
+      amax_tile_fast<T, kCol, 0>(p, row0, col0, lane, r_lo, r_hi, colpart);
     } else {
-      with_shift<T>(p.g.shift, [&](auto s) { amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane); });
+      with_shift<T>(p.g.shift, [&](auto s) {
+        amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane, r_lo, r_hi, colpart);
+      });
     }
   } else {
-    amax_tile_fast<T, kCol, 0>(p, row0, col0, lane);
+    amax_tile_fast<T, kCol, 0>(p, row0, col0, lane, r_lo, r_hi, colpart);
   }
 }
 
@@ -109,20 +120,36 @@ __device__ __forceinline__ void amax_fast(const AmaxParams& p, int64_t row0, int
 // written.  Inlined into the kernel, so the fragment geometry is read straight from
 // the kernel's parameters (behind a call, every store through an output pointer made
 // the compiler reload it, which doubled the time of small, all-masked fragments).
-template <class T, bool kCol>
+// Column maxima of a cut tile: only the columns whose 32x1 block meets the fragment.
+template <class T>
+__device__ __forceinline__ void store_colmax_masked(const AmaxParams& p, int64_t row0, int64_t j,
+                                                    const uint4& colmax) {
+  const FragGeom& g = p.g;
+  const int64_t r_end = min(row0 + 32, g.rows);
+#pragma unroll
+  for (int k = 0; k < T::V; ++k) {
+    const int64_t col = j + k;
+    if (col < g.cols && column_meets(g, col, row0, r_end))
+      store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, canonical_nan<T>(chunk_get<T>(colmax, k)));
+  }
+}
+
+// MB: rows per batch of predicated loads (a split tile's warp takes its 8 rows at once).
+template <class T, bool kCol, int MB = kMaskBatch>
 __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t row0, int64_t col0,
-                                              int lane) {
+                                              int lane, int r_lo = 0, int r_hi = 32,
+                                              uint4* colpart = nullptr) {
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
   const bool writer = (lane % T::G) == 0;
   const int64_t b0 = j & ~int64_t(31);  // first column of this lane's row block
   uint4 colmax = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += kMaskBatch) {  // warp-uniform: the butterfly stays converged
-    uint4 v[kMaskBatch];
-    load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+  for (int rb = r_lo; rb < r_hi; rb += MB) {  // warp-uniform: the butterfly stays converged
+    uint4 v[MB];
+    load_rows_masked<T, MB>(v, g, p.in, row0 + rb, j);
 #pragma unroll
-    for (int r = 0; r < kMaskBatch; ++r) {
+    for (int r = 0; r < MB; ++r) {
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);
       const int64_t i = row0 + rb + r;
       if (writer && i < g.rows && b0 < g.cols && row_span_meets(g, i, b0, min(b0 + 31, g.cols - 1)))
@@ -130,40 +157,81 @@ __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t ro
     }
   }
   if constexpr (kCol) {
-    const int64_t r_end = min(row0 + 32, g.rows);
-#pragma unroll
-    for (int k = 0; k < T::V; ++k) {
-      const int64_t col = j + k;
-      if (col < g.cols && column_meets(g, col, row0, r_end))
-        store_bits<T>(p.amax_c, (row0 >> 5) * p.ld_c + col, canonical_nan<T>(chunk_get<T>(colmax, k)));
+    if (colpart != nullptr) {
+      *colpart = colmax;
+    } else {
+      store_colmax_masked<T>(p, row0, j, colmax);
     }
   }
 }
 
-template <class T, int kDirs, bool kShift, int N>
+// kSplit: four warps share each tile, a quarter of its rows each (a block's eight warps
+// take two tiles), and combine the tile's column maxima in shared memory; for launches
+// with few tiles, whose time is one warp's chain of row batches rather than HBM traffic.
+template <class T, int kDirs, bool kShift, int N, bool kSplit>
 __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlocks) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
-  const int64_t stride = int64_t(gridDim.x) * kWarps;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
-    int64_t row0, col0;
-    const AmaxParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
-    const int kind = classify_tile<T>(p.g, row0, col0, TW);
-    const bool col = kDirs == kMixed ? p.amax_c != nullptr : kDirs == kBidir;
-    if (kind == kTileFast) {
-      if (col) {
-        if constexpr (kDirs != kRowOnly) amax_fast<T, true, kShift>(p, row0, col0, lane);
-      } else {
-        if constexpr (kDirs != kBidir) amax_fast<T, false, kShift>(p, row0, col0, lane);
+  if constexpr (!kSplit) {
+    const int64_t stride = int64_t(gridDim.x) * kWarps;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < total; t += stride) {
+      int64_t row0, col0;
+      const AmaxParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
+      const int kind = classify_tile<T>(p.g, row0, col0, TW);
+      const bool col = kDirs == kMixed ? p.amax_c != nullptr : kDirs == kBidir;
+      if (kind == kTileFast) {
+        if (col) {
+          if constexpr (kDirs != kRowOnly) amax_fast<T, true, kShift>(p, row0, col0, lane);
+        } else {
+          if constexpr (kDirs != kBidir) amax_fast<T, false, kShift>(p, row0, col0, lane);
+        }
+      } else if (kind == kTileMasked) {
+        if (col) {
+          if constexpr (kDirs != kRowOnly) amax_tile_masked<T, true>(p, row0, col0, lane);
+        } else {
+          if constexpr (kDirs != kBidir) amax_tile_masked<T, false>(p, row0, col0, lane);
+        }
       }
-    } else if (kind == kTileMasked) {
-      if (col) {
-        if constexpr (kDirs != kRowOnly) amax_tile_masked<T, true>(p, row0, col0, lane);
-      } else {
-        if constexpr (kDirs != kBidir) amax_tile_masked<T, false>(p, row0, col0, lane);
+    }
+  } else {
+    static_assert(kDirs != kMixed, "the split kernel serves single-direction-set launches");
+    __shared__ uint4 part[kWarps][32];
+    const int q = warp & 3;  // quarter: rows 8q .. 8q+7
+    // block-uniform rounds (every warp reaches every barrier); warp w of a round takes
+    // quarter w % 4 of tile (round * 8 + w) / 4
+    for (int64_t base = int64_t(blockIdx.x) * kWarps; base < total * 4; base += int64_t(gridDim.x) * kWarps) {
+      const int64_t t = (base + warp) >> 2;
+      int kind = kTileSkip;
+      int64_t row0 = 0, col0 = 0;
+      const AmaxParams* pp = nullptr;
+      if (t < total) {
+        pp = &b.job[batch_tile(b, t, TW, row0, col0)];
+        kind = classify_tile<T>(pp->g, row0, col0, TW);
+        uint4* cp = kDirs == kBidir ? &part[warp][lane] : nullptr;
+        if (kind == kTileFast) {
+          amax_fast<T, kDirs == kBidir, kShift>(*pp, row0, col0, lane, 8 * q, 8 * q + 8, cp);
+        } else if (kind == kTileMasked) {
+          amax_tile_masked<T, kDirs == kBidir, 8>(*pp, row0, col0, lane, 8 * q, 8 * q + 8, cp);
+        }
+      }
+      if constexpr (kDirs == kBidir) {
+        __syncthreads();
+        if (q == 0 && kind != kTileSkip) {
+          uint4 cm = part[warp][lane];
+#pragma unroll
+          for (int w = 1; w < 4; ++w) cm = chunk_max<T>(cm, part[warp + w][lane]);
+          const int64_t j = col0 + lane * T::V;
+          if (kind == kTileFast) {
+            store_colmax<T, true>(*pp, row0, j, cm);
+          } else {
+            store_colmax_masked<T>(*pp, row0, j, cm);
+          }
+        }
+        __syncthreads();
       }
     }
   }
@@ -171,12 +239,17 @@ __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlock
 
 template <class T, int kDirs, bool kShift, int N>
 cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  (void)dev;
   JobBatch<AmaxParams, N> b;
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
+  if constexpr (N == 1 && !kShift && kDirs != kMixed) {
+    if (total <= split_max_tiles(dev, MXFP8_AMAX_SPLIT_TILES_PER_SM)) {  // few tiles: four warps per tile
+      const unsigned grid = tile_grid(total * 4, kWarps);
+      return launch_kernel(k_partial_amax<T, kDirs, kShift, N, true>, grid, kThreads, 0, stream, b);
+    }
+  }
   const unsigned grid = tile_grid(total, kWarps);
-  return launch_kernel(k_partial_amax<T, kDirs, kShift, N>, grid, kThreads, 0, stream, b);
+  return launch_kernel(k_partial_amax<T, kDirs, kShift, N, false>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

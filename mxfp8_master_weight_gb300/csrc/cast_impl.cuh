@@ -71,7 +71,7 @@ __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t
 // stores; > 0: aligned pieces; < 0: bytes, the two outputs differ).
 template <class T, bool kCol, int kS, int kM, int kModel>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
-                                               int lane) {
+                                               int lane, int r_lo, int r_hi) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
@@ -85,7 +85,7 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
   float mc[T::V];
   if constexpr (kCol) colwise_multipliers<T>(p, row0, j, mc);
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += NB) {
+  for (int rb = r_lo; rb < r_hi; rb += NB) {
     uint4 v[NB];
     uint32_t sb[NB];
 #pragma unroll
@@ -114,22 +114,24 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
 // bytes.
 template <class T, bool kCol, int kS, int kModel>
 __device__ __forceinline__ void cast_tile_unaligned(const CastParams& p, int64_t row0, int64_t col0,
-                                                    int lane) {
+                                                    int lane, int r_lo, int r_hi) {
   constexpr uint32_t V = T::V;
   const uint32_t mr = static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.out_r) + uintptr_t(p.out_shift)) & (V - 1);
   const uint32_t mc =
       kCol ? static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p.out_c) + uintptr_t(p.out_shift)) & (V - 1) : mr;
   if (mr != mc || mr == 0) {
-    cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane);
+    cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane, r_lo, r_hi);
   } else if constexpr (kS != 0) {
     constexpr int M = (kS / T::kBytes) % int(V);
     if (M != 0 && mr == uint32_t(M)) {
-      cast_tile_fast<T, kCol, kS, M, kModel>(p, row0, col0, lane);
+      cast_tile_fast<T, kCol, kS, M, kModel>(p, row0, col0, lane, r_lo, r_hi);
     } else {
-      cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane);
+      cast_tile_fast<T, kCol, kS, -1, kModel>(p, row0, col0, lane, r_lo, r_hi);
     }
   } else {
-    with_out_offset<T>(mr, [&](auto m) { cast_tile_fast<T, kCol, 0, decltype(m)::value, kModel>(p, row0, col0, lane); });
+    with_out_offset<T>(mr, [&](auto m) {
+      cast_tile_fast<T, kCol, 0, decltype(m)::value, kModel>(p, row0, col0, lane, r_lo, r_hi);
+    });
   }
 }
 
@@ -137,28 +139,29 @@ __device__ __forceinline__ void cast_tile_unaligned(const CastParams& p, int64_t
 // that holds realigning fragments (kShift true: each fragment's own offset, 0 included,
 // picks the specialisation).
 template <class T, bool kCol, bool kShift, bool kVec, int kModel>
-__device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int64_t col0, int lane) {
+__device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int64_t col0, int lane,
+                                          int r_lo = 0, int r_hi = 32) {
   if constexpr (kShift) {
     if (p.g.shift == 0) {
       if constexpr (kVec) {
-        cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane);
+        cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane, r_lo, r_hi);
       } else {
-        cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane);
+        cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane, r_lo, r_hi);
       }
       return;
     }
     with_shift<T>(p.g.shift, [&](auto s) {
       if constexpr (kVec) {
-        cast_tile_fast<T, kCol, decltype(s)::value, 0, kModel>(p, row0, col0, lane);
+        cast_tile_fast<T, kCol, decltype(s)::value, 0, kModel>(p, row0, col0, lane, r_lo, r_hi);
       } else {
-        cast_tile_unaligned<T, kCol, decltype(s)::value, kModel>(p, row0, col0, lane);
+        cast_tile_unaligned<T, kCol, decltype(s)::value, kModel>(p, row0, col0, lane, r_lo, r_hi);
       }
     });
   } else {
     if constexpr (kVec) {
-      cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane);
+      cast_tile_fast<T, kCol, 0, 0, kModel>(p, row0, col0, lane, r_lo, r_hi);
     } else {
-      cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane);
+      cast_tile_unaligned<T, kCol, 0, kModel>(p, row0, col0, lane, r_lo, r_hi);
     }
   }
 }
@@ -168,9 +171,10 @@ __device__ __forceinline__ void cast_fast(const CastParams& p, int64_t row0, int
 // loads otherwise), one scale byte per row and block, and stores only the
 // fragment's elements (a word per whole chunk when the output is aligned).  Inlined
 // into the kernel, as in the amax kernel.
-template <class T, bool kCol, bool kVec, int kModel>
+// MB: rows per batch of predicated loads.
+template <class T, bool kCol, bool kVec, int kModel, int MB = kMaskBatch>
 __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t row0, int64_t col0,
-                                              int lane) {
+                                              int lane, int r_lo = 0, int r_hi = 32) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
@@ -184,18 +188,18 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
       mc[k] = j + k < g.cols ? scale_multiplier(p.s_c[(row0 >> 5) * p.ld_sc + j + k]) : 0.0f;
   }
 #pragma unroll 1
-  for (int rb = 0; rb < 32 && row0 + rb < g.rows; rb += kMaskBatch) {
-    uint4 v[kMaskBatch];
-    const uint64_t valid = load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+  for (int rb = r_lo; rb < r_hi && row0 + rb < g.rows; rb += MB) {
+    uint4 v[MB];
+    const uint64_t valid = load_rows_masked<T, MB>(v, g, p.in, row0 + rb, j);
     if (valid == 0) continue;
-    float mrow[kMaskBatch];
+    float mrow[MB];
 #pragma unroll
-    for (int r = 0; r < kMaskBatch; ++r) {
+    for (int r = 0; r < MB; ++r) {
       const int64_t i = row0 + rb + r;
       mrow[r] = ((valid >> (r * T::V)) & kChunkBits) ? scale_multiplier(p.s_r[i * p.ld_sr + blk]) : 0.0f;
     }
 #pragma unroll
-    for (int r = 0; r < kMaskBatch; ++r) {
+    for (int r = 0; r < MB; ++r) {
       const uint64_t bits = (valid >> (r * T::V)) & kChunkBits;
       if (bits == 0) continue;
       const int64_t i = row0 + rb + r;
@@ -222,30 +226,35 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
   }
 }
 
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
+// kSplit: four warps per tile, a quarter of its rows each (the cast needs no exchange
+// between them), for single-fragment launches with few tiles.
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N, bool kSplit>
 __global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec, kShift>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
   constexpr int TW = tile_width<T>();
+  constexpr int kParts = kSplit ? 4 : 1;
   const int lane = threadIdx.x & 31;
-  const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
+  const int64_t total = (b.prefix_a[b.njobs] + b.prefix_b[b.njobs]) * kParts;
   const int64_t stride = int64_t(gridDim.x) * kWarps;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
+  for (int64_t u = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < total; u += stride) {
+    const int64_t t = kSplit ? u >> 2 : u;
+    const int r_lo = kSplit ? 8 * int(u & 3) : 0, r_hi = kSplit ? r_lo + 8 : 32;
     int64_t row0, col0;
     const CastParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
     if (kind == kTileFast) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) cast_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kRowOnly) cast_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, r_lo, r_hi);
       } else {
-        if constexpr (kDirs != kBidir) cast_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kBidir) cast_fast<T, false, kShift, kVec, kModel>(p, row0, col0, lane, r_lo, r_hi);
       }
     } else if (kind == kTileMasked) {
       if (col) {
-        if constexpr (kDirs != kRowOnly) cast_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kRowOnly) cast_tile_masked<T, true, kVec, kModel>(p, row0, col0, lane, r_lo, r_hi);
       } else {
-        if constexpr (kDirs != kBidir) cast_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane);
+        if constexpr (kDirs != kBidir) cast_tile_masked<T, false, kVec, kModel>(p, row0, col0, lane, r_lo, r_hi);
       }
     }
   }
@@ -253,12 +262,17 @@ __global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec, kShift>()) k_
 
 template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N>
 cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStream_t stream) {
-  (void)dev;
   JobBatch<CastParams, N> b;
   const int64_t total = fill_batch(b, jobs, n);
   if (total == 0) return cudaSuccess;
+  if constexpr (N == 1 && !kShift && kDirs != kMixed) {
+    if (total <= split_max_tiles(dev, MXFP8_CAST_SPLIT_TILES_PER_SM)) {  // few tiles: four warps per tile
+      return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, true>,
+                           tile_grid(total * 4, kWarps), kThreads, 0, stream, b);
+    }
+  }
   const unsigned grid = tile_grid(total, kWarps);
-  return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N>, grid, kThreads, 0, stream, b);
+  return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, false>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

@@ -678,6 +678,21 @@ inline unsigned balanced_grid(int64_t ntiles, int warps, int64_t max_blocks) {
   return unsigned(blocks < max_blocks ? blocks : max_blocks);
 }
 
+// Single-fragment launches of at most this many warp tiles per SM split every tile over
+// four warps, a quarter of its rows each: with so few tiles a whole-tile grid leaves the
+// SMs short of warps, and a launch lasts one warp's chain of row batches (8 dependent
+// round trips on a cut tile) rather than its HBM traffic.  The cast, whose warps share
+// nothing, gains up to more tiles than the amax, whose quarters meet at a barrier.
+#ifndef MXFP8_AMAX_SPLIT_TILES_PER_SM
+#define MXFP8_AMAX_SPLIT_TILES_PER_SM 16
+#endif
+#ifndef MXFP8_CAST_SPLIT_TILES_PER_SM
+#define MXFP8_CAST_SPLIT_TILES_PER_SM 32
+#endif
+inline int64_t split_max_tiles(const DeviceInfo& dev, int tiles_per_sm) {
+  return int64_t(dev.sms) * tiles_per_sm;
+}
+
 // Blocks for one tile per warp: the hardware block scheduler then hands out tiles
 // dynamically, which absorbs uneven per-tile cost (tiles cut by a fragment boundary,
 // row-only next to bidirectional jobs in one batch) better than a static persistent
