@@ -19,7 +19,8 @@ with its GB/s and fraction of the measured HBM peak, both from that median;
 for the current kernel code under profiles/).  `clocks` comes from nvidia-smi samples
 over at least a second of continuous load around the timed region.  `e2e` runs the
 same four-step flow on pinned host buffers (copy-in, per-chunk partial amax, MAX
-reduction + scales, per-chunk partial cast, copy-out, all inside its timed region);
+reduction + scales, per-chunk partial cast storing into the pinned outputs, all inside its
+timed region; its staged-copy form beside it);
 `e2e_one_pass` the one-pass kernel reading and writing the pinned host buffers directly
 (its staged-copy pipeline beside it), over its own bytes; both give per-step spreads and
 the flow its measured copy-engine bound.  Outside the timed
@@ -763,12 +764,16 @@ def run_ours(args):
 
     link = copy_engine_rates(host, x, host_q[0], out_r, stream)
     bound_s = copy_bound_s(h2d, d2h, link)
-    flow = HostPartialFlow(ROWS, COLS, True, device=dev, chunk_rows=args.e2e_chunk_rows)
+    flow = HostPartialFlow(ROWS, COLS, True, device=dev, chunk_rows=args.e2e_chunk_rows, direct_out=True)
     flow_t, flow_per = time_host_path(lambda: flow.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
     flow_t, flow_bytes = aggregate_over_ranks(flow_t, step_bytes * e2e_steps, world, dev)
     flow_launches = flow.launches_per_run()
     flow_chunks = len(flow.chunks)
     del flow
+    sflow = HostPartialFlow(ROWS, COLS, True, device=dev, chunk_rows=args.e2e_chunk_rows, direct_out=False)
+    sflow_t, sflow_per = time_host_path(lambda: sflow.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
+    sflow_t, sflow_bytes = aggregate_over_ranks(sflow_t, step_bytes * e2e_steps, world, dev)
+    del sflow
     zc = ZeroCopyQuantizer(ROWS, COLS, True, device=dev)
     zc_t, zc_per = time_host_path(lambda: zc.run(host, host_q[0], host_q[1], host_s[0], host_s[1]))
     zc_t, zc_bytes = aggregate_over_ranks(zc_t, fused_bytes * e2e_steps, world, dev)
@@ -859,13 +864,23 @@ def run_ours(args):
                 "ms_per_step": round(flow_t / e2e_steps * 1e3, 4), "steps": e2e_steps,
                 "ms_per_step_spread": spread(flow_per),
                 "algorithmic_bytes_per_step": step_bytes,
-                "path": f"HostPartialFlow: partial amax per chunk as it lands ({flow_chunks} chunks of "
-                        f"{args.e2e_chunk_rows} rows), MAX reduction + scales, partial cast per "
-                        "chunk, copies out; 3 streams, device input double-buffered",
+                "path": f"HostPartialFlow: input copied in by chunks ({flow_chunks} of "
+                        f"{args.e2e_chunk_rows} rows), partial amax per chunk as it lands, MAX "
+                        "reduction + scales, partial cast per chunk storing straight into the "
+                        "pinned host outputs, scale grids copied out; device input double-buffered",
                 "gpu_launches_per_step": flow_launches,
-                "copy_gbs": round((h2d + d2h) * e2e_steps / flow_t / 1e9, 1),
+                "link_gbs": round((h2d + d2h) * e2e_steps / flow_t / 1e9, 1),
                 "copy_engines": dict(link, bound_ms=round(bound_s * 1e3, 4),
-                                     frac_of_bound=round(bound_s * e2e_steps / flow_t, 4))},
+                                     note="the least time the step's bytes need through the copy "
+                                          "engines alone; the flow's output stores bypass them"),
+                "staged_copies": {
+                    "path": "the same flow with the casts into device staging buffers and the "
+                            "E4M3 bytes copied out by the copy engine",
+                    "value": round(sflow_bytes / sflow_t / 1e9, 1),
+                    "ms_per_step": round(sflow_t / e2e_steps * 1e3, 4),
+                    "ms_per_step_spread": spread(sflow_per),
+                    "copy_gbs": round((h2d + d2h) * e2e_steps / sflow_t / 1e9, 1),
+                    "frac_of_copy_bound": round(bound_s * e2e_steps / sflow_t, 4)}},
         "e2e_one_pass": {"value": round(zc_bytes / zc_t / 1e9, 1), "unit": "GB/s",
                          "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                          "ms_per_step": round(zc_t / e2e_steps * 1e3, 4), "steps": e2e_steps,

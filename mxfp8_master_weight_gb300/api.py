@@ -437,12 +437,15 @@ def prepare_update_scales(amax_rowwise, amax_colwise, scale_inv_rowwise, scale_i
 
 
 def prepare_partial_cast(input, scale_inv_rowwise, scale_inv_colwise, output_rowwise,
-                         output_colwise, rows, cols, start_offset, out_offset=None) -> Prepared:
+                         output_colwise, rows, cols, start_offset, out_offset=None,
+                         allow_host=False) -> Prepared:
+    """``allow_host``: the outputs may be page-locked host memory the device can access
+    (the kernel's stores then cross the CPU-GPU link)."""
     if out_offset is None:
         out_offset = start_offset
     ts = (input, scale_inv_rowwise, scale_inv_colwise, output_rowwise, output_colwise)
-    hs = [handle(t, n) for t, n in zip(ts, ("input", "scale_inv_rowwise", "scale_inv_colwise",
-                                            "output_rowwise", "output_colwise"))]
+    names = ("input", "scale_inv_rowwise", "scale_inv_colwise", "output_rowwise", "output_colwise")
+    hs = [handle(t, n, allow_host and n.startswith("output")) for t, n in zip(ts, names)]
     return Prepared("mxfp8_partial_cast", hs, (rows, cols, start_offset, out_offset),
                     [t for t in ts if t is not None])
 

@@ -143,17 +143,23 @@ class HostPartialFlow:
     the weight: chunk k's block maxima are taken as soon as its copy has landed (while
     chunk k+1 is still being copied in), every chunk writing its own blocks of the one
     amax slot; after the last chunk the slot is reduced and the scales are derived; then
-    chunk k is cast into a staging buffer while chunk k-1's E4M3 bytes are copied out.
+    every chunk is cast straight into the pinned host outputs over the CPU-GPU link
+    (``direct_out``, the default), or -- ``direct_out=False`` -- chunk k is cast into a
+    staging buffer while chunk k-1's E4M3 bytes are copied out by the copy engine.
     The device input is double-buffered across calls, so one call's copy-in overlaps the
     previous call's copy-out.  All arithmetic runs in the library's kernels; this class
     only orders copies and launches on three streams.
     """
 
     def __init__(self, rows: int, cols: int, colwise: bool = True, dtype=torch.float32,
-                 device="cuda", chunk_rows: int = 4096, depth: int = 3):
+                 device="cuda", chunk_rows: int = 4096, depth: int = 3, direct_out: bool = True):
         if rows <= 0 or cols <= 0:
             raise ValueError("rows and cols must be positive")
         self.rows, self.cols, self.colwise, self.dtype = rows, cols, colwise, dtype
+        # direct_out: each chunk's cast stores its E4M3 bytes straight into the pinned host
+        # outputs over the CPU-GPU link (no staging buffers, no copy engine on the way out)
+        self.direct_out = direct_out
+        self._direct = None
         self.device = torch.device(device)
         self.chunk_rows = max(32, min((chunk_rows + 31) // 32 * 32, (rows + 31) // 32 * 32))
         self.depth = max(1, depth)
@@ -227,6 +233,9 @@ class HostPartialFlow:
         b = self._calls % 2
         self._calls += 1
         caller = torch.cuda.current_stream(self.device)
+        if self.direct_out:
+            self._run_direct(x, qr, qc, host_sr, host_sc, b, caller)
+            return
         # The copy-in reads host memory only: it does not wait for the caller's stream
         # (which, after a previous call, waits for that call's copies out), so one call's
         # copy-in overlaps the previous call's copy-out.  Kernels and copies out follow
@@ -265,6 +274,50 @@ class HostPartialFlow:
                     qc[r0 * cols:r1 * cols].copy_(self.dev_qc[s][:n], non_blocking=True)
                 self.d2h_done[s].record(self.d2h)
         with torch.cuda.stream(self.comp):
+            self.x_free[b].record(self.comp)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_stream(self.comp)
+            host_sr.copy_(self.scale_r, non_blocking=True)
+            if host_sc is not None:
+                host_sc.copy_(self.scale_c, non_blocking=True)
+            self.scales_out.record(self.d2h)
+        caller.wait_stream(self.d2h)
+
+    def _direct_casts(self, qr, qc):
+        """The casts of both device input buffers into these host outputs, marshalled once
+        per pair of output buffers."""
+        key = (qr.data_ptr(), None if qc is None else qc.data_ptr())
+        if self._direct is None or self._direct[0] != key:
+            rows, cols = self.rows, self.cols
+            calls = [[api.prepare_partial_cast(self.dev_x[b][r0 * cols:r1 * cols], self.scale_r,
+                                               self.scale_c, qr, qc, rows, cols, r0 * cols,
+                                               allow_host=True)
+                      for r0, r1 in self.chunks] for b in range(2)]
+            self._direct = (key, calls)
+        return self._direct[1]
+
+    def _run_direct(self, x, qr, qc, host_sr, host_sc, b, caller):
+        """run() with direct_out: copy-in and amax as in run(); every chunk's cast writes
+        the host outputs itself; only the scale grids go out through a copy."""
+        cols = self.cols
+        casts = self._direct_casts(qr, qc)
+        self.comp.wait_stream(caller)
+        self.d2h.wait_stream(caller)
+        dx = self.dev_x[b]
+        raw_comp = api._stream(self.comp, None)
+        with torch.cuda.stream(self.h2d):
+            self.h2d.wait_event(self.x_free[b])
+            for k, (r0, r1) in enumerate(self.chunks):
+                dx[r0 * cols:r1 * cols].copy_(x[r0 * cols:r1 * cols], non_blocking=True)
+                self.in_ready[k].record(self.h2d)
+        with torch.cuda.stream(self.comp):
+            for k in range(len(self.chunks)):
+                self.comp.wait_event(self.in_ready[k])
+                self._amax[b][k].call(raw_comp)
+            self.comp.wait_event(self.scales_out)
+            self._reduce.call(raw_comp)
+            for c in casts[b]:
+                c.call(raw_comp)
             self.x_free[b].record(self.comp)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_stream(self.comp)

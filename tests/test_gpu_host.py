@@ -38,15 +38,20 @@ def test_host_pipeline_matches_oracle(rows, cols, chunk_rows, depth, colwise):
     assert_bitwise(got[2:], want[2:], f"host pipeline {rows}x{cols} chunk {chunk_rows}")
 
 
+@pytest.mark.parametrize("direct_out", [False, True])
 @pytest.mark.parametrize("rows,cols,chunk_rows,depth,colwise,dtype", [
     (1000, 512, 64, 2, True, "f32"), (333, 96, 32, 3, False, "f32"), (64, 4096, 1024, 3, True, "f32"),
     (257, 1000, 96, 1, True, "f32"), (400, 640, 128, 3, True, "bf16")])
-def test_host_partial_flow_matches_oracle(rows, cols, chunk_rows, depth, colwise, dtype):
+def test_host_partial_flow_matches_oracle(rows, cols, chunk_rows, depth, colwise, dtype, direct_out):
     """Three calls in a row (the device input alternates between two buffers, the amax
-    slot, staging buffers and scales are reused), each with new values."""
+    slot, staging buffers and scales are reused), each with new values; with direct_out
+    the casts store into the pinned host outputs themselves (new output buffers on the
+    second call, the same ones again on the third)."""
     (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
-    flow = HostPartialFlow(rows, cols, colwise, dtype=tdt, chunk_rows=chunk_rows, depth=depth)
+    flow = HostPartialFlow(rows, cols, colwise, dtype=tdt, chunk_rows=chunk_rows, depth=depth,
+                           direct_out=direct_out)
+    keep = None
     for call in range(3):
         rng = np.random.default_rng(rows + cols + call)
         x = wl.normal_f32(rng, rows * cols) * np.float32(10.0) ** rng.uniform(-3, 3, rows * cols).astype(np.float32)
@@ -55,8 +60,15 @@ def test_host_partial_flow_matches_oracle(rows, cols, chunk_rows, depth, colwise
             hx = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
         else:
             hx = torch.from_numpy(x).pin_memory()
-        qr = torch.full((rows * cols,), 0xA5, dtype=torch.uint8).pin_memory()
-        qc = torch.full((rows * cols,), 0xA5, dtype=torch.uint8).pin_memory() if colwise else None
+        if call == 2 and keep is not None:
+            qr, qc = keep
+            qr.fill_(0xA5)
+            if qc is not None:
+                qc.fill_(0xA5)
+        else:
+            qr = torch.full((rows * cols,), 0xA5, dtype=torch.uint8).pin_memory()
+            qc = torch.full((rows * cols,), 0xA5, dtype=torch.uint8).pin_memory() if colwise else None
+        keep = (qr, qc)
         sr = torch.empty((rr, rc), dtype=torch.uint8).pin_memory()
         sc = torch.empty((cr, cc), dtype=torch.uint8).pin_memory() if colwise else None
         flow.run(hx, qr, qc, sr, sc)
