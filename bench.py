@@ -52,6 +52,15 @@ METRIC = "MXFP8 partial amax+cast µs/call and HBM GB/s (% of GB300 roofline), 1
 WORKLOAD = ("16384x6144 FP32 master (per-row scale 10^U(-4,1) x N(0,0.02), seed 0), full fragment, "
             "bidirectional MXFP8 E4M3 / E8M0 32-value blocks, model dtype BF16")
 PAGES_GB200_US = {"amax": 110.395, "cast": 210.154}  # context only: other hardware
+# The pages' whole table ("Support row-only MXFP8 distributed master-weight casts", section
+# "Bidirectional kernel performance": GB200, full input, both directions, median µs per
+# call over graph replays): (rows, cols, input dtype) -> (amax µs, cast µs).  Context only.
+PAGES_GB200_TABLE = {
+    (160, 96, "bf16"): (3.278, 7.578), (1024, 1024, "bf16"): (3.690, 7.894),
+    (4096, 4096, "bf16"): (20.099, 24.784), (16384, 6144, "bf16"): (113.376, 202.658),
+    (160, 96, "f32"): (2.953, 7.378), (1024, 1024, "f32"): (3.362, 7.870),
+    (4096, 4096, "f32"): (19.556, 35.254), (16384, 6144, "f32"): (110.395, 210.154),
+}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -418,6 +427,44 @@ def measure_configs(x_headline, dev) -> dict:
     return out
 
 
+def measure_pages_table(dev) -> dict:
+    """Every case of the pages' kernel table on this GPU, by the pages' method (each kernel
+    alone, full input, both directions, graph replays, median of 7 rounds): amax and cast
+    µs per call beside the pages' GB200 figures.  Inputs: N(0, 0.02) draws (seed 0) of the
+    shape, rounded to BF16 for the BF16 rows."""
+    import torch
+
+    from mxfp8_master_weight_gb300 import api
+    from mxfp8_master_weight_gb300 import workloads as wl
+
+    stream = torch.cuda.current_stream(dev)
+    out = {}
+    for (rows, cols, dt), (p_amax, p_cast) in PAGES_GB200_TABLE.items():
+        n = rows * cols
+        x = torch.from_numpy(wl.normal_f32(np.random.default_rng(0), n)).to(dev)
+        if dt == "bf16":
+            x = x.to(torch.bfloat16)
+        (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+        ar = torch.zeros((rr, rc), dtype=x.dtype, device=dev)
+        ac = torch.zeros((cr, cc), dtype=x.dtype, device=dev)
+        sr = torch.empty((rr, rc), dtype=torch.uint8, device=dev)
+        scl = torch.empty((cr, cc), dtype=torch.uint8, device=dev)
+        qr = torch.empty(n, dtype=torch.uint8, device=dev)
+        qc = torch.empty(n, dtype=torch.uint8, device=dev)
+        amax = api.prepare_partial_amax(x, ar, ac, rows, cols, 0)
+        amax.call(stream)
+        api.mxfp8_update_scales(ar, ac, sr, scl, rows, cols)
+        cast = api.prepare_partial_cast(x, sr, scl, qr, qc, rows, cols, 0)
+        a_us = graph_us_per_call(amax, stream, n)
+        c_us = graph_us_per_call(cast, stream, n)
+        out[f"{rows}x{cols} {dt.upper()}"] = {
+            "amax_us": round(a_us, 3), "cast_us": round(c_us, 3),
+            "pages_gb200_amax_us": p_amax, "pages_gb200_cast_us": p_cast,
+            "pages_over_ours_amax": round(p_amax / a_us, 2), "pages_over_ours_cast": round(p_cast / c_us, 2)}
+        del x, ar, ac, sr, scl, qr, qc, amax, cast
+    return out
+
+
 def sample_phases(step, n: int, nphases: int = 3):
     """Per-phase device time of `n` steps, each bracketed by CUDA events on the launching
     stream (events around every phase; recorded only in this sampling region, so the
@@ -727,6 +774,7 @@ def run_ours(args):
                         "gbs": round(b_phase_bytes[nm] / (med * 1e-6) / 1e9, 1)}
     del bshards, bsc, batch
     configs = measure_configs(x, dev)
+    pages_table = measure_pages_table(dev)
     peak, peak_kind = measured_peak()
     nvfp4 = measure_nvfp4(x, dev, peak, "frac_of_" + peak_kind + "_peak")
 
@@ -906,6 +954,11 @@ def run_ours(args):
                       "for the headline weight bidirectional are in pages_gb200_us_per_call); "
                       "outputs checked bitwise in the tests",
             "cases": configs},
+        "pages_table": {
+            "method": "each kernel alone, full input, both directions, CUDA graph of 50 calls "
+                      "(<= 4M elements) else 10, 20 replays per round, 7 rounds, median; the pages' "
+                      "figures are GB200 (context only: other hardware)",
+            "cases": pages_table},
         "gpu_launches": sc.launches_per_step() * args.steps,
         "clocks": dict(clocks.summary(), window=f"{load_steps} load steps around the timed region "
                                                f"and {KERNEL_SAMPLES} sampled steps"),

@@ -63,14 +63,18 @@ __device__ __forceinline__ void store_colmax(const AmaxParams& p, int64_t row0, 
 // virtual base sits kS bytes past a 16-byte boundary), no per-element tests.  Rows
 // r_lo .. r_hi-1 of the tile (all 32, or a quarter of them when four warps share the
 // tile); the column maxima are stored, or left in *colpart for the warps to combine.
-template <class T, bool kCol, int kS>
+// kEdge: a tile cut by the matrix's right edge (kTileEdge): the lanes past it load
+// nothing (their chunks read as zeros) and store nothing.
+template <class T, bool kCol, int kS, bool kEdge = false>
 __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0, int64_t col0,
                                                int lane, int r_lo, int r_hi, uint4* colpart) {
+  static_assert(!kEdge || kS == 0, "edge tiles are aligned");
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
   const int64_t row_bytes = cols * T::kBytes;
-  const bool writer = (lane % T::G) == 0;
+  const bool active = !kEdge || j < cols;
+  const bool writer = (lane % T::G) == 0 && active;
   const int64_t out_r = row0 * p.ld_r + (j >> 5);
   // the realigning path batches 8 rows too: lane r loads the words after row r of the
   // tile (one load for the batch) and lane 31 takes them by shuffle
@@ -80,7 +84,13 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
 #pragma unroll 1
   for (int rb = r_lo; rb < r_hi; rb += NB) {
     uint4 v[NB];
-    load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
+    if constexpr (kEdge) {
+#pragma unroll
+      for (int r = 0; r < NB; ++r)
+        v[r] = active ? ld_stream16(src + (rb + r) * row_bytes) : make_uint4(0u, 0u, 0u, 0u);
+    } else {
+      load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
+    }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       const uint32_t m = fold_row<T, kCol>(v[r], colmax);
@@ -90,7 +100,7 @@ __device__ __forceinline__ void amax_tile_fast(const AmaxParams& p, int64_t row0
   if constexpr (kCol) {
     if (colpart != nullptr) {
       *colpart = colmax;
-    } else {
+    } else if (active) {
       store_colmax<T, kCol>(p, row0, j, colmax);
     }
   }
@@ -168,7 +178,10 @@ __device__ __forceinline__ void amax_tile_masked(const AmaxParams& p, int64_t ro
 // kSplit: four warps share each tile, a quarter of its rows each (a block's eight warps
 // take two tiles), and combine the tile's column maxima in shared memory; for launches
 // with few tiles, whose time is one warp's chain of row batches rather than HBM traffic.
-template <class T, int kDirs, bool kShift, int N, bool kSplit>
+// kSplit 2 also takes tiles cut by the matrix's right edge on the fast path (instantiated
+// only for weights whose width is not a multiple of the tile's: the extra path costs
+// registers).
+template <class T, int kDirs, bool kShift, int N, int kSplit>
 __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlocks) k_partial_amax(
     const __grid_constant__ JobBatch<AmaxParams, N> b) {
   grid_dependency_sync();
@@ -176,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlock
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int64_t total = b.prefix_a[b.njobs] + b.prefix_b[b.njobs];
-  if constexpr (!kSplit) {
+  if constexpr (kSplit == 0) {
     const int64_t stride = int64_t(gridDim.x) * kWarps;
     for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < total; t += stride) {
       int64_t row0, col0;
@@ -210,10 +223,14 @@ __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlock
       const AmaxParams* pp = nullptr;
       if (t < total) {
         pp = &b.job[batch_tile(b, t, TW, row0, col0)];
-        kind = classify_tile<T>(pp->g, row0, col0, TW);
+        kind = kSplit == 2 ? classify_tile_edge<T>(pp->g, row0, col0, TW)
+                           : classify_tile<T>(pp->g, row0, col0, TW);
         uint4* cp = kDirs == kBidir ? &part[warp][lane] : nullptr;
         if (kind == kTileFast) {
           amax_fast<T, kDirs == kBidir, kShift>(*pp, row0, col0, lane, 8 * q, 8 * q + 8, cp);
+        } else if (kind == kTileEdge) {
+          if constexpr (kSplit == 2)
+            amax_tile_fast<T, kDirs == kBidir, 0, true>(*pp, row0, col0, lane, 8 * q, 8 * q + 8, cp);
         } else if (kind == kTileMasked) {
           amax_tile_masked<T, kDirs == kBidir, 8>(*pp, row0, col0, lane, 8 * q, 8 * q + 8, cp);
         }
@@ -225,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, kShift ? kShiftMinBlocks : kMinBlock
 #pragma unroll
           for (int w = 1; w < 4; ++w) cm = chunk_max<T>(cm, part[warp + w][lane]);
           const int64_t j = col0 + lane * T::V;
-          if (kind == kTileFast) {
+          if (kind == kTileFast || (kind == kTileEdge && j < pp->g.cols)) {
             store_colmax<T, true>(*pp, row0, j, cm);
-          } else {
+          } else if (kind == kTileMasked) {
             store_colmax_masked<T>(*pp, row0, j, cm);
           }
         }
@@ -245,11 +262,13 @@ cudaError_t launch_n(const AmaxParams* jobs, int n, const DeviceInfo& dev, cudaS
   if constexpr (N == 1 && !kShift && kDirs != kMixed) {
     if (total <= split_max_tiles(dev, MXFP8_AMAX_SPLIT_TILES_PER_SM)) {  // few tiles: four warps per tile
       const unsigned grid = tile_grid(total * 4, kWarps);
-      return launch_kernel(k_partial_amax<T, kDirs, kShift, N, true>, grid, kThreads, 0, stream, b);
+      if (jobs[0].g.cols % tile_width<T>() != 0)
+        return launch_kernel(k_partial_amax<T, kDirs, kShift, N, 2>, grid, kThreads, 0, stream, b);
+      return launch_kernel(k_partial_amax<T, kDirs, kShift, N, 1>, grid, kThreads, 0, stream, b);
     }
   }
   const unsigned grid = tile_grid(total, kWarps);
-  return launch_kernel(k_partial_amax<T, kDirs, kShift, N, false>, grid, kThreads, 0, stream, b);
+  return launch_kernel(k_partial_amax<T, kDirs, kShift, N, 0>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

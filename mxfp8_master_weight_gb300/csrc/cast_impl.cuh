@@ -69,11 +69,15 @@ __device__ __forceinline__ void colwise_multipliers(const CastParams& p, int64_t
 // base), one scale byte per row, word stores when the outputs are aligned.
 // kM: byte offset of the outputs' virtual bases past a V-byte boundary (0: word
 // stores; > 0: aligned pieces; < 0: bytes, the two outputs differ).
-template <class T, bool kCol, int kS, int kM, int kModel>
+// kEdge: a tile cut by the matrix's right edge (kTileEdge, word-aligned outputs): the lanes
+// past it read no input, scale or multiplier and store nothing.
+template <class T, bool kCol, int kS, int kM, int kModel, bool kEdge = false>
 __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0, int64_t col0,
                                                int lane, int r_lo, int r_hi) {
+  static_assert(!kEdge || (kS == 0 && kM == 0), "edge tiles are aligned, with word stores");
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
+  const bool active = !kEdge || j < cols;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
   const int64_t row_bytes = cols * T::kBytes;
   const uint8_t* srow = p.s_r + row0 * p.ld_sr + (j >> 5);
@@ -83,14 +87,29 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
   constexpr bool kRowLanes = kS != 0 && T::kBytes == 4;
   constexpr int NB = kS ? (kRowLanes ? kRowBatch : kShiftBatch) : kRowBatch;
   float mc[T::V];
-  if constexpr (kCol) colwise_multipliers<T>(p, row0, j, mc);
+  if constexpr (kCol) {
+    if (active) {
+      colwise_multipliers<T>(p, row0, j, mc);
+    } else {
+#pragma unroll
+      for (int k = 0; k < T::V; ++k) mc[k] = 0.0f;
+    }
+  }
 #pragma unroll 1
   for (int rb = r_lo; rb < r_hi; rb += NB) {
     uint4 v[NB];
     uint32_t sb[NB];
+    if constexpr (kEdge) {
 #pragma unroll
-    for (int r = 0; r < NB; ++r) sb[r] = srow[(rb + r) * p.ld_sr];
-    load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
+      for (int r = 0; r < NB; ++r) {
+        sb[r] = active ? srow[(rb + r) * p.ld_sr] : 0u;
+        v[r] = active ? ld_stream16(src + (rb + r) * row_bytes) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < NB; ++r) sb[r] = srow[(rb + r) * p.ld_sr];
+      load_rows<NB, kS, false, kRowLanes>(v, src + rb * row_bytes, row_bytes, lane);
+    }
 #pragma unroll
     for (int r = 0; r < NB; ++r) {
       float mr[T::V];
@@ -100,8 +119,10 @@ __device__ __forceinline__ void cast_tile_fast(const CastParams& p, int64_t row0
       uint2 qr, qc;
       cast_chunk<T, kModel, kCol>(v[r], mr, mc, qr, qc);
       const int64_t o = o0 + (rb + r) * cols;
-      store_chunk_at<T, kM>(p.out_r + o, qr);
-      if constexpr (kCol) store_chunk_at<T, kM>(p.out_c + o, qc);
+      if (active) {
+        store_chunk_at<T, kM>(p.out_r + o, qr);
+        if constexpr (kCol) store_chunk_at<T, kM>(p.out_c + o, qc);
+      }
     }
   }
 }
@@ -227,8 +248,10 @@ __device__ __forceinline__ void cast_tile_masked(const CastParams& p, int64_t ro
 }
 
 // kSplit: four warps per tile, a quarter of its rows each (the cast needs no exchange
-// between them), for single-fragment launches with few tiles.
-template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N, bool kSplit>
+// between them), for single-fragment launches with few tiles; kSplit 2 also takes tiles cut
+// by the matrix's right edge on the fast path (instantiated only for weights whose width is
+// not a multiple of the tile's: the extra path costs registers).
+template <class T, int kDirs, bool kShift, bool kVec, int kModel, int N, int kSplit>
 __global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec, kShift>()) k_partial_cast(
     const __grid_constant__ JobBatch<CastParams, N> b) {
   grid_dependency_sync();
@@ -242,8 +265,19 @@ __global__ void __launch_bounds__(kThreads, min_blocks<T, N, kVec, kShift>()) k_
     const int r_lo = kSplit ? 8 * int(u & 3) : 0, r_hi = kSplit ? r_lo + 8 : 32;
     int64_t row0, col0;
     const CastParams& p = b.job[batch_tile(b, t, TW, row0, col0)];
-    const int kind = classify_tile<T>(p.g, row0, col0, TW);
+    const int kind = kSplit == 2 && kVec ? classify_tile_edge<T>(p.g, row0, col0, TW)
+                                         : classify_tile<T>(p.g, row0, col0, TW);
     const bool col = kDirs == kMixed ? p.out_c != nullptr : kDirs == kBidir;
+    if constexpr (kSplit == 2 && kVec) {
+      if (kind == kTileEdge) {
+        if (col) {
+          if constexpr (kDirs != kRowOnly) cast_tile_fast<T, true, 0, 0, kModel, true>(p, row0, col0, lane, r_lo, r_hi);
+        } else {
+          if constexpr (kDirs != kBidir) cast_tile_fast<T, false, 0, 0, kModel, true>(p, row0, col0, lane, r_lo, r_hi);
+        }
+        continue;
+      }
+    }
     if (kind == kTileFast) {
       if (col) {
         if constexpr (kDirs != kRowOnly) cast_fast<T, true, kShift, kVec, kModel>(p, row0, col0, lane, r_lo, r_hi);
@@ -267,12 +301,14 @@ cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaS
   if (total == 0) return cudaSuccess;
   if constexpr (N == 1 && !kShift && kDirs != kMixed) {
     if (total <= split_max_tiles(dev, MXFP8_CAST_SPLIT_TILES_PER_SM)) {  // few tiles: four warps per tile
-      return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, true>,
-                           tile_grid(total * 4, kWarps), kThreads, 0, stream, b);
+      const unsigned grid = tile_grid(total * 4, kWarps);
+      if (jobs[0].g.cols % tile_width<T>() != 0)
+        return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 2>, grid, kThreads, 0, stream, b);
+      return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 1>, grid, kThreads, 0, stream, b);
     }
   }
   const unsigned grid = tile_grid(total, kWarps);
-  return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, false>, grid, kThreads, 0, stream, b);
+  return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 0>, grid, kThreads, 0, stream, b);
 }
 
 // One launch per batch of at most kMaxBatchJobs jobs, with the kernel for the batch's

@@ -478,6 +478,22 @@ __device__ __forceinline__ int classify_tile(const FragGeom& g, int64_t row0, in
   return kTileMasked;
 }
 
+// The split kernels' extra class: a tile cut only by the matrix's right edge, whose 32 rows
+// lie inside the matrix and whose every element inside the matrix belongs to the fragment
+// (aligned virtual base, cols a multiple of V).  It takes the fast path with the lanes past
+// the edge idle, instead of the masked path's per-row membership tests.
+constexpr int kTileEdge = 3;
+template <class T>
+__device__ __forceinline__ int classify_tile_edge(const FragGeom& g, int64_t row0, int64_t col0,
+                                                  int tw) {
+  const int kind = classify_tile<T>(g, row0, col0, tw);
+  if (kind != kTileMasked || !g.fast_ok || g.shift != 0 || row0 + 32 > g.rows || col0 + tw <= g.cols)
+    return kind;
+  const int64_t first = row0 * g.cols + col0;            // the tile's first element
+  const int64_t last = (row0 + 31) * g.cols + g.cols - 1;  // its last element inside the matrix
+  return (first >= g.start && last < g.end) ? kTileEdge : kind;
+}
+
 // ---------------------------------------------------------------- row loads
 template <bool kHint>
 __device__ __forceinline__ uint4 ld_chunk(const void* p, uint64_t pol) {

@@ -280,3 +280,24 @@ def test_every_fragment_misalignment(dtype, colwise):
         got = gpu_fragment(frag, rows, cols, start, colwise, shift=k)
         want = oracle_fragment(frag, rows, cols, start, colwise)
         assert_bitwise(got, want, f"{dtype} misalignment {k}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(160, 96), (64, 100), (96, 132), (64, 200), (32, 8), (96, 1064)])
+def test_tiles_cut_by_the_right_edge(dtype, rows, cols):
+    """Weights narrower than, or not a multiple of, a tile's width: tiles whose rows the
+    fragment covers whole take the fast path with the lanes past the right edge idle
+    (whole weights, whole bands, and fragments that cut a band), bidirectional and
+    row-only, against the oracle."""
+    rng = np.random.default_rng(rows * 31 + cols)
+    n = rows * cols
+    x = wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-3, 3, n).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    cases = [(0, n), (min(32, rows - 1) * cols, max(1, min(32, rows // 2)) * cols), (cols + 4, n - cols - 4)]
+    for start, length in cases:
+        for colwise in (True, False):
+            frag = np.ascontiguousarray(x[start:start + length])
+            got = gpu_fragment(frag, rows, cols, start, colwise, amax_fill=0.125)
+            want = oracle_fragment(frag, rows, cols, start, colwise, amax_fill=0.125)
+            assert_bitwise(got, want, f"{dtype} {rows}x{cols} [{start},{start + length}) colwise={colwise}")
