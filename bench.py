@@ -478,6 +478,37 @@ def sample_phases(step, n: int, nphases: int = 3):
     return [[e[a].elapsed_time(e[b]) * 1e3 for e in evs] for a, b in bounds]
 
 
+def marginal_costs(phases, stream, n: int = 200, rounds: int = 3) -> dict:
+    """What each phase adds to a step of back-to-back steps: the µs per step of the whole
+    step minus that of the step without the phase (the library calls of the other phases,
+    in order, n times; median of `rounds` rounds each).  A short kernel bracketed by events
+    also pays its launch and loses its programmatic overlap with the kernel before; this
+    figure does not."""
+    import torch
+
+    def loop(keep):
+        calls = [c for k, cs in enumerate(phases) if k in keep for c in cs]
+        for _ in range(5):
+            for c in calls:
+                c.call(stream)
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(n):
+                for c in calls:
+                    c.call(stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            per.append(a.elapsed_time(b) * 1e3 / n)
+        return statistics.median(per)
+
+    present = [k for k, cs in enumerate(phases) if cs]
+    full = loop(set(present))
+    return {k: full - loop(set(present) - {k}) for k in present}, full
+
+
 def run_for(step, seconds: float, stream) -> int:
     """Run steps back to back for about `seconds` of device time (the clock sampler's
     load window); returns the number of steps run."""
@@ -710,6 +741,8 @@ def run_ours(args):
         barrier(world)
         # per-kernel durations: a fixed number of in-step samples, events around each phase
         per_kernel = dict(zip(names, sample_phases(step, KERNEL_SAMPLES)))
+        # phases of the driver's step: amax, reduction (+ fused scales), scales (empty), cast
+        marg, marg_full = marginal_costs(sc._prepared([x]), stream)
         load_steps += run_for(step, args.clock_window_s / 2, stream)
     elapsed = start.elapsed_time(stop) / 1e3
     t_max, total_bytes = aggregate_over_ranks(elapsed, step_bytes * args.steps, world, dev)
@@ -845,6 +878,10 @@ def run_ours(args):
                        "us_per_call_mean": round(st["mean"], 3), "samples": st["n"],
                        "algorithmic_bytes": abytes[nm], "gbs": round(gbs, 1),
                        frac_key: round(gbs / peak, 4)}
+    for nm, k in zip(names, (0, 1, 3)):  # the driver's phase index of each kernel
+        mu = marg[k]
+        kernels[nm]["marginal_us_in_step"] = round(mu, 3)
+        kernels[nm]["marginal_gbs"] = round(abytes[nm] / (mu * 1e-6) / 1e9, 1)
     dom = "cast"
     achieved = kernels[dom]["gbs"]
 
@@ -880,7 +917,11 @@ def run_ours(args):
         "kernels": kernels,
         "kernel_timing": f"median of {KERNEL_SAMPLES} in-step samples per kernel: CUDA events on "
                          "the launching stream around each phase of every step of a sampling "
-                         "region that follows the timed steps (the timed steps carry no events)",
+                         "region that follows the timed steps (the timed steps carry no events); "
+                         "marginal_us_in_step: µs per step of 200 back-to-back steps of the "
+                         "library calls minus the same without that kernel (median of 3 rounds; "
+                         f"the full step {marg_full:.2f} µs this way), free of the launch and lost "
+                         "overlap an event-bracketed short kernel pays",
         "pages_gb200_us_per_call": PAGES_GB200_US,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
