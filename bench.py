@@ -676,13 +676,21 @@ def measure_nvfp4(x, dev, peak: float, frac_key: str, samples: int = 256, steps:
     for e in evs:
         step(e)
     torch.cuda.synchronize()
+
+    class _Reset:  # the tensor-amax reset as a call of the amax phase
+        def call(self, s):
+            with torch.cuda.stream(s):
+                at.zero_()
+
+    marg, marg_full = marginal_costs([[_Reset(), amax], [scales], [cast]], stream)
     nb = nvfp4_algorithmic_bytes(ROWS * COLS)
     step_bytes = sum(nb.values())
     out = {"workload": "16384x6144 FP32 headline weight, full fragment, rowwise+columnwise NVFP4 "
                        "(E2M1, 16-value blocks with E4M3 scales, F32 tensor scale)",
            "method": f"median of {samples} in-step samples per kernel (events around each phase; "
                      "the amax phase includes the 4-byte tensor-amax reset); step: "
-                     f"{steps} back-to-back steps without events",
+                     f"{steps} back-to-back steps without events; marginal_us_in_step as for the "
+                     f"MXFP8 kernels (full step {marg_full:.2f} µs this way)",
            "us_per_step": round(step_us, 2), "algorithmic_bytes_per_step": step_bytes,
            "step_gbs": round(step_bytes / (step_us * 1e-6) / 1e9, 1),
            "step_" + frac_key: round(step_bytes / (step_us * 1e-6) / 1e9 / peak, 4)}
@@ -690,7 +698,8 @@ def measure_nvfp4(x, dev, peak: float, frac_key: str, samples: int = 256, steps:
         us = statistics.median(e[k].elapsed_time(e[k + 1]) * 1e3 for e in evs)
         gbs = nb[nm] / (us * 1e-6) / 1e9
         out[nm] = {"us_per_call": round(us, 3), "algorithmic_bytes": nb[nm], "gbs": round(gbs, 1),
-                   frac_key: round(gbs / peak, 4)}
+                   frac_key: round(gbs / peak, 4), "marginal_us_in_step": round(marg[k], 3),
+                   "marginal_gbs": round(nb[nm] / (marg[k] * 1e-6) / 1e9, 1)}
     return out
 
 
