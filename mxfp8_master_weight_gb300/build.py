@@ -23,7 +23,8 @@ LIB_NAME = "libmxfp8_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 UNITS = ["capi.cu", "amax.cu", "cast_f32.cu", "cast_bf16.cu", "cast_f32_unaligned.cu",
-         "cast_bf16_unaligned.cu", "fused_f32.cu", "fused_bf16.cu", "misc.cu", "noalloc.cu", "nvfp4.cu"]
+         "cast_bf16_unaligned.cu", "cast_bf16_unaligned_f16.cu", "fused_f32.cu", "fused_bf16.cu",
+         "misc.cu", "noalloc.cu", "nvfp4.cu"]
 
 
 def _nvcc() -> str:

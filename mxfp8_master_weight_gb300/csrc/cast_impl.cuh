@@ -302,8 +302,10 @@ cudaError_t launch_n(const CastParams* jobs, int n, const DeviceInfo& dev, cudaS
   if constexpr (N == 1 && !kShift && kDirs != kMixed) {
     if (total <= split_max_tiles(dev, MXFP8_CAST_SPLIT_TILES_PER_SM)) {  // few tiles: four warps per tile
       const unsigned grid = tile_grid(total * 4, kWarps);
-      if (jobs[0].g.cols % tile_width<T>() != 0)
-        return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 2>, grid, kThreads, 0, stream, b);
+      if constexpr (kVec) {  // the edge path stores whole words
+        if (jobs[0].g.cols % tile_width<T>() != 0)
+          return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 2>, grid, kThreads, 0, stream, b);
+      }
       return launch_kernel(k_partial_cast<T, kDirs, kShift, kVec, kModel, N, 1>, grid, kThreads, 0, stream, b);
     }
   }
@@ -339,6 +341,15 @@ cudaError_t launch(const CastParams* jobs, int n, const DeviceInfo& dev, cudaStr
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+// All launches for one input dtype T, output alignment kVec and model dtype kModel.
+template <class T, bool kVec, int kModel>
+cudaError_t launch_for_model(const CastParams* jobs, int n, bool shifted, const DeviceInfo& dev,
+                             cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  return shifted ? launch<T, true, kVec, kModel>(jobs, n, dev, stream)
+                 : launch<T, false, kVec, kModel>(jobs, n, dev, stream);
 }
 
 // All launches for one input dtype T and output alignment kVec (instantiated by that

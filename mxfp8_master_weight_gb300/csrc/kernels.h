@@ -223,6 +223,8 @@ cudaError_t launch_partial_cast_bf16(const CastParams* jobs, int n, bool shifted
                                      const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_partial_cast_bf16_unaligned(const CastParams* jobs, int n, bool shifted, int model,
                                                const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_partial_cast_bf16_unaligned_f16(const CastParams* jobs, int n, bool shifted,
+                                                  const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_fused_quantize_f32(const FusedParams* jobs, int n, bool shifted, bool vec_out,
                                       int model, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_fused_quantize_bf16(const FusedParams* jobs, int n, bool shifted,
