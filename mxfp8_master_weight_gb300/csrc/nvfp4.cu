@@ -170,10 +170,14 @@ __device__ __forceinline__ void store_col16(const Nvfp4AmaxParams& p, int64_t ba
   }
 }
 
-// Whole tile inside the fragment; returns the lane's largest |x| (input-dtype bits).
+// Whole tile inside the fragment; returns the lane's largest |x| (input-dtype bits).  Rows
+// r_lo .. r_hi-1 of the tile (all 32, or a quarter when four warps share it); the column
+// maxima are stored, or -- colpart != nullptr, a quarter lies inside one 16-row half --
+// that half's maxima are left in *colpart for the warps to combine.
 template <class T, bool kCol, int kS>
 __device__ __forceinline__ uint32_t amax_tile_fast(const Nvfp4AmaxParams& p, int64_t row0,
-                                                   int64_t col0, int lane) {
+                                                   int64_t col0, int lane, int r_lo = 0,
+                                                   int r_hi = 32, uint4* colpart = nullptr) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
@@ -183,7 +187,7 @@ __device__ __forceinline__ uint32_t amax_tile_fast(const Nvfp4AmaxParams& p, int
   uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
   uint32_t tmax = 0;
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += kRowBatch) {
+  for (int rb = r_lo; rb < r_hi; rb += kRowBatch) {
     uint4 v[kRowBatch];
     load_rows<kRowBatch, kS, false, kS != 0>(v, src + rb * row_bytes, row_bytes, lane);
 #pragma unroll
@@ -198,17 +202,40 @@ __device__ __forceinline__ uint32_t amax_tile_fast(const Nvfp4AmaxParams& p, int
     }
   }
   if constexpr (kCol) {
-    store_col16<T>(p, row0 >> 4, j, c0);
-    store_col16<T>(p, (row0 >> 4) + 1, j, c1);
+    if (colpart != nullptr) {
+      *colpart = r_lo < 16 ? c0 : c1;
+    } else {
+      store_col16<T>(p, row0 >> 4, j, c0);
+      store_col16<T>(p, (row0 >> 4) + 1, j, c1);
+    }
   }
   return tmax;
 }
 
 // Tile cut by the fragment boundary or the matrix edge: predicated loads; only blocks
 // that meet the fragment are written.
-template <class T, bool kCol>
+// Column maxima of 16-row half h of a cut tile: only the columns whose block meets the
+// fragment.
+template <class T>
+__device__ __forceinline__ void store_col16_masked(const Nvfp4AmaxParams& p, int64_t row0, int64_t j,
+                                                   int h, const uint4& cm) {
+  const FragGeom& g = p.g;
+  const int64_t ra = row0 + 16 * h;
+  if (ra >= g.rows) return;
+  const int64_t re = min(ra + 16, g.rows);
+#pragma unroll
+  for (int k = 0; k < T::V; ++k) {
+    const int64_t col = j + k;
+    if (col < g.cols && column_meets(g, col, ra, re))
+      p.amax_c[(ra >> 4) * p.ld_c + col] = __uint_as_float(f32_bits<T>(chunk_get<T>(cm, k)));
+  }
+}
+
+// MB: rows per batch of predicated loads (a split tile's warp takes its 8 rows at once).
+template <class T, bool kCol, int MB = kMaskBatch>
 __device__ __forceinline__ uint32_t amax_tile_masked(const Nvfp4AmaxParams& p, int64_t row0,
-                                                     int64_t col0, int lane) {
+                                                     int64_t col0, int lane, int r_lo = 0,
+                                                     int r_hi = 32, uint4* colpart = nullptr) {
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
   const bool writer = (lane % lanes16<T>()) == 0;
@@ -216,11 +243,11 @@ __device__ __forceinline__ uint32_t amax_tile_masked(const Nvfp4AmaxParams& p, i
   uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
   uint32_t tmax = 0;
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += kMaskBatch) {  // warp-uniform: the butterflies stay converged
-    uint4 v[kMaskBatch];
-    load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
+  for (int rb = r_lo; rb < r_hi; rb += MB) {  // warp-uniform: the butterflies stay converged
+    uint4 v[MB];
+    load_rows_masked<T, MB>(v, g, p.in, row0 + rb, j);
 #pragma unroll
-    for (int r = 0; r < kMaskBatch; ++r) {
+    for (int r = 0; r < MB; ++r) {
       const uint4 a = chunk_abs<T>(v[r]);
       if constexpr (kCol) {
         if (rb < 16) c0 = chunk_max<T>(c0, a); else c1 = chunk_max<T>(c1, a);
@@ -233,24 +260,20 @@ __device__ __forceinline__ uint32_t amax_tile_masked(const Nvfp4AmaxParams& p, i
     }
   }
   if constexpr (kCol) {
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int64_t ra = row0 + 16 * h;
-      if (ra >= g.rows) break;
-      const int64_t re = min(ra + 16, g.rows);
-      const uint4& cm = h ? c1 : c0;
-#pragma unroll
-      for (int k = 0; k < T::V; ++k) {
-        const int64_t col = j + k;
-        if (col < g.cols && column_meets(g, col, ra, re))
-          p.amax_c[(ra >> 4) * p.ld_c + col] = __uint_as_float(f32_bits<T>(chunk_get<T>(cm, k)));
-      }
+    if (colpart != nullptr) {
+      *colpart = r_lo < 16 ? c0 : c1;
+    } else {
+      store_col16_masked<T>(p, row0, j, 0, c0);
+      store_col16_masked<T>(p, row0, j, 1, c1);
     }
   }
   return tmax;
 }
 
-template <class T, bool kCol, bool kShift>
+// kSplit: four warps share each tile, 8 rows each (a block's eight warps take two tiles);
+// the two warps of each 16-row half combine their column maxima in shared memory.  For
+// launches of few tiles, whose time is one warp's chain of row batches.
+template <class T, bool kCol, bool kShift, bool kSplit>
 __global__ void __launch_bounds__(kThreads, kAmaxMinBlocks) k_nvfp4_amax(
     const __grid_constant__ JobBatch<Nvfp4AmaxParams, 1> b) {
   __shared__ uint32_t block_max;
@@ -259,24 +282,61 @@ __global__ void __launch_bounds__(kThreads, kAmaxMinBlocks) k_nvfp4_amax(
   __syncthreads();
   constexpr int TW = tile_width<T>();
   const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
   const Nvfp4AmaxParams& p = b.job[0];
   const int64_t total = b.prefix_a[1] + b.prefix_b[1];
-  const int64_t stride = int64_t(gridDim.x) * kWarps;
   uint32_t wmax = 0;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
-    int64_t row0, col0;
-    batch_tile(b, t, TW, row0, col0);
-    const int kind = classify_tile<T>(p.g, row0, col0, TW);
-    if (kind == kTileFast) {
-      if constexpr (kShift) {
-        with_shift<T>(p.g.shift, [&](auto s) {
-          wmax = max(wmax, amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane));
-        });
-      } else {
-        wmax = max(wmax, amax_tile_fast<T, kCol, 0>(p, row0, col0, lane));
+  if constexpr (!kSplit) {
+    const int64_t stride = int64_t(gridDim.x) * kWarps;
+    for (int64_t t = int64_t(blockIdx.x) * kWarps + warp; t < total; t += stride) {
+      int64_t row0, col0;
+      batch_tile(b, t, TW, row0, col0);
+      const int kind = classify_tile<T>(p.g, row0, col0, TW);
+      if (kind == kTileFast) {
+        if constexpr (kShift) {
+          with_shift<T>(p.g.shift, [&](auto s) {
+            wmax = max(wmax, amax_tile_fast<T, kCol, decltype(s)::value>(p, row0, col0, lane));
+          });
+        } else {
+          wmax = max(wmax, amax_tile_fast<T, kCol, 0>(p, row0, col0, lane));
+        }
+      } else if (kind == kTileMasked) {
+        wmax = max(wmax, amax_tile_masked<T, kCol>(p, row0, col0, lane));
       }
-    } else if (kind == kTileMasked) {
-      wmax = max(wmax, amax_tile_masked<T, kCol>(p, row0, col0, lane));
+    }
+  } else {
+    static_assert(!kShift, "the split kernel serves aligned fragments");
+    __shared__ uint4 part[kWarps][32];
+    const int q = warp & 3;  // quarter: rows 8q .. 8q+7, in 16-row half q / 2
+    // block-uniform rounds (every warp reaches every barrier); warp w of a round takes
+    // quarter w % 4 of tile (round * 8 + w) / 4
+    for (int64_t base = int64_t(blockIdx.x) * kWarps; base < total * 4; base += int64_t(gridDim.x) * kWarps) {
+      const int64_t t = (base + warp) >> 2;
+      int kind = kTileSkip;
+      int64_t row0 = 0, col0 = 0;
+      if (t < total) {
+        batch_tile(b, t, TW, row0, col0);
+        kind = classify_tile<T>(p.g, row0, col0, TW);
+        uint4* cp = kCol ? &part[warp][lane] : nullptr;
+        if (kind == kTileFast) {
+          wmax = max(wmax, amax_tile_fast<T, kCol, 0>(p, row0, col0, lane, 8 * q, 8 * q + 8, cp));
+        } else if (kind == kTileMasked) {
+          wmax = max(wmax, amax_tile_masked<T, kCol, 8>(p, row0, col0, lane, 8 * q, 8 * q + 8, cp));
+        }
+      }
+      if constexpr (kCol) {
+        __syncthreads();
+        if ((q & 1) == 0 && kind != kTileSkip) {  // quarters 0 and 2 combine their half
+          const uint4 cm = chunk_max<T>(part[warp][lane], part[warp + 1][lane]);
+          const int64_t j = col0 + lane * T::V;
+          if (kind == kTileFast) {
+            store_col16<T>(p, (row0 >> 4) + (q >> 1), j, cm);
+          } else {
+            store_col16_masked<T>(p, row0, j, q >> 1, cm);
+          }
+        }
+        __syncthreads();
+      }
     }
   }
   wmax = warp_max(f32_bits<T>(wmax));
@@ -330,7 +390,8 @@ __global__ void __launch_bounds__(kThreads, kScaleBlocksPerSM) k_nvfp4_scales(
 // Whole tile inside the fragment: 16-byte loads, the row's multiplier from the table.
 template <class T, bool kCol, int kS>
 __device__ __forceinline__ void cast_tile_fast(const Nvfp4CastParams& p, const float* mult,
-                                               int64_t row0, int64_t col0, int lane) {
+                                               int64_t row0, int64_t col0, int lane,
+                                               int r_lo = 0, int r_hi = 32) {
   const int64_t cols = p.g.cols;
   const int64_t j = col0 + lane * T::V;
   const char* src = static_cast<const char*>(p.in) + (row0 * cols + j - p.g.start) * T::kBytes;
@@ -350,7 +411,7 @@ __device__ __forceinline__ void cast_tile_fast(const Nvfp4CastParams& p, const f
   }
   const bool vec = p.vec_out != 0;
 #pragma unroll 1
-  for (int rb = 0; rb < 32; rb += NB) {
+  for (int rb = r_lo; rb < r_hi; rb += NB) {
     uint4 v[NB];
     uint32_t sb[NB];
 #pragma unroll
@@ -377,7 +438,8 @@ __device__ __forceinline__ void cast_tile_fast(const Nvfp4CastParams& p, const f
 // bytes only.
 template <class T, bool kCol>
 __device__ __forceinline__ void cast_tile_masked(const Nvfp4CastParams& p, const float* mult,
-                                                 int64_t row0, int64_t col0, int lane) {
+                                                 int64_t row0, int64_t col0, int lane,
+                                                 int r_lo = 0, int r_hi = 32) {
   constexpr uint64_t kChunkBits = (uint64_t(1) << T::V) - 1;
   const FragGeom& g = p.g;
   const int64_t j = col0 + lane * T::V;
@@ -393,7 +455,7 @@ __device__ __forceinline__ void cast_tile_masked(const Nvfp4CastParams& p, const
     }
   }
 #pragma unroll 1
-  for (int rb = 0; rb < 32 && row0 + rb < g.rows; rb += kMaskBatch) {
+  for (int rb = r_lo; rb < r_hi && row0 + rb < g.rows; rb += kMaskBatch) {
     uint4 v[kMaskBatch];
     const uint64_t valid = load_rows_masked<T, kMaskBatch>(v, g, p.in, row0 + rb, j);
     if (valid == 0) continue;
@@ -428,7 +490,9 @@ __device__ __forceinline__ void cast_tile_masked(const Nvfp4CastParams& p, const
   }
 }
 
-template <class T, bool kCol, bool kShift>
+// kSplit: four warps per tile, 8 rows each (no exchange between them), for launches of
+// few tiles.
+template <class T, bool kCol, bool kShift, bool kSplit>
 __global__ void __launch_bounds__(kThreads, kCastMinBlocks) k_nvfp4_cast(
     const __grid_constant__ JobBatch<Nvfp4CastParams, 1> b) {
   __shared__ float mult[256];
@@ -443,69 +507,83 @@ __global__ void __launch_bounds__(kThreads, kCastMinBlocks) k_nvfp4_cast(
   }
   __syncthreads();
   constexpr int TW = tile_width<T>();
+  constexpr int kParts = kSplit ? 4 : 1;
   const int lane = threadIdx.x & 31;
-  const int64_t total = b.prefix_a[1] + b.prefix_b[1];
+  const int64_t total = (b.prefix_a[1] + b.prefix_b[1]) * kParts;
   const int64_t stride = int64_t(gridDim.x) * kWarps;
-  for (int64_t t = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); t < total; t += stride) {
+  for (int64_t u = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5); u < total; u += stride) {
+    const int64_t t = kSplit ? u >> 2 : u;
+    const int r_lo = kSplit ? 8 * int(u & 3) : 0, r_hi = kSplit ? r_lo + 8 : 32;
     int64_t row0, col0;
     batch_tile(b, t, TW, row0, col0);
     const int kind = classify_tile<T>(p.g, row0, col0, TW);
     if (kind == kTileFast) {
       if constexpr (kShift) {
         with_shift<T>(p.g.shift, [&](auto s) {
-          cast_tile_fast<T, kCol, decltype(s)::value>(p, mult, row0, col0, lane);
+          cast_tile_fast<T, kCol, decltype(s)::value>(p, mult, row0, col0, lane, r_lo, r_hi);
         });
       } else {
-        cast_tile_fast<T, kCol, 0>(p, mult, row0, col0, lane);
+        cast_tile_fast<T, kCol, 0>(p, mult, row0, col0, lane, r_lo, r_hi);
       }
     } else if (kind == kTileMasked) {
-      cast_tile_masked<T, kCol>(p, mult, row0, col0, lane);
+      cast_tile_masked<T, kCol>(p, mult, row0, col0, lane, r_lo, r_hi);
     }
   }
 }
 
+// Few tiles (at most the MXFP8 amax kernel's per-SM threshold): the split kernels.
 template <class T, bool kCol, bool kShift>
-cudaError_t launch_amax(const Nvfp4AmaxParams& p, cudaStream_t stream) {
+cudaError_t launch_amax(const Nvfp4AmaxParams& p, const DeviceInfo& dev, cudaStream_t stream) {
   JobBatch<Nvfp4AmaxParams, 1> b;
   const int64_t total = fill_batch(b, &p, 1);
   if (total == 0) return cudaSuccess;
-  return launch_kernel(k_nvfp4_amax<T, kCol, kShift>, tile_grid(total, kWarps), kThreads, 0, stream, b);
+  if constexpr (!kShift) {
+    if (total <= split_max_tiles(dev, MXFP8_AMAX_SPLIT_TILES_PER_SM))
+      return launch_kernel(k_nvfp4_amax<T, kCol, kShift, true>, tile_grid(total * 4, kWarps), kThreads, 0,
+                           stream, b);
+  }
+  return launch_kernel(k_nvfp4_amax<T, kCol, kShift, false>, tile_grid(total, kWarps), kThreads, 0, stream, b);
 }
 
 template <class T, bool kCol, bool kShift>
-cudaError_t launch_cast(const Nvfp4CastParams& p, cudaStream_t stream) {
+cudaError_t launch_cast(const Nvfp4CastParams& p, const DeviceInfo& dev, cudaStream_t stream) {
   JobBatch<Nvfp4CastParams, 1> b;
   const int64_t total = fill_batch(b, &p, 1);
   if (total == 0) return cudaSuccess;
-  return launch_kernel(k_nvfp4_cast<T, kCol, kShift>, tile_grid(total, kWarps), kThreads, 0, stream, b);
+  if constexpr (!kShift) {
+    // the MXFP8 amax threshold: split measured slower on the 4096x4096 FP32 cast (4096
+    // tiles, 14.1 -> 16.6 us), which the MXFP8 cast's threshold would split
+    if (total <= split_max_tiles(dev, MXFP8_AMAX_SPLIT_TILES_PER_SM))
+      return launch_kernel(k_nvfp4_cast<T, kCol, kShift, true>, tile_grid(total * 4, kWarps), kThreads, 0,
+                           stream, b);
+  }
+  return launch_kernel(k_nvfp4_cast<T, kCol, kShift, false>, tile_grid(total, kWarps), kThreads, 0, stream, b);
 }
 
 template <class T>
-cudaError_t amax_for(const Nvfp4AmaxParams& p, bool shifted, cudaStream_t stream) {
+cudaError_t amax_for(const Nvfp4AmaxParams& p, bool shifted, const DeviceInfo& dev, cudaStream_t stream) {
   const bool col = p.amax_c != nullptr;
-  if (shifted) return col ? launch_amax<T, true, true>(p, stream) : launch_amax<T, false, true>(p, stream);
-  return col ? launch_amax<T, true, false>(p, stream) : launch_amax<T, false, false>(p, stream);
+  if (shifted) return col ? launch_amax<T, true, true>(p, dev, stream) : launch_amax<T, false, true>(p, dev, stream);
+  return col ? launch_amax<T, true, false>(p, dev, stream) : launch_amax<T, false, false>(p, dev, stream);
 }
 
 template <class T>
-cudaError_t cast_for(const Nvfp4CastParams& p, bool shifted, cudaStream_t stream) {
+cudaError_t cast_for(const Nvfp4CastParams& p, bool shifted, const DeviceInfo& dev, cudaStream_t stream) {
   const bool col = p.out_c != nullptr;
-  if (shifted) return col ? launch_cast<T, true, true>(p, stream) : launch_cast<T, false, true>(p, stream);
-  return col ? launch_cast<T, true, false>(p, stream) : launch_cast<T, false, false>(p, stream);
+  if (shifted) return col ? launch_cast<T, true, true>(p, dev, stream) : launch_cast<T, false, true>(p, dev, stream);
+  return col ? launch_cast<T, true, false>(p, dev, stream) : launch_cast<T, false, false>(p, dev, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_nvfp4_amax(const Nvfp4AmaxParams& p, int dtype, bool shifted,
                               const DeviceInfo& dev, cudaStream_t stream) {
-  (void)dev;
-  return dtype == 0 ? amax_for<F32T>(p, shifted, stream) : amax_for<BF16T>(p, shifted, stream);
+  return dtype == 0 ? amax_for<F32T>(p, shifted, dev, stream) : amax_for<BF16T>(p, shifted, dev, stream);
 }
 
 cudaError_t launch_nvfp4_cast(const Nvfp4CastParams& p, int dtype, bool shifted,
                               const DeviceInfo& dev, cudaStream_t stream) {
-  (void)dev;
-  return dtype == 0 ? cast_for<F32T>(p, shifted, stream) : cast_for<BF16T>(p, shifted, stream);
+  return dtype == 0 ? cast_for<F32T>(p, shifted, dev, stream) : cast_for<BF16T>(p, shifted, dev, stream);
 }
 
 cudaError_t launch_nvfp4_scales(const Nvfp4ScaleParams& p, const DeviceInfo& dev,
