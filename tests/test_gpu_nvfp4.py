@@ -318,3 +318,23 @@ def test_scale_update_every_mantissa_and_edge_values():
             raise AssertionError(f"g={g}: {bad.size} mismatches, first amax {v!r} "
                                  f"({np.float32(v).view(np.uint32):#x}): gpu {got.reshape(-1)[bad[0]]:#x} "
                                  f"oracle {want.reshape(-1)[bad[0]]:#x}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(64, 256), (96, 200), (40, 96), (160, 96)])
+def test_small_launches_split_kernels(dtype, rows, cols):
+    """Launches of few tiles run the split NVFP4 kernels (four warps per tile; the amax
+    combines each 16-row half's column maxima across two warps): whole and partial (even)
+    fragments, both direction sets, aligned and realigning buffers, against the oracle."""
+    rng = np.random.default_rng(rows * 7 + cols + (dtype == "bf16"))
+    n = rows * cols
+    x = wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-3, 3, n).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    for start, length in [(0, n), (2 * cols + 6, n - 2 * cols - 40), (16 * cols, 8 * cols)]:
+        frag = np.ascontiguousarray(x[start:start + length])
+        for colwise in (True, False):
+            for shift in (0, 2):
+                got = gpu_nvfp4(frag, rows, cols, start, colwise, shift=shift)
+                want = oracle_nvfp4(frag, rows, cols, start, colwise)
+                assert_same(got, want, f"{dtype} {rows}x{cols} [{start},+{length}) col={colwise} shift={shift}")

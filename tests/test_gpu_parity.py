@@ -301,3 +301,30 @@ def test_tiles_cut_by_the_right_edge(dtype, rows, cols):
             got = gpu_fragment(frag, rows, cols, start, colwise, amax_fill=0.125)
             want = oracle_fragment(frag, rows, cols, start, colwise, amax_fill=0.125)
             assert_bitwise(got, want, f"{dtype} {rows}x{cols} [{start},{start + length}) colwise={colwise}")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("rows,cols", [(64, 256), (96, 200), (40, 96), (128, 512)])
+def test_small_launches_every_path(dtype, rows, cols):
+    """Launches of few tiles run the split kernels (four warps per tile; with right-edge
+    tiles when the width is not a multiple of the tile's): whole and partial fragments,
+    bidirectional and row-only, full-size and fragment-sized outputs (word-aligned or not),
+    fragment buffers aligned and realigning (the realigning ones take the whole-tile kernels),
+    BF16 and FP16 model dtypes -- every combination against the oracle."""
+    rng = np.random.default_rng(rows * 101 + cols + (dtype == "bf16"))
+    n = rows * cols
+    x = wl.normal_f32(rng, n) * np.float32(10.0) ** rng.uniform(-3, 3, n).astype(np.float32)
+    if dtype == "bf16":
+        x = wl.truncate_to_bf16_bits(x)
+    frags = [(0, n), (cols * 33 + 5, n - cols * 33 - 40), (3 * cols, 2 * cols)]
+    for start, length in frags:
+        frag = np.ascontiguousarray(x[start:start + length])
+        for colwise in (True, False):
+            for out_offset in (start, 0, 3):
+                for shift in (0, 1):
+                    for model in ("bf16", "f16"):
+                        kw = dict(out_offset=out_offset, amax_fill=0.25, model=model)
+                        got = gpu_fragment(frag, rows, cols, start, colwise, shift=shift, **kw)
+                        want = oracle_fragment(frag, rows, cols, start, colwise, **kw)
+                        assert_bitwise(got, want, f"{dtype} {rows}x{cols} [{start},+{length}) col={colwise} "
+                                                  f"out={out_offset} shift={shift} model={model}")
