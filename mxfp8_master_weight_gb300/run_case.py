@@ -9,6 +9,8 @@ Cases (seeded synthetic inputs of the workloads module):
   sharded     the config-5 batch in four emulated shards (dimensions divided by --scale):
               batched amax -> ranged reduction + scales -> batched cast
   nvfp4       the 16384x6144 FP32 weight through the NVFP4 amax, scale update and cast
+  small       the 160x96 FP32 weight (config 1), one full fragment: amax -> scales -> cast
+              (a launch of five tiles: the split kernels)
 
 Every call runs the whole case; nothing is skipped.  The outputs are not checked here
 (the tests check them against the oracle).  One untimed call comes first (it marshals the
@@ -77,7 +79,29 @@ def case_nvfp4(dev, scale):
     return run
 
 
-CASES = {"step": case_step, "one_pass": case_one_pass, "sharded": case_sharded, "nvfp4": case_nvfp4}
+def case_small(dev, scale):
+    w = wl.cfg1_tiny()
+    rows, cols = w.rows, w.cols
+    x = torch.from_numpy(w.data).to(dev)
+    (rr, rc), (cr, cc) = api.block_shapes(rows, cols)
+    ar = torch.zeros((rr, rc), device=dev)
+    ac = torch.zeros((cr, cc), device=dev)
+    sr = torch.empty((rr, rc), dtype=torch.uint8, device=dev)
+    scl = torch.empty((cr, cc), dtype=torch.uint8, device=dev)
+    qr = torch.empty(rows * cols, dtype=torch.uint8, device=dev)
+    qc = torch.empty(rows * cols, dtype=torch.uint8, device=dev)
+    calls = [api.prepare_partial_amax(x, ar, ac, rows, cols, 0),
+             api.prepare_update_scales(ar, ac, sr, scl, rows, cols),
+             api.prepare_partial_cast(x, sr, scl, qr, qc, rows, cols, 0)]
+
+    def run():
+        for c in calls:
+            c.call()
+    return run
+
+
+CASES = {"step": case_step, "one_pass": case_one_pass, "sharded": case_sharded, "nvfp4": case_nvfp4,
+         "small": case_small}
 
 
 def main(argv=None):
